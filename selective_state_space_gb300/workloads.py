@@ -1,0 +1,135 @@
+"""Seeded synthetic workloads for the SSD forward pass.
+
+This module only draws random inputs; it holds none of the method's
+arithmetic.  Both the GPU path and the CPU oracle consume the tensors it
+returns, so both sides see exactly the same (already rounded) values.
+
+Shapes follow the benchmark shapes of the cuTile Mamba-2 blog (section
+"Mamba-2 forward benchmark": ``Mamba2ProblemSpec(batch_size, num_tokens,
+num_groups, num_heads, state_size, head_size, chunk_size, dtype,
+state_dtype)``) and five named layer shapes used throughout this library.
+
+Draw order for one workload, from a single CPU ``torch.Generator`` seeded
+with the workload seed, every draw in float32 and then cast to the input
+dtype: x, B, C, dt (or its pre-activation), A, D, h0, the dt-zero mask.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Shape:
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int       # H, the per-head value width (x, y)
+    dstate: int        # S, the state width (B, C)
+    ngroups: int
+    chunk: int
+    dtype: str         # "f32" or "bf16": dtype of x, dt, B, C and y
+    dt_recipe: str     # "loguniform" (exp(U(log 1e-3, log 1e-1))) or "softplus" (softplus(N(-4, 1)))
+    a_range: tuple     # A = -U(lo, hi)
+    d_recipe: str      # "one" or "normal" (N(1, 0.1))
+    h0_recipe: str     # "zeros", "none" or "normal" (N(0, 0.1), float32)
+    dt_zero_frac: float
+    seed: int
+
+    @property
+    def nchunks(self) -> int:
+        return (self.seqlen + self.chunk - 1) // self.chunk
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.seqlen
+
+
+# The five layer shapes, in order, plus the blog's own benchmark shape.
+WORKLOADS = [
+    Shape("tiny-f32", 1, 256, 4, 64, 64, 1, 64, "f32", "loguniform", (1.0, 16.0), "one", "zeros", 0.0, 0),
+    Shape("mamba2-130m-layer", 2, 2048, 24, 64, 128, 1, 256, "bf16", "softplus", (1.0, 16.0), "normal", "none", 0.0, 1),
+    Shape("mamba2-2.7b-layer", 4, 4096, 80, 64, 128, 1, 256, "bf16", "softplus", (1.0, 16.0), "normal", "normal", 0.0, 2),
+    Shape("long-prefill-64k", 1, 65536, 32, 64, 128, 8, 256, "bf16", "softplus", (1.0, 16.0), "normal", "none", 0.05, 3),
+    Shape("wide-state-batched", 32, 1024, 64, 128, 256, 4, 128, "bf16", "loguniform", (0.5, 8.0), "normal", "none", 0.0, 4),
+]
+BLOG_SHAPE = Shape("blog-b4-l16k", 4, 16384, 8, 64, 128, 1, 128, "bf16", "softplus", (1.0, 16.0), "normal", "none", 0.0, 5)
+
+
+def by_name(name: str) -> Shape:
+    for s in WORKLOADS + [BLOG_SHAPE]:
+        if s.name == name:
+            return s
+    raise KeyError(name)
+
+
+def custom(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype="bf16", *,
+           dt_recipe="softplus", a_range=(1.0, 16.0), d_recipe="normal", h0_recipe="none",
+           dt_zero_frac=0.0, seed=0, name="custom") -> Shape:
+    return Shape(name, batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype, dt_recipe,
+                 tuple(a_range), d_recipe, h0_recipe, dt_zero_frac, seed)
+
+
+def torch_dtype(d: str) -> torch.dtype:
+    return {"f32": torch.float32, "bf16": torch.bfloat16}[d]
+
+
+@dataclasses.dataclass
+class Inputs:
+    shape: Shape
+    x: torch.Tensor            # [B, L, nh, H]      input dtype
+    dt: torch.Tensor           # [B, L, nh]         input dtype
+    A: torch.Tensor            # [nh]               float32 (all negative)
+    B: torch.Tensor            # [B, L, G, S]       input dtype
+    C: torch.Tensor            # [B, L, G, S]       input dtype
+    D: torch.Tensor            # [nh]               float32
+    h0: Optional[torch.Tensor]  # [B, nh, H, S]     float32 or None
+
+    def tensors(self):
+        return dict(x=self.x, dt=self.dt, A=self.A, B=self.B, C=self.C, D=self.D, h0=self.h0)
+
+
+def make_inputs(shape: Shape, seed: Optional[int] = None) -> Inputs:
+    """Draw one workload on the CPU (deterministic for a given seed)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(shape.seed if seed is None else seed)
+    Bsz, L, nh, H, S, G = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    dt_ = torch_dtype(shape.dtype)
+    f32 = torch.float32
+    x = torch.randn((Bsz, L, nh, H), generator=g, dtype=f32).to(dt_)
+    scale = 1.0 / math.sqrt(S)
+    Bm = (torch.randn((Bsz, L, G, S), generator=g, dtype=f32) * scale).to(dt_)
+    Cm = (torch.randn((Bsz, L, G, S), generator=g, dtype=f32) * scale).to(dt_)
+    if shape.dt_recipe == "loguniform":
+        u = torch.rand((Bsz, L, nh), generator=g, dtype=f32)
+        lo, hi = math.log(1e-3), math.log(1e-1)
+        dt = torch.exp(lo + (hi - lo) * u)
+    elif shape.dt_recipe == "softplus":
+        dt = torch.nn.functional.softplus(torch.randn((Bsz, L, nh), generator=g, dtype=f32) - 4.0)
+    else:
+        raise ValueError(shape.dt_recipe)
+    lo, hi = shape.a_range
+    A = -(lo + (hi - lo) * torch.rand((nh,), generator=g, dtype=f32))
+    if shape.d_recipe == "one":
+        D = torch.ones((nh,), dtype=f32)
+    else:
+        D = 1.0 + 0.1 * torch.randn((nh,), generator=g, dtype=f32)
+    if shape.h0_recipe == "zeros":
+        h0 = torch.zeros((Bsz, nh, H, S), dtype=f32)
+    elif shape.h0_recipe == "normal":
+        h0 = 0.1 * torch.randn((Bsz, nh, H, S), generator=g, dtype=f32)
+    else:
+        h0 = None
+    if shape.dt_zero_frac > 0.0:
+        # exactly round(frac * L) token positions per batch row hold their state (dt = 0 for all heads)
+        nz = int(round(shape.dt_zero_frac * L))
+        for b in range(Bsz):
+            idx = torch.randperm(L, generator=g)[:nz]
+            dt[b, idx, :] = 0.0
+    dt = dt.to(dt_)
+    return Inputs(shape, x.contiguous(), dt.contiguous(), A.contiguous(), Bm.contiguous(),
+                  Cm.contiguous(), D.contiguous(), None if h0 is None else h0.contiguous())
