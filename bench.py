@@ -1,0 +1,375 @@
+"""Benchmark of the chunked SSD forward pass on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one ssd_fwd call (all four stages: chunk_cumsum, chunk_state,
+state_passing, chunk_scan) over one batch of seeded synthetic inputs already
+resident in HBM.  The headline workload is the Mamba-2-2.7B-shaped layer
+(B=4, L=4096, 80 heads, H=64, S=128, chunk 256, bf16 inputs, float32 state).
+Its inputs and outputs (367 MB) are larger than the 129 MB L2, so no L2 flush
+is done between steps.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload
+(independent problems, no collective on the data path); value = tokens of all
+ranks / max-over-ranks time.  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_gb300 import workloads  # noqa: E402
+
+METRIC = "ssd_fwd_tokens_per_s"
+UNIT = "tokens/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")
+KERNEL_SOURCES = {  # the file that holds each stage's kernels (for the traffic record's freshness check)
+    "chunk_cumsum": ["ssd_simt.cu"], "state_passing": ["ssd_simt.cu"],
+    "chunk_state": ["ssd_simt.cu", "ssd_tc.cu"], "chunk_scan": ["ssd_simt.cu", "ssd_tc.cu"],
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def esize(dtype: str) -> int:
+    return 2 if dtype == "bf16" else 4
+
+
+def stage_bytes(s: workloads.Shape):
+    """Algorithmic bytes per launch of each stage: its own compulsory inputs read
+    once and outputs written once (intermediates G, s_local, h_start count as that
+    stage's inputs/outputs), and the whole-step compulsory I/O."""
+    e = esize(s.dtype)
+    Bsz, L, nh, H, S, G, nc = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups, s.nchunks
+    x = Bsz * L * nh * H * e
+    dt = Bsz * L * nh * e
+    bc = Bsz * L * G * S * e
+    g = Bsz * nh * L * 4
+    states32 = Bsz * nh * nc * H * S * 4
+    states_in = Bsz * nh * nc * H * S * e
+    h = Bsz * nh * H * S * 4
+    h0 = h if s.h0_recipe != "none" else 0
+    y = Bsz * L * nh * H * e
+    ad = 2 * nh * 4
+    return {
+        "chunk_cumsum": dt + nh * 4 + g,
+        "chunk_state": x + dt + bc + g + states32,
+        "state_passing": states32 + (Bsz * nh * nc * 4) + h0 + states_in + h,
+        "chunk_scan": x + dt + 2 * bc + g + states_in + nh * 4 + y,
+        "step": x + dt + 2 * bc + ad + h0 + y + h,
+    }
+
+
+def alg_flops(s: workloads.Shape) -> float:
+    """Algorithmic flops of one forward pass: per (batch, chunk), per head
+    2TSH (chunk state) + 2TSH (C h^T) + 2 T(T+1)/2 H (causal intra-chunk product)
+    + 2SH (state pass), plus per group 2 T(T+1)/2 S (C B^T, lower triangle)."""
+    T, S, H = s.chunk, s.dstate, s.headdim
+    per_head = 4 * T * S * H + T * (T + 1) * H + 2 * S * H
+    per_group = T * (T + 1) * S
+    return float(s.batch * s.nchunks * (s.nheads * per_head + s.ngroups * per_group))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ssd_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def traffic_record(stage: str, shape_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is
+    unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(shape_name, {}).get(stage)
+    if not ent:
+        return None
+    h = hashlib.sha256()
+    for fn in KERNEL_SOURCES[stage]:
+        with open(os.path.join(ROOT, "selective_state_space_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    if ent.get("source_sha256") != h.hexdigest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def _head_windows(s, width):
+    """(batch, lo, hi) head windows whose heads keep their B/C group mapping when
+    cut out as a sub-problem: inside one group, or whole groups."""
+    hpg = s.nheads // s.ngroups
+    if hpg >= width:
+        step = width
+    else:
+        step = max(1, width // hpg) * hpg
+    for b in range(s.batch):
+        lo = 0
+        while lo < s.nheads:
+            hi = min(s.nheads, lo + step)
+            if hpg >= width:     # stay inside one group
+                hi = min(hi, (lo // hpg + 1) * hpg)
+            yield b, lo, hi
+            lo = hi
+
+
+def cpu_baseline(inp, budget_s: float):
+    """The oracle as it stands, timed on a bounded sample of (batch, head) pairs at
+    full sequence length, with every core this process may use."""
+    import oracle
+    s = inp.shape
+    cores = oracle.default_threads()
+    hpg = s.nheads // s.ngroups
+    done, t0 = 0, time.perf_counter()
+    for b, lo, hi in _head_windows(s, cores):
+        glo, ghi = lo // hpg, (hi - 1) // hpg + 1
+        oracle.ssd_fwd_seq(inp.x[b:b + 1, :, lo:hi], inp.dt[b:b + 1, :, lo:hi], inp.A[lo:hi],
+                           inp.B[b:b + 1, :, glo:ghi], inp.C[b:b + 1, :, glo:ghi], inp.D[lo:hi],
+                           None if inp.h0 is None else inp.h0[b:b + 1, lo:hi], nthreads=cores)
+        done += hi - lo
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    tokens_equiv = done * s.seqlen / s.nheads      # (batch, head) pairs -> whole-workload tokens
+    return {"value": tokens_equiv / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {s.batch * s.nheads} (batch, head) pairs at full length L={s.seqlen}, "
+                      f"sequential float64 recurrence, {el:.1f} s; tokens/s scaled to the whole workload"}
+
+
+def run_reference(args, shape):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = workloads.make_inputs(shape)
+    import oracle
+    oracle.build()
+    per_step = max(1.0, args.ref_step_s)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(inp, per_step)
+        if i >= args.warmup:
+            vals.append(r)
+    tok = statistics.median(v["value"] for v in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": tok, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": shape.tokens / tok * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(shape),
+            "cpu_baseline": {"value": tok, "unit": UNIT, "cores": vals[0]["cores"], "kind": "oracle",
+                             "sample": vals[0]["sample"]},
+            "e2e": {"value": tok, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(shape):
+    return {"workload": shape.name, "batch": shape.batch, "seqlen": shape.seqlen, "nheads": shape.nheads,
+            "headdim": shape.headdim, "dstate": shape.dstate, "ngroups": shape.ngroups, "chunk": shape.chunk,
+            "input_dtype": shape.dtype, "state_dtype": "f32",
+            "l2": "no flush: compulsory I/O per step exceeds the 129 MB L2"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mamba2-2.7b-layer")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--ref-step-s", type=float, default=2.0)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    shape = workloads.by_name(args.workload)
+    if args.impl == "reference":
+        run_reference(args, shape)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    from selective_state_space_gb300 import api
+    from selective_state_space_gb300.build import build
+    build()
+    inp = workloads.make_inputs(shape)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.tensors().items()}
+    desc = api.desc_for(d["x"], d["B"], shape.chunk)
+    tc = api.uses_tensor_cores(desc)
+    ws = api.alloc_workspace(desc, dev)
+    y = torch.empty_like(d["x"])
+    hf = torch.empty((shape.batch, shape.nheads, shape.headdim, shape.dstate), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        api.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], shape.chunk, d["h0"], y=y, h_final=hf,
+                    workspace=ws, stream=stream, events=events)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(ev[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    stage_ms = {st: statistics.mean(ev[i][2 * j].elapsed_time(ev[i][2 * j + 1]) for i in range(args.steps))
+                for j, st in enumerate(STAGES)}
+
+    # end to end through the public API: pinned host inputs -> device -> ssd_fwd -> host outputs
+    host = {k: (None if v is None else v.pin_memory()) for k, v in inp.tensors().items()}
+    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    hf_host = torch.empty(hf.shape, dtype=hf.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = y_host.numel() * y_host.element_size() + hf_host.numel() * hf_host.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            if v is not None:
+                d[k].copy_(v, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+        hf_host.copy_(hf, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_kind = load_peaks()
+    sb = stage_bytes(shape)
+    top = max(STAGES, key=lambda s_: stage_ms[s_])
+    achieved = sb[top] / (stage_ms[top] * 1e-3) / 1e9
+    # a kernel timed inside a long step: burst copy bandwidth is the only HBM figure measured
+    peak = float(peaks["hbm_gbs"])
+    tokens_per_s = world * shape.tokens / (ms_per_step * 1e-3)
+    flops = alg_flops(shape)
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if tc else ("f32" if shape.dtype == "f32" else "f32 (bf16 inputs)"),
+        "data": "synthetic", "config": dict(config_of(shape), parallelism=f"replicas{world}",
+                                            tensor_cores=tc),
+        "tflops": flops / (ms_per_step * 1e-3) / 1e12,
+        "roofline": {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "alg_bytes_per_launch": sb[top], "traffic": traffic_record(top, shape.name)},
+        "step_roofline": {"alg_bytes": sb["step"], "alg_flops": flops,
+                          "roofline_ms": max(sb["step"] / (peak * 1e9), flops / (float(peaks["bf16_tflops"]) * 1e12)) * 1e3,
+                          "frac": max(sb["step"] / (peak * 1e9), flops / (float(peaks["bf16_tflops"]) * 1e12)) * 1e3 / ms_per_step},
+        "stages_ms": stage_ms,
+        "stages_gbs": {s_: sb[s_] / (stage_ms[s_] * 1e-3) / 1e9 for s_ in STAGES},
+        "e2e": {"value": world * shape.tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_budget_s)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

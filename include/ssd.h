@@ -1,0 +1,164 @@
+/*
+ * ssd.h -- C ABI of libssd.so: the Mamba-2 selective-state-space (SSD) forward
+ * pass in chunked form and its single-token recurrent decode, on one GPU.
+ *
+ * The method is the one described in the NVIDIA developer blog "Accelerating
+ * Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA CUDA Tile":
+ *
+ *   section "Mamba-2 architecture":
+ *     h_t = exp(A dt_t) h_{t-1} + dt_t B_t x_t^T,      y_t = c_t^T h_t + D x_t
+ *     G   = in-chunk cumsum of a_t = A dt_t
+ *     h_{k+1} = exp(G_last) h_k + (exp(G_last - G) o b)^T X           (b = dt o B)
+ *     Y_k     = exp(G) o (C h_k) + (exp(G - G^T) o (C B^T) o M) (dt o X) + D X
+ *   sections "Kernel 1" .. "Kernel 3": the three stages chunk_cumsum,
+ *   fwd_pass_state (split here into chunk_state + state_passing) and
+ *   compute_out (here chunk_scan).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All pointers are DEVICE pointers unless stated otherwise.  Every tensor is
+ *    dense and row-major ("contiguous") in the layout given below.
+ *  - The caller owns every buffer, the workspace included.  The library never
+ *    allocates or frees device memory and keeps no state between calls.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
+ *    the legacy default stream).  A return of SSD_OK means the work was
+ *    enqueued; errors in the kernels themselves surface on the stream.
+ *  - Arguments are validated before anything is enqueued: every error other
+ *    than SSD_ERR_CUDA means nothing was launched and no buffer was touched.
+ *  - Symbols:  B batch, L seqlen, nh heads, H headdim, S dstate, G ngroups,
+ *    T chunk, nc = ceil(L / T).  Head h reads B/C group h / (nh / G).
+ *
+ * Tensor layouts (dtype "in" = desc.in_dtype, "out" = desc.out_dtype):
+ *    x   [B][L][nh][H]   in        y       [B][L][nh][H]  out
+ *    dt  [B][L][nh]      in        A, D    [nh]           float32
+ *    Bm  [B][L][G][S]    in        Cm      [B][L][G][S]   in
+ *    h0, h_final [B][nh][H][S] float32  (state of head h: row p < H, column s < S)
+ *  dt must already be the positive step (any softplus or bias applied by the
+ *  caller); A must be negative for the usual decaying model (not enforced).
+ */
+#ifndef SSD_H_
+#define SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ssd_stream_t;   /* identical to cudaStream_t */
+typedef struct CUevent_st *ssd_event_t;     /* identical to cudaEvent_t  */
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, negative size, bad dtype, G does not divide nh */
+    SSD_ERR_UNSUPPORTED = 2,  /* well-formed problem outside what this build handles (see limits below) */
+    SSD_ERR_WORKSPACE = 3,    /* workspace NULL, smaller than ssd_fwd_workspace_size, or not 256-B aligned */
+    SSD_ERR_CUDA = 4          /* a CUDA runtime call or a kernel launch failed; call cudaGetLastError */
+} ssd_status;
+
+/* Problem description.  Mirrors the blog's Mamba2ProblemSpec(batch_size,
+ * num_tokens, num_groups, num_heads, state_size, head_size, chunk_size, dtype,
+ * state_dtype) (section "Mamba-2 forward benchmark"); the state dtype is
+ * always float32 here. */
+typedef struct {
+    int64_t batch;      /* B  >= 0 */
+    int64_t seqlen;     /* L  >= 0 (0: y is empty, h_final = h0 or zeros) */
+    int64_t nheads;     /* nh >= 0, a multiple of ngroups */
+    int64_t headdim;    /* H  in [1, 1024] */
+    int64_t dstate;     /* S  in [1, 256] */
+    int64_t ngroups;    /* G  >= 1 */
+    int64_t chunk;      /* T  in [1, 1024]; any L is accepted (the last chunk may be short) */
+    int32_t in_dtype;   /* ssd_dtype of x, dt, Bm, Cm */
+    int32_t out_dtype;  /* ssd_dtype of y */
+    int32_t flags;      /* SSD_FLAG_* bits, 0 by default */
+    int32_t reserved;   /* must be 0 */
+} ssd_desc;
+
+/* Use the CUDA-core kernels for every stage even where tensor-core kernels
+ * exist for the shape (both are GPU code; this exists for cross-checking). */
+#define SSD_FLAG_FORCE_SIMT 1
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *ssd_status_string(ssd_status s);
+
+/* Bytes of device workspace ssd_fwd needs for `desc` (written to *bytes).
+ * The workspace holds the in-chunk cumsum G, the local chunk states and the
+ * chunk-start states.  Errors: SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED. */
+ssd_status ssd_fwd_workspace_size(const ssd_desc *desc, size_t *bytes);
+
+/* Whether ssd_fwd runs its chunk_state and chunk_scan stages on the tensor
+ * cores (tcgen05) for `desc` (*uses_tensor_cores = 1) or on the CUDA cores
+ * (0).  Both are GPU code; the choice depends only on the shape, the dtypes
+ * and desc.flags. */
+ssd_status ssd_fwd_path(const ssd_desc *desc, int32_t *uses_tensor_cores);
+
+/* Chunked SSD forward pass: y = SSD(x, dt, A, Bm, Cm, D; h0) and the state
+ * after the last token (blog section "Mamba-2 architecture", the chunk jump
+ * and chunk output; the stages of sections "Kernel 1".."Kernel 3").
+ *   h0       nullable: NULL means a zero initial state.
+ *   h_final  nullable: NULL means the final state is not written.
+ *   workspace, ws_bytes: device scratch of at least ssd_fwd_workspace_size()
+ *            bytes, 256-byte aligned, owned by the caller; its contents on
+ *            entry are ignored and on exit are unspecified.
+ * x, dt, Bm, Cm, y must be 16-byte aligned; A, D, h0, h_final 4-byte aligned.
+ * y must not overlap any input.  Results are deterministic for a given input. */
+ssd_status ssd_fwd(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                   const void *Bm, const void *Cm, const float *D, const float *h0, void *y,
+                   float *h_final, void *workspace, size_t ws_bytes, ssd_stream_t stream);
+
+/* Same as ssd_fwd, and records events around each stage on `stream`:
+ * events[2*i] before and events[2*i+1] after stage i, for i = 0..3 in the order
+ * chunk_cumsum, chunk_state, state_passing, chunk_scan.  `events` is a host
+ * array of 8 created events (cudaEventCreate); used for per-stage timing. */
+ssd_status ssd_fwd_timed(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                         const void *Bm, const void *Cm, const float *D, const float *h0, void *y,
+                         float *h_final, void *workspace, size_t ws_bytes, ssd_stream_t stream,
+                         ssd_event_t const *events);
+
+/* One recurrent decode step for every (batch, head) (blog section "Mamba-2
+ * architecture": the recurrent form suits sequential inference).
+ * desc.seqlen and desc.chunk are ignored.  Layouts:
+ *   x [B][nh][H] in, dt [B][nh] in, Bm, Cm [B][G][S] in, A, D [nh] float32,
+ *   h [B][nh][H][S] float32 read and overwritten in place, y [B][nh][H] out.
+ * All pointers 4-byte aligned (16 for h when S % 4 == 0 is used vectorised). */
+ssd_status ssd_step(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                    const void *Bm, const void *Cm, const float *D, float *h, void *y,
+                    ssd_stream_t stream);
+
+/* ---- The four stages of ssd_fwd, callable one by one --------------------
+ * Intermediate layouts (all float32 unless stated):
+ *   G        [B][nh][L]          log2(e) * inclusive in-chunk cumsum of A dt
+ *   s_local  [B][nh][nc][H][S]   chunk state from a zero start
+ *   h_start  [B][nh][nc][H][S]   state entering each chunk, in desc.in_dtype
+ *                                 (the dtype the chunk-output contraction reads)
+ */
+
+/* Stage 1 (blog section "Kernel 1: cumulative sum"): G from dt and A. */
+ssd_status ssd_chunk_cumsum(const ssd_desc *desc, const void *dt, const float *A, float *G,
+                            ssd_stream_t stream);
+
+/* Stage 2 (blog section "Kernel 2: fwd_pass_state", the per-chunk contraction):
+ * s_local[b][h][k] = sum_{t in chunk k} dt_t exp2(G_last - G_t) x_t B_t^T. */
+ssd_status ssd_chunk_state(const ssd_desc *desc, const void *x, const void *dt, const void *Bm,
+                           const float *G, float *s_local, ssd_stream_t stream);
+
+/* Stage 3 (blog section "Kernel 2: fwd_pass_state", the sequential chunk loop):
+ * h_start[k] = h_k with h_0 = h0 (NULL: zeros), h_{k+1} = exp2(G_last,k) h_k + s_local[k];
+ * h_final (nullable) = h_nc.  s_local and h_start may not overlap. */
+ssd_status ssd_state_passing(const ssd_desc *desc, const float *G, const float *s_local,
+                             const float *h0, void *h_start, float *h_final, ssd_stream_t stream);
+
+/* Stage 4 (blog section "Kernel 3: compute_out"): y from the chunk-start states:
+ * Y_k = exp2(G) o (C h_k^T) + ((C B^T) o exp2(G_i - G_j) o [i >= j]) (dt o X) + D X. */
+ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, const void *Bm,
+                          const void *Cm, const float *D, const float *G, const void *h_start,
+                          void *y, ssd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_H_ */

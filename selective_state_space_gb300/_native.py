@@ -1,0 +1,76 @@
+"""ctypes view of libssd.so (include/ssd.h).  Loading fails loudly if the library
+is missing: there is no other implementation to fall back to."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libssd.so")
+
+SSD_F32, SSD_BF16 = 0, 1
+SSD_FLAG_FORCE_SIMT = 1
+STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_WORKSPACE",
+          4: "SSD_ERR_CUDA"}
+
+# Every symbol include/ssd.h declares.
+EXPORTS = ("ssd_status_string", "ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd", "ssd_fwd_timed", "ssd_step",
+           "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan")
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+                ("chunk", ctypes.c_int64), ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class SSDError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libssd.so not built ({path}); run selective_state_space_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        DP = ctypes.POINTER(Desc)
+        st = ctypes.c_int
+        lib.ssd_status_string.argtypes = [st]
+        lib.ssd_status_string.restype = ctypes.c_char_p
+        lib.ssd_fwd_workspace_size.argtypes = [DP, ctypes.POINTER(ctypes.c_size_t)]
+        lib.ssd_fwd_workspace_size.restype = st
+        lib.ssd_fwd_path.argtypes = [DP, ctypes.POINTER(ctypes.c_int32)]
+        lib.ssd_fwd_path.restype = st
+        lib.ssd_fwd.argtypes = [DP] + [P] * 10 + [ctypes.c_size_t, P]
+        lib.ssd_fwd.restype = st
+        lib.ssd_fwd_timed.argtypes = [DP] + [P] * 10 + [ctypes.c_size_t, P, ctypes.POINTER(P)]
+        lib.ssd_fwd_timed.restype = st
+        lib.ssd_step.argtypes = [DP] + [P] * 9
+        lib.ssd_step.restype = st
+        lib.ssd_chunk_cumsum.argtypes = [DP, P, P, P, P]
+        lib.ssd_chunk_cumsum.restype = st
+        lib.ssd_chunk_state.argtypes = [DP, P, P, P, P, P, P]
+        lib.ssd_chunk_state.restype = st
+        lib.ssd_state_passing.argtypes = [DP, P, P, P, P, P, P]
+        lib.ssd_state_passing.restype = st
+        lib.ssd_chunk_scan.argtypes = [DP] + [P] * 9
+        lib.ssd_chunk_scan.restype = st
+        _lib = lib
+        return lib
+
+
+def check(fn: str, code: int) -> None:
+    if code != 0:
+        raise SSDError(fn, code)

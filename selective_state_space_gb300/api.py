@@ -1,0 +1,166 @@
+"""Thin torch-facing binding of libssd.so: argument marshalling only.
+
+Every function here checks shapes, allocates outputs with torch (device
+memory is PyTorch's job) and calls the C ABI of include/ssd.h, which runs
+every step of the computation in CUDA kernels.  Tensors must live on a CUDA
+device; there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _native
+from ._native import Desc, SSD_BF16, SSD_F32, check
+
+_DT = {torch.float32: SSD_F32, torch.bfloat16: SSD_BF16}
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t not in _DT:
+        raise TypeError(f"unsupported dtype {t}; use float32 or bfloat16")
+    return _DT[t]
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must be on a CUDA device (no CPU implementation exists)")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_desc(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, in_dtype, out_dtype,
+              flags: int = 0) -> Desc:
+    d = Desc()
+    d.batch, d.seqlen, d.nheads, d.headdim = batch, seqlen, nheads, headdim
+    d.dstate, d.ngroups, d.chunk = dstate, ngroups, chunk
+    d.in_dtype = _dtype_code(in_dtype) if isinstance(in_dtype, torch.dtype) else int(in_dtype)
+    d.out_dtype = _dtype_code(out_dtype) if isinstance(out_dtype, torch.dtype) else int(out_dtype)
+    d.flags, d.reserved = flags, 0
+    return d
+
+
+def desc_for(x: torch.Tensor, Bm: torch.Tensor, chunk: int, out_dtype=None, flags: int = 0) -> Desc:
+    batch, seqlen, nheads, headdim = x.shape
+    ngroups, dstate = Bm.shape[2], Bm.shape[3]
+    return make_desc(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, x.dtype,
+                     out_dtype or x.dtype, flags)
+
+
+def workspace_size(desc: Desc) -> int:
+    n = ctypes.c_size_t(0)
+    check("ssd_fwd_workspace_size", _native.load().ssd_fwd_workspace_size(ctypes.byref(desc), ctypes.byref(n)))
+    return int(n.value)
+
+
+def uses_tensor_cores(desc: Desc) -> bool:
+    v = ctypes.c_int32(0)
+    check("ssd_fwd_path", _native.load().ssd_fwd_path(ctypes.byref(desc), ctypes.byref(v)))
+    return bool(v.value)
+
+
+def alloc_workspace(desc: Desc, device) -> torch.Tensor:
+    n = workspace_size(desc)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def ssd_fwd(x, dt, A, B, C, D, chunk: int, h0=None, *, y=None, h_final=None, want_h_final=True,
+            workspace=None, out_dtype=None, flags: int = 0, stream=None, events: Sequence = None):
+    """Chunked SSD forward.  Returns (y, h_final or None).
+
+    x [B,L,nh,H], dt [B,L,nh], B/C [B,L,G,S] in float32 or bfloat16 (same dtype);
+    A, D [nh] float32; h0 [B,nh,H,S] float32 or None.  ``events`` (8 CUDA events)
+    selects ssd_fwd_timed, which records them around the four stages.
+    """
+    desc = desc_for(x, B, chunk, out_dtype, flags)
+    batch, seqlen, nheads, headdim = x.shape
+    dstate = B.shape[3]
+    if y is None:
+        y = torch.empty((batch, seqlen, nheads, headdim), dtype=out_dtype or x.dtype, device=x.device)
+    if h_final is None and want_h_final:
+        h_final = torch.empty((batch, nheads, headdim, dstate), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace(desc, x.device)
+    args = [ctypes.byref(desc), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(h0), _ptr(y),
+            _ptr(h_final), _ptr(workspace), workspace.numel(), _stream(stream)]
+    lib = _native.load()
+    if events is None:
+        check("ssd_fwd", lib.ssd_fwd(*args))
+    else:
+        arr = (ctypes.c_void_p * 8)(*[e.cuda_event for e in events])
+        check("ssd_fwd_timed", lib.ssd_fwd_timed(*args, arr))
+    return y, h_final
+
+
+def ssd_step(x, dt, A, B, C, D, h, *, y=None, out_dtype=None, stream=None):
+    """One decode step.  x [B,nh,H], dt [B,nh], B/C [B,G,S], h [B,nh,H,S] float32 (updated in place).
+    Returns y [B,nh,H]."""
+    batch, nheads, headdim = x.shape
+    ngroups, dstate = B.shape[1], B.shape[2]
+    desc = make_desc(batch, 1, nheads, headdim, dstate, ngroups, 1, x.dtype, out_dtype or x.dtype)
+    if y is None:
+        y = torch.empty((batch, nheads, headdim), dtype=out_dtype or x.dtype, device=x.device)
+    check("ssd_step", _native.load().ssd_step(ctypes.byref(desc), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                              _ptr(D), _ptr(h), _ptr(y), _stream(stream)))
+    return y
+
+
+# ---- the four stages, one call each (intermediate layouts in include/ssd.h) ----
+
+def ssd_chunk_cumsum(dt, A, chunk: int, desc: Desc = None, *, G=None, stream=None):
+    batch, seqlen, nheads = dt.shape
+    if desc is None:
+        desc = make_desc(batch, seqlen, nheads, 1, 1, 1, chunk, dt.dtype, dt.dtype)
+    if G is None:
+        G = torch.empty((batch, nheads, seqlen), dtype=torch.float32, device=dt.device)
+    check("ssd_chunk_cumsum", _native.load().ssd_chunk_cumsum(ctypes.byref(desc), _ptr(dt), _ptr(A), _ptr(G),
+                                                              _stream(stream)))
+    return G
+
+
+def ssd_chunk_state(x, dt, B, G, chunk: int, *, s_local=None, flags: int = 0, stream=None):
+    desc = desc_for(x, B, chunk, None, flags)
+    batch, seqlen, nheads, headdim = x.shape
+    nc = (seqlen + chunk - 1) // chunk
+    if s_local is None:
+        s_local = torch.empty((batch, nheads, nc, headdim, B.shape[3]), dtype=torch.float32, device=x.device)
+    check("ssd_chunk_state", _native.load().ssd_chunk_state(ctypes.byref(desc), _ptr(x), _ptr(dt), _ptr(B), _ptr(G),
+                                                            _ptr(s_local), _stream(stream)))
+    return s_local
+
+
+def ssd_state_passing(G, s_local, chunk: int, in_dtype, h0=None, *, ngroups: int = 1, h_start=None,
+                      want_h_final=True, stream=None):
+    batch, nheads, nc, headdim, dstate = s_local.shape
+    seqlen = G.shape[2]
+    desc = make_desc(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, in_dtype, in_dtype)
+    if h_start is None:
+        h_start = torch.empty(s_local.shape, dtype=in_dtype, device=s_local.device)
+    h_final = torch.empty((batch, nheads, headdim, dstate), dtype=torch.float32,
+                          device=s_local.device) if want_h_final else None
+    check("ssd_state_passing", _native.load().ssd_state_passing(ctypes.byref(desc), _ptr(G), _ptr(s_local), _ptr(h0),
+                                                                _ptr(h_start), _ptr(h_final), _stream(stream)))
+    return h_start, h_final
+
+
+def ssd_chunk_scan(x, dt, B, C, D, G, h_start, chunk: int, *, y=None, out_dtype=None, flags: int = 0,
+                   stream=None):
+    desc = desc_for(x, B, chunk, out_dtype, flags)
+    if y is None:
+        y = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
+    check("ssd_chunk_scan", _native.load().ssd_chunk_scan(ctypes.byref(desc), _ptr(x), _ptr(dt), _ptr(B), _ptr(C),
+                                                          _ptr(D), _ptr(G), _ptr(h_start), _ptr(y), _stream(stream)))
+    return y

@@ -1,0 +1,272 @@
+// ssd_api.cu -- the extern "C" entry points of libssd.so (declared in include/ssd.h):
+// argument validation, workspace carving and the stage sequence of the forward pass.
+#include <stdint.h>
+#include <string.h>
+
+#include "ssd_common.cuh"
+#include "ssd_tc.cuh"
+
+namespace {
+
+using ssd::Problem;
+
+constexpr size_t kWsAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Validate a descriptor; fills `pr` on success.  `need_seq` is false for the
+// decode step, which ignores seqlen and chunk.
+ssd_status check_desc(const ssd_desc *d, Problem *pr, bool need_seq)
+{
+    if (!d) return SSD_ERR_INVALID_ARG;
+    if (d->batch < 0 || d->nheads < 0 || d->headdim < 1 || d->dstate < 1 || d->ngroups < 1)
+        return SSD_ERR_INVALID_ARG;
+    if (d->nheads % d->ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (d->in_dtype != SSD_F32 && d->in_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (d->out_dtype != SSD_F32 && d->out_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (d->reserved != 0 || (d->flags & ~SSD_FLAG_FORCE_SIMT) != 0) return SSD_ERR_INVALID_ARG;
+    if (need_seq && (d->seqlen < 0 || d->chunk < 1)) return SSD_ERR_INVALID_ARG;
+    if (d->dstate > 256 || d->headdim > 1024) return SSD_ERR_UNSUPPORTED;
+    if (need_seq && d->chunk > 1024) return SSD_ERR_UNSUPPORTED;
+    // grid-dimension limits of the launches (y and z are at most 65535)
+    if (d->batch > 65535) return SSD_ERR_UNSUPPORTED;
+    if (d->nheads * ((d->headdim + 31) / 32) * ((d->dstate + 63) / 64) > 65535) return SSD_ERR_UNSUPPORTED;
+    pr->B = d->batch;
+    pr->L = need_seq ? d->seqlen : 1;
+    pr->nh = d->nheads;
+    pr->H = d->headdim;
+    pr->S = d->dstate;
+    pr->G = d->ngroups;
+    pr->T = need_seq ? d->chunk : 1;
+    pr->nc = need_seq ? (d->seqlen + d->chunk - 1) / d->chunk : 1;
+    pr->hpg = d->ngroups ? d->nheads / d->ngroups : 1;
+    pr->in_dt = d->in_dtype;
+    pr->out_dt = d->out_dtype;
+    if (need_seq && pr->nc > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+size_t esize(int dt) { return dt == SSD_BF16 ? 2 : 4; }
+
+struct Workspace {
+    float *G;          // [B][nh][L]
+    float *s_local;    // [B][nh][nc][H][S]
+    void *h_start;     // [B][nh][nc][H][S] in_dtype
+    size_t bytes;
+};
+
+Workspace carve(const Problem &pr, void *base)
+{
+    Workspace w;
+    const size_t g_bytes = align_up(sizeof(float) * (size_t)(pr.B * pr.nh * pr.L), kWsAlign);
+    const size_t states = (size_t)(pr.B * pr.nh * pr.nc * pr.H * pr.S);
+    const size_t s_bytes = align_up(sizeof(float) * states, kWsAlign);
+    const size_t h_bytes = align_up(esize(pr.in_dt) * states, kWsAlign);
+    char *p = (char *)base;
+    w.G = (float *)p;
+    w.s_local = (float *)(p + g_bytes);
+    w.h_start = (void *)(p + g_bytes + s_bytes);
+    w.bytes = g_bytes + s_bytes + h_bytes;
+    return w;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+ssd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
+
+ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                    const void *Bm, const void *Cm, const float *D, const float *h0, void *y,
+                    float *h_final, void *workspace, size_t ws_bytes, cudaStream_t st,
+                    ssd_event_t const *events)
+{
+    Problem pr;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    const size_t nstate = (size_t)(pr.B * pr.nh * pr.H * pr.S);
+    const bool empty = pr.B == 0 || pr.nh == 0 || pr.L == 0;
+    if (!empty) {
+        if (!x || !dt || !A || !Bm || !Cm || !D || !y) return SSD_ERR_INVALID_ARG;
+        if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(Bm, 16) || !aligned(Cm, 16) || !aligned(y, 16))
+            return SSD_ERR_INVALID_ARG;
+        if (!aligned(A, 4) || !aligned(D, 4)) return SSD_ERR_INVALID_ARG;
+        const size_t ny = (size_t)(pr.B * pr.L * pr.nh * pr.H) * esize(pr.out_dt);
+        const size_t nx = (size_t)(pr.B * pr.L * pr.nh * pr.H) * esize(pr.in_dt);
+        const size_t nbc = (size_t)(pr.B * pr.L * pr.G * pr.S) * esize(pr.in_dt);
+        if (overlaps(y, ny, x, nx) || overlaps(y, ny, Bm, nbc) || overlaps(y, ny, Cm, nbc))
+            return SSD_ERR_INVALID_ARG;
+    }
+    if ((h0 && !aligned(h0, 4)) || (h_final && !aligned(h_final, 4))) return SSD_ERR_INVALID_ARG;
+    if (empty) {
+        // Nothing to scan: the final state is the initial state (zeros if absent).
+        if (h_final && nstate) {
+            cudaError_t e = h0 ? cudaMemcpyAsync(h_final, h0, nstate * sizeof(float), cudaMemcpyDeviceToDevice, st)
+                               : cudaMemsetAsync(h_final, 0, nstate * sizeof(float), st);
+            return cuda_status(e);
+        }
+        return SSD_OK;
+    }
+    Workspace w = carve(pr, workspace);
+    if (!workspace || !aligned(workspace, kWsAlign) || ws_bytes < w.bytes) return SSD_ERR_WORKSPACE;
+
+    const bool use_tc = !(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr);
+    auto rec = [&](int i) -> cudaError_t { return events ? cudaEventRecord((cudaEvent_t)events[i], st) : cudaSuccess; };
+    cudaError_t e;
+    if ((e = rec(0)) != cudaSuccess) return SSD_ERR_CUDA;
+    if ((e = ssd::launch_chunk_cumsum(pr, dt, A, w.G, st)) != cudaSuccess) return SSD_ERR_CUDA;
+    if ((e = rec(1)) != cudaSuccess || (e = rec(2)) != cudaSuccess) return SSD_ERR_CUDA;
+    e = use_tc ? ssd::launch_chunk_state_tc(pr, x, dt, Bm, w.G, w.s_local, st)
+               : ssd::launch_chunk_state_simt(pr, x, dt, Bm, w.G, w.s_local, st);
+    if (e != cudaSuccess) return SSD_ERR_CUDA;
+    if ((e = rec(3)) != cudaSuccess || (e = rec(4)) != cudaSuccess) return SSD_ERR_CUDA;
+    if ((e = ssd::launch_state_passing(pr, w.G, w.s_local, h0, w.h_start, h_final, st)) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if ((e = rec(5)) != cudaSuccess || (e = rec(6)) != cudaSuccess) return SSD_ERR_CUDA;
+    e = use_tc ? ssd::launch_chunk_scan_tc(pr, x, dt, Bm, Cm, D, w.G, w.h_start, y, st)
+               : ssd::launch_chunk_scan_simt(pr, x, dt, Bm, Cm, D, w.G, w.h_start, y, st);
+    if (e != cudaSuccess) return SSD_ERR_CUDA;
+    if ((e = rec(7)) != cudaSuccess) return SSD_ERR_CUDA;
+    return SSD_OK;
+}
+
+bool nonempty(const Problem &pr) { return pr.B > 0 && pr.nh > 0 && pr.L > 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char *ssd_status_string(ssd_status s)
+{
+    switch (s) {
+    case SSD_OK: return "SSD_OK";
+    case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG: invalid argument (null/misaligned pointer, bad size or dtype)";
+    case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: problem size outside what this build handles";
+    case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing, too small or not 256-byte aligned";
+    case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA call or kernel launch failed";
+    }
+    return "unknown ssd_status";
+}
+
+ssd_status ssd_fwd_workspace_size(const ssd_desc *desc, size_t *bytes)
+{
+    Problem pr;
+    if (!bytes) return SSD_ERR_INVALID_ARG;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    *bytes = nonempty(pr) ? carve(pr, nullptr).bytes : 0;
+    return SSD_OK;
+}
+
+ssd_status ssd_fwd_path(const ssd_desc *desc, int32_t *uses_tensor_cores)
+{
+    Problem pr;
+    if (!uses_tensor_cores) return SSD_ERR_INVALID_ARG;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    *uses_tensor_cores = (!(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr)) ? 1 : 0;
+    return SSD_OK;
+}
+
+ssd_status ssd_fwd(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                   const void *Bm, const void *Cm, const float *D, const float *h0, void *y,
+                   float *h_final, void *workspace, size_t ws_bytes, ssd_stream_t stream)
+{
+    return fwd_impl(desc, x, dt, A, Bm, Cm, D, h0, y, h_final, workspace, ws_bytes,
+                    (cudaStream_t)stream, nullptr);
+}
+
+ssd_status ssd_fwd_timed(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                         const void *Bm, const void *Cm, const float *D, const float *h0, void *y,
+                         float *h_final, void *workspace, size_t ws_bytes, ssd_stream_t stream,
+                         ssd_event_t const *events)
+{
+    if (!events) return SSD_ERR_INVALID_ARG;
+    for (int i = 0; i < 8; ++i)
+        if (!events[i]) return SSD_ERR_INVALID_ARG;
+    return fwd_impl(desc, x, dt, A, Bm, Cm, D, h0, y, h_final, workspace, ws_bytes,
+                    (cudaStream_t)stream, events);
+}
+
+ssd_status ssd_step(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                    const void *Bm, const void *Cm, const float *D, float *h, void *y,
+                    ssd_stream_t stream)
+{
+    Problem pr;
+    ssd_status s = check_desc(desc, &pr, false);
+    if (s != SSD_OK) return s;
+    if (pr.B == 0 || pr.nh == 0) return SSD_OK;
+    if (!x || !dt || !A || !Bm || !Cm || !D || !h || !y) return SSD_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(dt, 2) || !aligned(Bm, 2) || !aligned(Cm, 2) || !aligned(y, 2) ||
+        !aligned(h, 4) || !aligned(A, 4) || !aligned(D, 4))
+        return SSD_ERR_INVALID_ARG;
+    return cuda_status(ssd::launch_ssd_step(pr, x, dt, A, Bm, Cm, D, h, y, (cudaStream_t)stream));
+}
+
+ssd_status ssd_chunk_cumsum(const ssd_desc *desc, const void *dt, const float *A, float *G,
+                            ssd_stream_t stream)
+{
+    Problem pr;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    if (!nonempty(pr)) return SSD_OK;
+    if (!dt || !A || !G || !aligned(G, 4) || !aligned(A, 4)) return SSD_ERR_INVALID_ARG;
+    return cuda_status(ssd::launch_chunk_cumsum(pr, dt, A, G, (cudaStream_t)stream));
+}
+
+ssd_status ssd_chunk_state(const ssd_desc *desc, const void *x, const void *dt, const void *Bm,
+                           const float *G, float *s_local, ssd_stream_t stream)
+{
+    Problem pr;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    if (!nonempty(pr)) return SSD_OK;
+    if (!x || !dt || !Bm || !G || !s_local) return SSD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(Bm, 16) || !aligned(G, 16) || !aligned(s_local, 16))
+        return SSD_ERR_INVALID_ARG;
+    const bool use_tc = !(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr);
+    cudaError_t e = use_tc ? ssd::launch_chunk_state_tc(pr, x, dt, Bm, G, s_local, (cudaStream_t)stream)
+                           : ssd::launch_chunk_state_simt(pr, x, dt, Bm, G, s_local, (cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+ssd_status ssd_state_passing(const ssd_desc *desc, const float *G, const float *s_local,
+                             const float *h0, void *h_start, float *h_final, ssd_stream_t stream)
+{
+    Problem pr;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    if (!nonempty(pr)) return SSD_OK;
+    if (!G || !s_local || !h_start) return SSD_ERR_INVALID_ARG;
+    if (!aligned(G, 4) || !aligned(s_local, 4) || !aligned(h_start, 4) ||
+        (h0 && !aligned(h0, 4)) || (h_final && !aligned(h_final, 4)))
+        return SSD_ERR_INVALID_ARG;
+    const size_t states = (size_t)(pr.B * pr.nh * pr.nc * pr.H * pr.S);
+    if (overlaps(s_local, states * 4, h_start, states * esize(pr.in_dt))) return SSD_ERR_INVALID_ARG;
+    return cuda_status(ssd::launch_state_passing(pr, G, s_local, h0, h_start, h_final, (cudaStream_t)stream));
+}
+
+ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, const void *Bm,
+                          const void *Cm, const float *D, const float *G, const void *h_start,
+                          void *y, ssd_stream_t stream)
+{
+    Problem pr;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    if (!nonempty(pr)) return SSD_OK;
+    if (!x || !dt || !Bm || !Cm || !D || !G || !h_start || !y) return SSD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(Bm, 16) || !aligned(Cm, 16) || !aligned(G, 16) ||
+        !aligned(h_start, 16) || !aligned(y, 16) || !aligned(D, 4))
+        return SSD_ERR_INVALID_ARG;
+    const bool use_tc = !(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr);
+    cudaError_t e = use_tc ? ssd::launch_chunk_scan_tc(pr, x, dt, Bm, Cm, D, G, h_start, y, (cudaStream_t)stream)
+                           : ssd::launch_chunk_scan_simt(pr, x, dt, Bm, Cm, D, G, h_start, y, (cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// ssd_common.cuh -- shared definitions for the SSD kernels (GPU side only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssd.h"
+
+namespace ssd {
+
+// G is stored pre-multiplied by log2(e) so that every later stage uses exp2
+// (blog section "Kernel 1: cumulative sum": the cumsum is scaled by log2(e)).
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Validated problem sizes, passed by value to kernels and launchers.
+struct Problem {
+    int64_t B, L, nh, H, S, G, T, nc, hpg;
+    int in_dt, out_dt;
+};
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Host-side launchers (one per stage).  Each returns the launch status.
+cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *A, float *G,
+                                cudaStream_t st);
+cudaError_t launch_chunk_state_simt(const Problem &pr, const void *x, const void *dt,
+                                    const void *Bm, const float *G, float *s_local,
+                                    cudaStream_t st);
+cudaError_t launch_state_passing(const Problem &pr, const float *G, const float *s_local,
+                                 const float *h0, void *h_start, float *h_final, cudaStream_t st);
+cudaError_t launch_chunk_scan_simt(const Problem &pr, const void *x, const void *dt,
+                                   const void *Bm, const void *Cm, const float *D, const float *G,
+                                   const void *h_start, void *y, cudaStream_t st);
+cudaError_t launch_ssd_step(const Problem &pr, const void *x, const void *dt, const float *A,
+                            const void *Bm, const void *Cm, const float *D, float *h, void *y,
+                            cudaStream_t st);
+
+}  // namespace ssd

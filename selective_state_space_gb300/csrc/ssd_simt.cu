@@ -1,0 +1,418 @@
+// ssd_simt.cu -- CUDA-core kernels for the four SSD stages and the decode step.
+//
+// These kernels handle every supported shape (any L, any chunk up to 1024,
+// S up to 256, any H) in float32 arithmetic on the CUDA cores.  The
+// tensor-core kernels in ssd_tc.cu take over the chunk_state and chunk_scan
+// stages for the shapes they are built for.
+//
+// Method: NVIDIA developer blog "Accelerating Mamba-2 with High-Performance
+// Forward Pass Kernels in NVIDIA CUDA Tile", sections "Mamba-2 architecture"
+// and "Kernel 1" .. "Kernel 3".
+#include "ssd_common.cuh"
+
+namespace ssd {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Stage 1 -- chunk_cumsum (blog section "Kernel 1: cumulative sum").
+// G[b][h][t] = log2(e) * sum_{s in chunk(t), s <= t} A[h] dt[b][s][h].
+// One block per (chunk, 32-head tile, batch); one warp-scan per (head, 32 tokens),
+// carried across the chunk.  dt is read as [token][head] tiles and G is written
+// transposed, [head][token], so both sides are coalesced.
+// ---------------------------------------------------------------------------
+template <typename Tin>
+__global__ void __launch_bounds__(256)
+k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *__restrict__ G,
+               int64_t L, int nh, int T)
+{
+    __shared__ float tile[32][33];
+    const int k = blockIdx.x, hbase = blockIdx.y * 32, b = blockIdx.z;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t0 = (int64_t)k * T;
+    const int n = (int)((int64_t)T < L - t0 ? (int64_t)T : L - t0);
+    float carry[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int seg = 0; seg < n; seg += 32) {
+        for (int r = warp; r < 32; r += 8) {
+            const int t = seg + r, h = hbase + lane;
+            float v = 0.f;   // zero padding past the end of the chunk
+            if (t < n && h < nh) v = A[h] * to_f32(dt[((int64_t)b * L + t0 + t) * nh + h]);
+            tile[r][lane] = v;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = warp * 4 + q;
+            float v = tile[lane][j];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += u;
+            }
+            v += carry[q];
+            carry[q] = __shfl_sync(0xffffffffu, v, 31);
+            tile[lane][j] = v;
+        }
+        __syncthreads();
+        for (int j = warp; j < 32; j += 8) {
+            const int h = hbase + j, t = seg + lane;
+            if (h < nh && t < n) G[((int64_t)b * nh + h) * L + t0 + t] = tile[lane][j] * kLog2e;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 2 -- chunk_state on CUDA cores (blog section "Kernel 2: fwd_pass_state",
+// the contraction x_tile^T (b dt exp2(d_last - d))).
+// s_local[b][h][k][p][s] = sum_t w_t x[t][p] B[t][s],  w_t = dt_t exp2(G_last - G_t).
+// One block per (chunk, head x 32-row p tile x 64-column s tile, batch).
+// ---------------------------------------------------------------------------
+template <typename Tin>
+__global__ void __launch_bounds__(256)
+k_chunk_state_simt(const Tin *__restrict__ x, const Tin *__restrict__ dt,
+                   const Tin *__restrict__ Bm, const float *__restrict__ G,
+                   float *__restrict__ s_local, Problem pr, int ptiles, int stiles)
+{
+    __shared__ float xw[32][33];   // [token][p]  w_t x[t][p]
+    __shared__ float bt[32][64];   // [token][s]
+    __shared__ float w[32];
+    const int k = blockIdx.x, b = blockIdx.z;
+    const int h = blockIdx.y / (ptiles * stiles);
+    const int tile = blockIdx.y % (ptiles * stiles);
+    const int p0 = (tile / stiles) * 32, s0 = (tile % stiles) * 64;
+    const int g = (int)(h / pr.hpg);
+    const int64_t t0 = (int64_t)k * pr.T;
+    const int n = (int)(pr.T < pr.L - t0 ? pr.T : pr.L - t0);
+    const float *Gh = G + ((int64_t)b * pr.nh + h) * pr.L;
+    const float glast = Gh[t0 + n - 1];
+    const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;   // s column, p group of 8
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int seg = 0; seg < n; seg += 32) {
+        if (threadIdx.x < 32) {
+            const int t = seg + threadIdx.x;
+            float v = 0.f;
+            if (t < n) v = to_f32(dt[((int64_t)b * pr.L + t0 + t) * pr.nh + h]) * exp2f(glast - Gh[t0 + t]);
+            w[threadIdx.x] = v;
+        }
+        __syncthreads();
+        for (int r = warp; r < 32; r += 8) {
+            const int t = seg + r, p = p0 + lane;
+            float v = 0.f;
+            if (t < n && p < pr.H) v = w[r] * to_f32(x[(((int64_t)b * pr.L + t0 + t) * pr.nh + h) * pr.H + p]);
+            xw[r][lane] = v;
+            for (int c = lane; c < 64; c += 32) {
+                const int s = s0 + c;
+                float u = 0.f;
+                if (t < n && s < pr.S) u = to_f32(Bm[(((int64_t)b * pr.L + t0 + t) * pr.G + g) * pr.S + s]);
+                bt[r][c] = u;
+            }
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int r = 0; r < 32; ++r) {
+            const float bv = bt[r][tx];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(xw[r][ty * 8 + i], bv, acc[i]);
+        }
+        __syncthreads();
+    }
+    const int s = s0 + tx;
+    if (s < pr.S) {
+        float *dst = s_local + ((((int64_t)b * pr.nh + h) * pr.nc + k) * pr.H) * pr.S;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int p = p0 + ty * 8 + i;
+            if (p < pr.H) dst[(int64_t)p * pr.S + s] = acc[i];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 3 -- state_passing (blog section "Kernel 2: fwd_pass_state", the
+// sequential loop over chunks).  One thread per state element, walking the
+// chunks in order: store h_k, then h_{k+1} = exp2(G_last,k) h_k + s_local[k].
+// Consecutive threads own consecutive elements, so every step is coalesced.
+// ---------------------------------------------------------------------------
+template <typename Tst>
+__global__ void __launch_bounds__(256)
+k_state_passing(const float *__restrict__ G, const float *__restrict__ s_local,
+                const float *__restrict__ h0, Tst *__restrict__ h_start,
+                float *__restrict__ h_final, Problem pr)
+{
+    const int64_t HS = pr.H * pr.S;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int h = blockIdx.y, b = blockIdx.z;
+    if (e >= HS) return;
+    const int64_t bh = (int64_t)b * pr.nh + h;
+    float st = h0 ? h0[bh * HS + e] : 0.f;
+    const float *Gh = G + bh * pr.L;
+    const int64_t base = bh * pr.nc * HS + e;
+    float s_next = s_local[base];
+    for (int64_t k = 0; k < pr.nc; ++k) {
+        const float s = s_next;
+        if (k + 1 < pr.nc) s_next = s_local[base + (k + 1) * HS];   // prefetch the next chunk
+        h_start[base + k * HS] = from_f32<Tst>(st);
+        const int64_t last = min(pr.L, (k + 1) * pr.T) - 1;
+        st = fmaf(exp2f(Gh[last]), st, s);
+    }
+    if (h_final) h_final[bh * HS + e] = st;
+}
+
+// ---------------------------------------------------------------------------
+// Stage 4 -- chunk_scan on CUDA cores (blog section "Kernel 3: compute_out").
+// For 32 rows i of one chunk and a 64-wide slice of p:
+//   y[i][p] = exp2(G_i) sum_s C[i][s] h_k[p][s]
+//           + sum_{j <= i} (C_i . B_j) exp2(G_i - G_j) dt_j x[j][p]      (select, never multiply, the mask)
+//           + D x[i][p]
+// ---------------------------------------------------------------------------
+constexpr int kScanRows = 32, kScanCols = 64;
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(256)
+k_chunk_scan_simt(const Tin *__restrict__ x, const Tin *__restrict__ dt,
+                  const Tin *__restrict__ Bm, const Tin *__restrict__ Cm,
+                  const float *__restrict__ D, const float *__restrict__ G,
+                  const Tin *__restrict__ h_start, Tout *__restrict__ y, Problem pr,
+                  int rtiles, int ptiles)
+{
+    extern __shared__ float smem[];
+    const int SP = (int)pr.S + 1;                 // padded row stride
+    float *Ct = smem;                             // [32][SP]   C rows i
+    float *Bs = Ct + kScanRows * SP;              // [32][SP]   B rows j
+    float *Xs = Bs + kScanRows * SP;              // [32][65]   dt_j x[j][p]
+    float *Pm = Xs + kScanRows * (kScanCols + 1); // [32][33]   masked, decayed C B^T
+    float *Hs = Pm + kScanRows * 33;              // [64][33]   h_k[p][s-slice]
+    float *Gi = Hs + kScanCols * 33;              // [32]
+    float *Gj = Gi + kScanRows;                   // [32]
+
+    const int k = blockIdx.x / rtiles, rt = blockIdx.x % rtiles;
+    const int h = blockIdx.y / ptiles, pt = blockIdx.y % ptiles;
+    const int b = blockIdx.z;
+    const int g = (int)(h / pr.hpg);
+    const int64_t t0 = (int64_t)k * pr.T;
+    const int n = (int)(pr.T < pr.L - t0 ? pr.T : pr.L - t0);
+    const int i0 = rt * kScanRows, p0 = pt * kScanCols;
+    if (i0 >= n) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = tid >> 3, c = tid & 7;           // output row, p lane (p = c + 8q)
+    const float *Gh = G + ((int64_t)b * pr.nh + h) * pr.L + t0;
+    auto bc_row = [&](const Tin *M, int t) { return M + (((int64_t)b * pr.L + t0 + t) * pr.G + g) * pr.S; };
+
+    for (int rr = warp; rr < kScanRows; rr += 8) {
+        const int i = i0 + rr;
+        const Tin *src = bc_row(Cm, i < n ? i : 0);
+        for (int s = lane; s < pr.S; s += 32) Ct[rr * SP + s] = (i < n) ? to_f32(src[s]) : 0.f;
+    }
+    if (tid < kScanRows) Gi[tid] = (i0 + tid < n) ? Gh[i0 + tid] : 0.f;
+
+    float acc[8], sacc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) { acc[q] = 0.f; sacc[q] = 0.f; }
+
+    const int jend = min(n, i0 + kScanRows);
+    for (int js = 0; js < jend; js += kScanRows) {
+        __syncthreads();
+        for (int rr = warp; rr < kScanRows; rr += 8) {
+            const int j = js + rr;
+            const Tin *src = bc_row(Bm, j < n ? j : 0);
+            for (int s = lane; s < pr.S; s += 32) Bs[rr * SP + s] = (j < n) ? to_f32(src[s]) : 0.f;
+            const float dtj = (j < n) ? to_f32(dt[((int64_t)b * pr.L + t0 + j) * pr.nh + h]) : 0.f;
+            for (int pp = lane; pp < kScanCols; pp += 32) {
+                const int p = p0 + pp;
+                float v = 0.f;
+                if (j < n && p < pr.H) v = dtj * to_f32(x[(((int64_t)b * pr.L + t0 + j) * pr.nh + h) * pr.H + p]);
+                Xs[rr * (kScanCols + 1) + pp] = v;
+            }
+        }
+        if (tid < kScanRows) Gj[tid] = (js + tid < n) ? Gh[js + tid] : 0.f;
+        __syncthreads();
+        // masked, decayed C B^T for rows i0.., columns js..
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int jj = c + 8 * q;
+            const int i = i0 + r, j = js + jj;
+            float v = 0.f;
+            if (j <= i && i < n && j < n) {
+                float cb = 0.f;
+                const float *ci = Ct + r * SP, *bj = Bs + jj * SP;
+                for (int s = 0; s < pr.S; ++s) cb = fmaf(ci[s], bj[s], cb);
+                v = cb * exp2f(Gi[r] - Gj[jj]);
+            }
+            Pm[r * 33 + jj] = v;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int jj = 0; jj < kScanRows; ++jj) {
+            const float pv = Pm[r * 33 + jj];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = fmaf(pv, Xs[jj * (kScanCols + 1) + c + 8 * q], acc[q]);
+        }
+    }
+    // carried-state term: C_i . h_k[p]
+    const Tin *hk = h_start + ((((int64_t)b * pr.nh + h) * pr.nc + k) * pr.H) * pr.S;
+    for (int ss = 0; ss < pr.S; ss += 32) {
+        __syncthreads();
+        for (int pp = warp; pp < kScanCols; pp += 8) {
+            const int p = p0 + pp, s = ss + lane;
+            Hs[pp * 33 + lane] = (p < pr.H && s < pr.S) ? to_f32(hk[(int64_t)p * pr.S + s]) : 0.f;
+        }
+        __syncthreads();
+        const int send = min(32, (int)pr.S - ss);
+        for (int s2 = 0; s2 < send; ++s2) {
+            const float cv = Ct[r * SP + ss + s2];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sacc[q] = fmaf(cv, Hs[(c + 8 * q) * 33 + s2], sacc[q]);
+        }
+    }
+    const int i = i0 + r;
+    if (i < n) {
+        const float eg = exp2f(Gi[r]);
+        const float dh = D[h];
+        const int64_t row = (((int64_t)b * pr.L + t0 + i) * pr.nh + h) * pr.H;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int p = p0 + c + 8 * q;
+            if (p < pr.H) {
+                const float xv = to_f32(x[row + p]);
+                y[row + p] = from_f32<Tout>(fmaf(eg, sacc[q], acc[q]) + dh * xv);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Decode step (blog section "Mamba-2 architecture", the recurrent form).
+// One warp per state row (b, h, p): h[p][s] = exp(A dt) h[p][s] + dt x[p] B[s],
+// y[p] = sum_s C[s] h[p][s] + D x[p].  Rows are contiguous in s: coalesced.
+// ---------------------------------------------------------------------------
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(256)
+k_ssd_step(const Tin *__restrict__ x, const Tin *__restrict__ dt, const float *__restrict__ A,
+           const Tin *__restrict__ Bm, const Tin *__restrict__ Cm, const float *__restrict__ D,
+           float *__restrict__ hst, Tout *__restrict__ y, Problem pr)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t p = (int64_t)blockIdx.x * 8 + warp;
+    const int hh = blockIdx.y, b = blockIdx.z;
+    if (p >= pr.H) return;
+    const int g = (int)(hh / pr.hpg);
+    const int64_t bh = (int64_t)b * pr.nh + hh;
+    const float dtv = to_f32(dt[bh]);
+    const float alpha = exp2f(A[hh] * dtv * kLog2e);
+    const float xp = to_f32(x[bh * pr.H + p]);
+    const Tin *Bv = Bm + ((int64_t)b * pr.G + g) * pr.S;
+    const Tin *Cv = Cm + ((int64_t)b * pr.G + g) * pr.S;
+    float *row = hst + (bh * pr.H + p) * pr.S;
+    const float u = dtv * xp;
+    float acc = 0.f;
+    for (int64_t s = lane; s < pr.S; s += 32) {
+        const float v = fmaf(alpha, row[s], u * to_f32(Bv[s]));
+        row[s] = v;
+        acc = fmaf(to_f32(Cv[s]), v, acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) y[bh * pr.H + p] = from_f32<Tout>(fmaf(D[hh], xp, acc));
+}
+
+size_t scan_smem_bytes(const Problem &pr)
+{
+    const size_t SP = (size_t)pr.S + 1;
+    return sizeof(float) * (2 * kScanRows * SP + kScanRows * (kScanCols + 1) + kScanRows * 33 +
+                            kScanCols * 33 + 2 * kScanRows);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *A, float *G,
+                                cudaStream_t st)
+{
+    dim3 grid((unsigned)pr.nc, (unsigned)((pr.nh + 31) / 32), (unsigned)pr.B);
+    if (pr.in_dt == SSD_BF16)
+        k_chunk_cumsum<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)dt, A, G, pr.L, (int)pr.nh, (int)pr.T);
+    else
+        k_chunk_cumsum<float><<<grid, 256, 0, st>>>((const float *)dt, A, G, pr.L, (int)pr.nh, (int)pr.T);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_state_simt(const Problem &pr, const void *x, const void *dt,
+                                    const void *Bm, const float *G, float *s_local,
+                                    cudaStream_t st)
+{
+    const int ptiles = (int)((pr.H + 31) / 32), stiles = (int)((pr.S + 63) / 64);
+    dim3 grid((unsigned)pr.nc, (unsigned)(pr.nh * ptiles * stiles), (unsigned)pr.B);
+    if (pr.in_dt == SSD_BF16)
+        k_chunk_state_simt<__nv_bfloat16><<<grid, 256, 0, st>>>(
+            (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)dt, (const __nv_bfloat16 *)Bm, G, s_local, pr, ptiles, stiles);
+    else
+        k_chunk_state_simt<float><<<grid, 256, 0, st>>>(
+            (const float *)x, (const float *)dt, (const float *)Bm, G, s_local, pr, ptiles, stiles);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_passing(const Problem &pr, const float *G, const float *s_local,
+                                 const float *h0, void *h_start, float *h_final, cudaStream_t st)
+{
+    const int64_t HS = pr.H * pr.S;
+    dim3 grid((unsigned)((HS + 255) / 256), (unsigned)pr.nh, (unsigned)pr.B);
+    if (pr.in_dt == SSD_BF16)
+        k_state_passing<__nv_bfloat16><<<grid, 256, 0, st>>>(G, s_local, h0, (__nv_bfloat16 *)h_start, h_final, pr);
+    else
+        k_state_passing<float><<<grid, 256, 0, st>>>(G, s_local, h0, (float *)h_start, h_final, pr);
+    return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout>
+static cudaError_t scan_launch(const Problem &pr, const void *x, const void *dt, const void *Bm,
+                               const void *Cm, const float *D, const float *G, const void *h_start,
+                               void *y, cudaStream_t st)
+{
+    const int rtiles = (int)((pr.T + kScanRows - 1) / kScanRows);
+    const int ptiles = (int)((pr.H + kScanCols - 1) / kScanCols);
+    const size_t smem = scan_smem_bytes(pr);
+    auto kern = k_chunk_scan_simt<Tin, Tout>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(pr.nc * rtiles), (unsigned)(pr.nh * ptiles), (unsigned)pr.B);
+    kern<<<grid, 256, smem, st>>>((const Tin *)x, (const Tin *)dt, (const Tin *)Bm, (const Tin *)Cm, D, G,
+                                  (const Tin *)h_start, (Tout *)y, pr, rtiles, ptiles);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_scan_simt(const Problem &pr, const void *x, const void *dt,
+                                   const void *Bm, const void *Cm, const float *D, const float *G,
+                                   const void *h_start, void *y, cudaStream_t st)
+{
+    const bool ib = pr.in_dt == SSD_BF16, ob = pr.out_dt == SSD_BF16;
+    if (ib && ob) return scan_launch<__nv_bfloat16, __nv_bfloat16>(pr, x, dt, Bm, Cm, D, G, h_start, y, st);
+    if (ib) return scan_launch<__nv_bfloat16, float>(pr, x, dt, Bm, Cm, D, G, h_start, y, st);
+    if (ob) return scan_launch<float, __nv_bfloat16>(pr, x, dt, Bm, Cm, D, G, h_start, y, st);
+    return scan_launch<float, float>(pr, x, dt, Bm, Cm, D, G, h_start, y, st);
+}
+
+template <typename Tin, typename Tout>
+static cudaError_t step_launch(const Problem &pr, const void *x, const void *dt, const float *A,
+                               const void *Bm, const void *Cm, const float *D, float *h, void *y,
+                               cudaStream_t st)
+{
+    dim3 grid((unsigned)((pr.H + 7) / 8), (unsigned)pr.nh, (unsigned)pr.B);
+    k_ssd_step<Tin, Tout><<<grid, 256, 0, st>>>((const Tin *)x, (const Tin *)dt, A, (const Tin *)Bm,
+                                                (const Tin *)Cm, D, h, (Tout *)y, pr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ssd_step(const Problem &pr, const void *x, const void *dt, const float *A,
+                            const void *Bm, const void *Cm, const float *D, float *h, void *y,
+                            cudaStream_t st)
+{
+    const bool ib = pr.in_dt == SSD_BF16, ob = pr.out_dt == SSD_BF16;
+    if (ib && ob) return step_launch<__nv_bfloat16, __nv_bfloat16>(pr, x, dt, A, Bm, Cm, D, h, y, st);
+    if (ib) return step_launch<__nv_bfloat16, float>(pr, x, dt, A, Bm, Cm, D, h, y, st);
+    if (ob) return step_launch<float, __nv_bfloat16>(pr, x, dt, A, Bm, Cm, D, h, y, st);
+    return step_launch<float, float>(pr, x, dt, A, Bm, Cm, D, h, y, st);
+}
+
+}  // namespace ssd

@@ -1,0 +1,135 @@
+"""Host-side checks of libssd.so that need no GPU: the library loads, exports every
+symbol include/ssd.h declares, and rejects bad arguments before launching anything.
+
+The invalid-argument calls below return during validation, before any CUDA
+call; the pointers passed are never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_gb300 import _native
+from selective_state_space_gb300.build import build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "ssd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _native.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(ssd_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    assert sorted(names) == sorted(_native.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = lib.ssd_status_string(code).decode()
+        assert s.startswith(_native.STATUS[code])
+    assert lib.ssd_status_string(99).decode() == "unknown ssd_status"
+
+
+def desc(**kw):
+    d = _native.Desc()
+    base = dict(batch=2, seqlen=512, nheads=8, headdim=64, dstate=128, ngroups=2, chunk=256,
+                in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16, flags=0, reserved=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(d, k, v)
+    return d
+
+
+def ws_size(lib, d):
+    n = ctypes.c_size_t(0)
+    rc = lib.ssd_fwd_workspace_size(ctypes.byref(d), ctypes.byref(n))
+    return rc, n.value
+
+
+def test_workspace_size_arithmetic(lib):
+    rc, n = ws_size(lib, desc())
+    assert rc == 0
+    B, L, nh, H, S, T = 2, 512, 8, 64, 128, 256
+    nc = (L + T - 1) // T
+    al = lambda v: (v + 255) // 256 * 256
+    assert n == al(4 * B * nh * L) + al(4 * B * nh * nc * H * S) + al(2 * B * nh * nc * H * S)
+    rc, n = ws_size(lib, desc(seqlen=0))
+    assert rc == 0 and n == 0
+    rc, n = ws_size(lib, desc(seqlen=513))   # ragged: one more chunk
+    assert rc == 0 and n > ws_size(lib, desc())[1]
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(ngroups=3), 1), (dict(nheads=-1), 1), (dict(headdim=0), 1), (dict(dstate=0), 1),
+    (dict(chunk=0), 1), (dict(seqlen=-5), 1), (dict(in_dtype=7), 1), (dict(out_dtype=-1), 1),
+    (dict(flags=1 << 8), 1), (dict(reserved=1), 1),
+    (dict(dstate=257), 2), (dict(headdim=2048), 2), (dict(chunk=4096), 2),
+])
+def test_bad_descriptors_rejected(lib, bad, code):
+    rc, _ = ws_size(lib, desc(**bad))
+    assert rc == code
+    d = desc(**bad)
+    fake = 1 << 20     # 256-byte aligned, never dereferenced
+    rc = lib.ssd_fwd(ctypes.byref(d), fake, fake, fake, fake, fake, fake, None, fake * 2, None, fake * 4,
+                     1 << 40, None)
+    assert rc == code
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    d = desc()
+    a = 1 << 20
+    args = [a, a, a, a, a, a, None, 1 << 30, None, 1 << 34, 1 << 40, None]
+    for i in (0, 1, 2, 3, 4, 5, 7):      # required pointers
+        bad = list(args)
+        bad[i] = None
+        assert lib.ssd_fwd(ctypes.byref(d), *bad) == 1, i
+    bad = list(args)
+    bad[0] = a + 2                        # x not 16-byte aligned
+    assert lib.ssd_fwd(ctypes.byref(d), *bad) == 1
+    bad = list(args)
+    bad[7] = a                            # y overlaps x
+    assert lib.ssd_fwd(ctypes.byref(d), *bad) == 1
+    bad = list(args)
+    bad[9] = None                         # no workspace
+    assert lib.ssd_fwd(ctypes.byref(d), *bad) == 3
+    bad = list(args)
+    bad[10] = 1024                        # workspace too small
+    assert lib.ssd_fwd(ctypes.byref(d), *bad) == 3
+    bad = list(args)
+    bad[9] = (1 << 34) + 128              # workspace misaligned
+    assert lib.ssd_fwd(ctypes.byref(d), *bad) == 3
+
+
+def test_step_and_stage_validation(lib):
+    d = desc(ngroups=3)
+    a = 1 << 20
+    assert lib.ssd_step(ctypes.byref(d), a, a, a, a, a, a, a, a, None) == 1
+    assert lib.ssd_chunk_cumsum(ctypes.byref(d), a, a, a, None) == 1
+    d = desc()
+    assert lib.ssd_step(ctypes.byref(d), None, a, a, a, a, a, a, a, None) == 1
+    assert lib.ssd_chunk_state(ctypes.byref(d), a, a, a, a, None, None) == 1
+    assert lib.ssd_chunk_scan(ctypes.byref(d), a, a, a, a, a, a, a, None, None) == 1
+    assert lib.ssd_state_passing(ctypes.byref(d), a, a, None, a, None, None) == 1   # s_local overlaps h_start
+    iv = ctypes.c_int32(-1)
+    assert lib.ssd_fwd_path(ctypes.byref(d), ctypes.byref(iv)) == 0 and iv.value in (0, 1)
+    assert lib.ssd_fwd_path(ctypes.byref(d), None) == 1
+
+
+def test_timed_variant_requires_events(lib):
+    d = desc()
+    a = 1 << 20
+    assert lib.ssd_fwd_timed(ctypes.byref(d), a, a, a, a, a, a, None, 1 << 30, None, 1 << 34, 1 << 40, None,
+                             None) == 1
