@@ -184,19 +184,22 @@ def cpu_baseline(inp, budget_s: float):
     s = inp.shape
     cores = oracle.default_threads()
     hpg = s.nheads // s.ngroups
-    done, t0 = 0, time.perf_counter()
-    for b, lo, hi in _head_windows(s, cores):
+    windows = list(_head_windows(s, cores))
+    done, rounds, t0 = 0, 0, time.perf_counter()
+    while True:   # cycle over the windows (repeating the workload if it is small) until the budget is spent
+        b, lo, hi = windows[rounds % len(windows)]
         glo, ghi = lo // hpg, (hi - 1) // hpg + 1
         oracle.ssd_fwd_seq(inp.x[b:b + 1, :, lo:hi], inp.dt[b:b + 1, :, lo:hi], inp.A[lo:hi],
                            inp.B[b:b + 1, :, glo:ghi], inp.C[b:b + 1, :, glo:ghi], inp.D[lo:hi],
                            None if inp.h0 is None else inp.h0[b:b + 1, lo:hi], nthreads=cores)
         done += hi - lo
+        rounds += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     el = time.perf_counter() - t0
     tokens_equiv = done * s.seqlen / s.nheads      # (batch, head) pairs -> whole-workload tokens
     return {"value": tokens_equiv / el, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {s.batch * s.nheads} (batch, head) pairs at full length L={s.seqlen}, "
+            "sample": f"{done} (batch, head) pairs (workload has {s.batch * s.nheads}) at full length L={s.seqlen}, "
                       f"sequential float64 recurrence, {el:.1f} s; tokens/s scaled to the whole workload"}
 
 
@@ -279,6 +282,9 @@ def main():
         step()
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    for row in ev:          # torch creates the underlying CUDA event on first record
+        for e in row:
+            e.record(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
