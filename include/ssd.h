@@ -56,7 +56,8 @@ typedef enum {
     SSD_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, negative size, bad dtype, G does not divide nh */
     SSD_ERR_UNSUPPORTED = 2,  /* well-formed problem outside what this build handles (see limits below) */
     SSD_ERR_WORKSPACE = 3,    /* workspace NULL, smaller than ssd_fwd_workspace_size, or not 256-B aligned */
-    SSD_ERR_CUDA = 4          /* a CUDA runtime call or a kernel launch failed; call cudaGetLastError */
+    SSD_ERR_CUDA = 4,         /* a CUDA runtime call or a kernel launch failed; call cudaGetLastError */
+    SSD_ERR_TOO_LARGE = 5     /* ssd_fwd_noalloc: the problem needs more scratch than SSD_NOALLOC_SCRATCH_BYTES */
 } ssd_status;
 
 /* Problem description.  Mirrors the blog's Mamba2ProblemSpec(batch_size,
@@ -156,6 +157,37 @@ ssd_status ssd_state_passing(const ssd_desc *desc, const float *G, const float *
 ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, const void *Bm,
                           const void *Cm, const float *D, const float *G, const void *h_start,
                           void *y, ssd_stream_t stream);
+
+/* ---- Forward pass for callers that cannot allocate device memory ---------
+ * (The pages have no counterpart to this entry point: it is a deployment aid.)
+ *
+ * Some callers cannot call cudaMalloc at the point where they run the forward
+ * pass: code running while a CUDA graph is being captured, allocator-less
+ * embedded runtimes, or plug-ins whose host application owns every device
+ * allocation.  ssd_fwd_noalloc computes exactly what ssd_fwd computes but takes
+ * no workspace argument; it uses a scratch array that is part of libssd.so
+ * itself (a file-scope __device__ array of SSD_NOALLOC_SCRATCH_BYTES bytes, which
+ * every GPU that loads the library holds until the process exits).  The caller
+ * still provides all inputs and outputs.  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *
+ *  - The first call on a device looks up the device address of the array
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture on that device.
+ *  - Problems whose workspace (ssd_fwd_workspace_size) exceeds
+ *    SSD_NOALLOC_SCRATCH_BYTES are rejected with SSD_ERR_TOO_LARGE before
+ *    anything is launched.
+ *  - All calls in the process share the one array per device: calls whose
+ *    executions overlap on the GPU (different streams, or different host
+ *    threads without ordering) race on it and give wrong results.  Order them
+ *    on one stream.  The array keeps the previous call's contents; the forward
+ *    pass writes every scratch byte it reads, so nothing needs clearing.
+ * Arguments, layouts and the other errors are those of ssd_fwd.            */
+#define SSD_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+ssd_status ssd_fwd_noalloc(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                           const void *Bm, const void *Cm, const float *D, const float *h0,
+                           void *y, float *h_final, ssd_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -149,6 +149,7 @@ const char *ssd_status_string(ssd_status s)
     case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: problem size outside what this build handles";
     case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing, too small or not 256-byte aligned";
     case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA call or kernel launch failed";
+    case SSD_ERR_TOO_LARGE: return "SSD_ERR_TOO_LARGE: problem needs more scratch than the built-in no-alloc array";
     }
     return "unknown ssd_status";
 }
@@ -270,3 +271,53 @@ ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, c
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward pass without a caller-provided workspace (ssd_fwd_noalloc).
+//
+// For callers that cannot allocate device memory when they run the forward
+// pass (graph capture in progress, allocator-less runtimes, plug-ins whose host
+// owns all allocations): the scratch lives in this file-scope device array,
+// which every GPU that loads libssd.so keeps for the life of the process.
+// Host code must not hand the array's name to a kernel -- on the host it is
+// only a stand-in symbol -- so the device address is looked up once per device
+// with cudaGetSymbolAddress and cached.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_addr[kMaxDevices];   // device address of g_noalloc_scratch, per device ordinal
+
+// Device address of the scratch array on the current device (nullptr on error).
+void *noalloc_scratch_address()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+        g_noalloc_addr[dev] = p;
+    }
+    return g_noalloc_addr[dev];
+}
+}  // namespace
+
+extern "C" ssd_status ssd_fwd_noalloc(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                                      const void *Bm, const void *Cm, const float *D, const float *h0,
+                                      void *y, float *h_final, ssd_stream_t stream)
+{
+    Problem pr;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    const size_t need = nonempty(pr) ? carve(pr, nullptr).bytes : 0;
+    if (need > SSD_NOALLOC_SCRATCH_BYTES) return SSD_ERR_TOO_LARGE;
+    void *scratch = noalloc_scratch_address();
+    if (!scratch) return SSD_ERR_CUDA;
+    return fwd_impl(desc, x, dt, A, Bm, Cm, D, h0, y, h_final, scratch, SSD_NOALLOC_SCRATCH_BYTES,
+                    (cudaStream_t)stream, nullptr);
+}

@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(5):
+    for code in range(6):
         s = lib.ssd_status_string(code).decode()
         assert s.startswith(_native.STATUS[code])
     assert lib.ssd_status_string(99).decode() == "unknown ssd_status"
