@@ -57,7 +57,8 @@ typedef enum {
     SSD_ERR_UNSUPPORTED = 2,  /* well-formed problem outside what this build handles (see limits below) */
     SSD_ERR_WORKSPACE = 3,    /* workspace NULL, smaller than ssd_fwd_workspace_size, or not 256-B aligned */
     SSD_ERR_CUDA = 4,         /* a CUDA runtime call or a kernel launch failed; call cudaGetLastError */
-    SSD_ERR_TOO_LARGE = 5     /* ssd_fwd_noalloc: the problem needs more scratch than SSD_NOALLOC_SCRATCH_BYTES */
+    SSD_ERR_TOO_LARGE = 5,    /* ssd_fwd_noalloc: the problem needs more scratch than SSD_NOALLOC_SCRATCH_BYTES */
+    SSD_ERR_TIMEOUT = 6       /* ssd_fwd_check: a bounded wait inside a kernel expired; outputs are invalid */
 } ssd_status;
 
 /* Problem description.  Mirrors the blog's Mamba2ProblemSpec(batch_size,
@@ -86,8 +87,9 @@ typedef struct {
 const char *ssd_status_string(ssd_status s);
 
 /* Bytes of device workspace ssd_fwd needs for `desc` (written to *bytes).
- * The workspace holds the in-chunk cumsum G, the local chunk states and the
- * chunk-start states.  Errors: SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED. */
+ * The workspace holds an error word, the in-chunk cumsum G, the local
+ * (super-)chunk states and the (super-)chunk-start states, all float32.
+ * Errors: SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED. */
 ssd_status ssd_fwd_workspace_size(const ssd_desc *desc, size_t *bytes);
 
 /* Whether ssd_fwd runs its chunk_state and chunk_scan stages on the tensor
@@ -119,6 +121,13 @@ ssd_status ssd_fwd_timed(const ssd_desc *desc, const void *x, const void *dt, co
                          float *h_final, void *workspace, size_t ws_bytes, ssd_stream_t stream,
                          ssd_event_t const *events);
 
+/* Synchronises `stream` and reports whether the last ssd_fwd that used
+ * `workspace` hit a bounded device-side wait that expired (SSD_ERR_TIMEOUT:
+ * the outputs of that call are invalid) or completed normally (SSD_OK).  The
+ * tensor-core kernels bound every wait on a barrier (2 s) and record expiry
+ * in the workspace's error word instead of hanging. */
+ssd_status ssd_fwd_check(const void *workspace, ssd_stream_t stream);
+
 /* One recurrent decode step for every (batch, head) (blog section "Mamba-2
  * architecture": the recurrent form suits sequential inference).
  * desc.seqlen and desc.chunk are ignored.  Layouts:
@@ -133,8 +142,9 @@ ssd_status ssd_step(const ssd_desc *desc, const void *x, const void *dt, const f
  * Intermediate layouts (all float32 unless stated):
  *   G        [B][nh][L]          log2(e) * inclusive in-chunk cumsum of A dt
  *   s_local  [B][nh][nc][H][S]   chunk state from a zero start
- *   h_start  [B][nh][nc][H][S]   state entering each chunk, in desc.in_dtype
- *                                 (the dtype the chunk-output contraction reads)
+ *   h_start  [B][nh][nc][H][S]   state entering each chunk (the state dtype,
+ *                                 float32; the chunk-output contraction casts it
+ *                                 to its operand dtype)
  */
 
 /* Stage 1 (blog section "Kernel 1: cumulative sum"): G from dt and A. */
@@ -150,12 +160,12 @@ ssd_status ssd_chunk_state(const ssd_desc *desc, const void *x, const void *dt, 
  * h_start[k] = h_k with h_0 = h0 (NULL: zeros), h_{k+1} = exp2(G_last,k) h_k + s_local[k];
  * h_final (nullable) = h_nc.  s_local and h_start may not overlap. */
 ssd_status ssd_state_passing(const ssd_desc *desc, const float *G, const float *s_local,
-                             const float *h0, void *h_start, float *h_final, ssd_stream_t stream);
+                             const float *h0, float *h_start, float *h_final, ssd_stream_t stream);
 
 /* Stage 4 (blog section "Kernel 3: compute_out"): y from the chunk-start states:
  * Y_k = exp2(G) o (C h_k^T) + ((C B^T) o exp2(G_i - G_j) o [i >= j]) (dt o X) + D X. */
 ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, const void *Bm,
-                          const void *Cm, const float *D, const float *G, const void *h_start,
+                          const void *Cm, const float *D, const float *G, const float *h_start,
                           void *y, ssd_stream_t stream);
 
 /* ---- Forward pass for callers that cannot allocate device memory ---------

@@ -12,10 +12,11 @@ LIB_PATH = os.path.join(_PKG, "_build", "libssd.so")
 SSD_F32, SSD_BF16 = 0, 1
 SSD_FLAG_FORCE_SIMT = 1
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_WORKSPACE",
-          4: "SSD_ERR_CUDA", 5: "SSD_ERR_TOO_LARGE"}
+          4: "SSD_ERR_CUDA", 5: "SSD_ERR_TOO_LARGE", 6: "SSD_ERR_TIMEOUT"}
 
 # Every symbol include/ssd.h declares.
-EXPORTS = ("ssd_status_string", "ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd", "ssd_fwd_timed", "ssd_step",
+EXPORTS = ("ssd_status_string", "ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd", "ssd_fwd_timed", "ssd_fwd_check",
+           "ssd_step",
            "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_fwd_noalloc")
 
 
@@ -67,6 +68,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ssd_state_passing.restype = st
         lib.ssd_chunk_scan.argtypes = [DP] + [P] * 9
         lib.ssd_chunk_scan.restype = st
+        lib.ssd_fwd_check.argtypes = [P, P]
+        lib.ssd_fwd_check.restype = st
         lib.ssd_fwd_noalloc.argtypes = [DP] + [P] * 9 + [P]
         lib.ssd_fwd_noalloc.restype = st
         _lib = lib

@@ -78,12 +78,14 @@ def alloc_workspace(desc: Desc, device) -> torch.Tensor:
 
 
 def ssd_fwd(x, dt, A, B, C, D, chunk: int, h0=None, *, y=None, h_final=None, want_h_final=True,
-            workspace=None, out_dtype=None, flags: int = 0, stream=None, events: Sequence = None):
+            workspace=None, out_dtype=None, flags: int = 0, stream=None, events: Sequence = None,
+            check_errors: bool = False):
     """Chunked SSD forward.  Returns (y, h_final or None).
 
     x [B,L,nh,H], dt [B,L,nh], B/C [B,L,G,S] in float32 or bfloat16 (same dtype);
     A, D [nh] float32; h0 [B,nh,H,S] float32 or None.  ``events`` (8 CUDA events)
     selects ssd_fwd_timed, which records them around the four stages.
+    ``check_errors`` synchronises and raises if a bounded device wait expired.
     """
     desc = desc_for(x, B, chunk, out_dtype, flags)
     batch, seqlen, nheads, headdim = x.shape
@@ -102,6 +104,8 @@ def ssd_fwd(x, dt, A, B, C, D, chunk: int, h0=None, *, y=None, h_final=None, wan
     else:
         arr = (ctypes.c_void_p * 8)(*[e.cuda_event for e in events])
         check("ssd_fwd_timed", lib.ssd_fwd_timed(*args, arr))
+    if check_errors:
+        check("ssd_fwd_check", lib.ssd_fwd_check(_ptr(workspace), _stream(stream)))
     return y, h_final
 
 
@@ -148,7 +152,7 @@ def ssd_state_passing(G, s_local, chunk: int, in_dtype, h0=None, *, ngroups: int
     seqlen = G.shape[2]
     desc = make_desc(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, in_dtype, in_dtype)
     if h_start is None:
-        h_start = torch.empty(s_local.shape, dtype=in_dtype, device=s_local.device)
+        h_start = torch.empty(s_local.shape, dtype=torch.float32, device=s_local.device)
     h_final = torch.empty((batch, nheads, headdim, dstate), dtype=torch.float32,
                           device=s_local.device) if want_h_final else None
     check("ssd_state_passing", _native.load().ssd_state_passing(ctypes.byref(desc), _ptr(G), _ptr(s_local), _ptr(h0),

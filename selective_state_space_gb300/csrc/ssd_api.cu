@@ -3,6 +3,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "ssd_common.cuh"
 #include "ssd_tc.cuh"
 
@@ -50,25 +52,29 @@ ssd_status check_desc(const ssd_desc *d, Problem *pr, bool need_seq)
 
 size_t esize(int dt) { return dt == SSD_BF16 ? 2 : 4; }
 
+// Workspace: [error word | G [B][nh][L] | s_local [B][nh][nc][H][S] | h_start [B][nh][nc][H][S]],
+// all float32, sized for one state per chunk (the largest any path uses).
 struct Workspace {
-    float *G;          // [B][nh][L]
-    float *s_local;    // [B][nh][nc][H][S]
-    void *h_start;     // [B][nh][nc][H][S] in_dtype
+    int *err;
+    float *G;
+    float *s_local;
+    float *h_start;
     size_t bytes;
 };
 
 Workspace carve(const Problem &pr, void *base)
 {
     Workspace w;
+    const size_t e_bytes = kWsAlign;
     const size_t g_bytes = align_up(sizeof(float) * (size_t)(pr.B * pr.nh * pr.L), kWsAlign);
     const size_t states = (size_t)(pr.B * pr.nh * pr.nc * pr.H * pr.S);
     const size_t s_bytes = align_up(sizeof(float) * states, kWsAlign);
-    const size_t h_bytes = align_up(esize(pr.in_dt) * states, kWsAlign);
     char *p = (char *)base;
-    w.G = (float *)p;
-    w.s_local = (float *)(p + g_bytes);
-    w.h_start = (void *)(p + g_bytes + s_bytes);
-    w.bytes = g_bytes + s_bytes + h_bytes;
+    w.err = (int *)p;
+    w.G = (float *)(p + e_bytes);
+    w.s_local = (float *)(p + e_bytes + g_bytes);
+    w.h_start = (float *)(p + e_bytes + g_bytes + s_bytes);
+    w.bytes = e_bytes + g_bytes + 2 * s_bytes;
     return w;
 }
 
@@ -80,6 +86,56 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 }
 
 ssd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
+
+bool use_tensor_cores(const ssd_desc *desc, const Problem &pr)
+{
+    return !(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr);
+}
+
+int device_sms()
+{
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Chunks per super-chunk for the tensor-core path.  Each scan CTA walks one
+// super-chunk of one (batch, head, 64-column block); more super-chunks give more
+// CTAs but cost an extra read of x and B (the chunk_state pass) and state traffic.
+// Pick the count that minimises estimated bytes / wave efficiency (one CTA per SM).
+int choose_chunks_per_super(const Problem &pr)
+{
+    const double sms = (double)device_sms();
+    const double es = (double)esize(pr.in_dt);
+    const double units1 = (double)(pr.B * pr.nh * (pr.H / 64));
+    const double x_bytes = (double)(pr.B * pr.L * pr.nh * pr.H) * es;
+    const double bc_bytes = (double)(pr.B * pr.L * pr.G * pr.S) * es;
+    const double alg = 2.0 * x_bytes + 2.0 * bc_bytes;
+    const double state_bytes = (double)(pr.B * pr.nh * pr.H * pr.S) * 4.0;
+    int best_R = (int)pr.nc;
+    double best = 1e300;
+    const int max_sup = (int)(pr.nc < 256 ? pr.nc : 256);
+    for (int want = 1; want <= max_sup; ++want) {
+        const int R = (int)((pr.nc + want - 1) / want);
+        if (R > 256) continue;
+        const int nsup = (int)((pr.nc + R - 1) / R);
+        const double units = units1 * nsup;
+        const double waves = units / sms;
+        const double eff = waves / ceil(waves);
+        const double extra = (nsup - 1.0) / nsup * (x_bytes + bc_bytes) + 4.0 * (nsup - 1.0) * state_bytes;
+        const double cost = (alg + extra) / eff;
+        if (cost < best * 0.999) { best = cost; best_R = R; }
+    }
+    return best_R;
+}
 
 ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const float *A,
                     const void *Bm, const void *Cm, const float *D, const float *h0, void *y,
@@ -115,23 +171,36 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
     Workspace w = carve(pr, workspace);
     if (!workspace || !aligned(workspace, kWsAlign) || ws_bytes < w.bytes) return SSD_ERR_WORKSPACE;
 
-    const bool use_tc = !(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr);
-    auto rec = [&](int i) -> cudaError_t { return events ? cudaEventRecord((cudaEvent_t)events[i], st) : cudaSuccess; };
-    cudaError_t e;
-    if ((e = rec(0)) != cudaSuccess) return SSD_ERR_CUDA;
-    if ((e = ssd::launch_chunk_cumsum(pr, dt, A, w.G, st)) != cudaSuccess) return SSD_ERR_CUDA;
-    if ((e = rec(1)) != cudaSuccess || (e = rec(2)) != cudaSuccess) return SSD_ERR_CUDA;
-    e = use_tc ? ssd::launch_chunk_state_tc(pr, x, dt, Bm, w.G, w.s_local, st)
-               : ssd::launch_chunk_state_simt(pr, x, dt, Bm, w.G, w.s_local, st);
-    if (e != cudaSuccess) return SSD_ERR_CUDA;
-    if ((e = rec(3)) != cudaSuccess || (e = rec(4)) != cudaSuccess) return SSD_ERR_CUDA;
-    if ((e = ssd::launch_state_passing(pr, w.G, w.s_local, h0, w.h_start, h_final, st)) != cudaSuccess)
+    auto rec = [&](int i) -> bool { return !events || cudaEventRecord((cudaEvent_t)events[i], st) == cudaSuccess; };
+    if (cudaMemsetAsync(w.err, 0, sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
+    if (!rec(0) || ssd::launch_chunk_cumsum(pr, dt, A, w.G, st) != cudaSuccess || !rec(1)) return SSD_ERR_CUDA;
+
+    if (use_tensor_cores(desc, pr)) {
+        const int R = choose_chunks_per_super(pr);
+        const int nsup = (int)((pr.nc + R - 1) / R);
+        // states of super-chunks 0 .. nsup-2 (the last one's state is produced by the scan)
+        if (!rec(2)) return SSD_ERR_CUDA;
+        if (nsup > 1 && ssd::launch_chunk_state_tc(pr, x, dt, Bm, w.G, w.s_local, R, nsup, nsup - 1, w.err, st) != cudaSuccess)
+            return SSD_ERR_CUDA;
+        if (!rec(3) || !rec(4)) return SSD_ERR_CUDA;
+        if (nsup > 1 &&
+            ssd::launch_state_passing(pr, w.G, w.s_local, h0, w.h_start, nullptr, R, nsup, nsup - 1, st) != cudaSuccess)
+            return SSD_ERR_CUDA;
+        if (!rec(5) || !rec(6)) return SSD_ERR_CUDA;
+        if (ssd::launch_chunk_scan_tc(pr, x, dt, Bm, Cm, D, w.G, h0, w.h_start, h_final, y, R, nsup, 1, w.err, st) !=
+            cudaSuccess)
+            return SSD_ERR_CUDA;
+        if (!rec(7)) return SSD_ERR_CUDA;
+        return SSD_OK;
+    }
+    const int nc = (int)pr.nc;
+    if (!rec(2) || ssd::launch_chunk_state_simt(pr, x, dt, Bm, w.G, w.s_local, st) != cudaSuccess || !rec(3))
         return SSD_ERR_CUDA;
-    if ((e = rec(5)) != cudaSuccess || (e = rec(6)) != cudaSuccess) return SSD_ERR_CUDA;
-    e = use_tc ? ssd::launch_chunk_scan_tc(pr, x, dt, Bm, Cm, D, w.G, w.h_start, y, st)
-               : ssd::launch_chunk_scan_simt(pr, x, dt, Bm, Cm, D, w.G, w.h_start, y, st);
-    if (e != cudaSuccess) return SSD_ERR_CUDA;
-    if ((e = rec(7)) != cudaSuccess) return SSD_ERR_CUDA;
+    if (!rec(4) || ssd::launch_state_passing(pr, w.G, w.s_local, h0, w.h_start, h_final, 1, nc, nc, st) != cudaSuccess ||
+        !rec(5))
+        return SSD_ERR_CUDA;
+    if (!rec(6) || ssd::launch_chunk_scan_simt(pr, x, dt, Bm, Cm, D, w.G, w.h_start, y, st) != cudaSuccess || !rec(7))
+        return SSD_ERR_CUDA;
     return SSD_OK;
 }
 
@@ -150,6 +219,7 @@ const char *ssd_status_string(ssd_status s)
     case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing, too small or not 256-byte aligned";
     case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA call or kernel launch failed";
     case SSD_ERR_TOO_LARGE: return "SSD_ERR_TOO_LARGE: problem needs more scratch than the built-in no-alloc array";
+    case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: a bounded wait inside a kernel expired; results are invalid";
     }
     return "unknown ssd_status";
 }
@@ -170,7 +240,7 @@ ssd_status ssd_fwd_path(const ssd_desc *desc, int32_t *uses_tensor_cores)
     if (!uses_tensor_cores) return SSD_ERR_INVALID_ARG;
     ssd_status s = check_desc(desc, &pr, true);
     if (s != SSD_OK) return s;
-    *uses_tensor_cores = (!(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr)) ? 1 : 0;
+    *uses_tensor_cores = use_tensor_cores(desc, pr) ? 1 : 0;
     return SSD_OK;
 }
 
@@ -192,6 +262,16 @@ ssd_status ssd_fwd_timed(const ssd_desc *desc, const void *x, const void *dt, co
         if (!events[i]) return SSD_ERR_INVALID_ARG;
     return fwd_impl(desc, x, dt, A, Bm, Cm, D, h0, y, h_final, workspace, ws_bytes,
                     (cudaStream_t)stream, events);
+}
+
+ssd_status ssd_fwd_check(const void *workspace, ssd_stream_t stream)
+{
+    if (!workspace || !aligned(workspace, kWsAlign)) return SSD_ERR_INVALID_ARG;
+    int word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess ||
+        cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    return word ? SSD_ERR_TIMEOUT : SSD_OK;
 }
 
 ssd_status ssd_step(const ssd_desc *desc, const void *x, const void *dt, const float *A,
@@ -230,14 +310,15 @@ ssd_status ssd_chunk_state(const ssd_desc *desc, const void *x, const void *dt, 
     if (!x || !dt || !Bm || !G || !s_local) return SSD_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(Bm, 16) || !aligned(G, 16) || !aligned(s_local, 16))
         return SSD_ERR_INVALID_ARG;
-    const bool use_tc = !(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr);
-    cudaError_t e = use_tc ? ssd::launch_chunk_state_tc(pr, x, dt, Bm, G, s_local, (cudaStream_t)stream)
-                           : ssd::launch_chunk_state_simt(pr, x, dt, Bm, G, s_local, (cudaStream_t)stream);
+    const int nc = (int)pr.nc;
+    cudaError_t e = use_tensor_cores(desc, pr)
+                        ? ssd::launch_chunk_state_tc(pr, x, dt, Bm, G, s_local, 1, nc, nc, nullptr, (cudaStream_t)stream)
+                        : ssd::launch_chunk_state_simt(pr, x, dt, Bm, G, s_local, (cudaStream_t)stream);
     return cuda_status(e);
 }
 
 ssd_status ssd_state_passing(const ssd_desc *desc, const float *G, const float *s_local,
-                             const float *h0, void *h_start, float *h_final, ssd_stream_t stream)
+                             const float *h0, float *h_start, float *h_final, ssd_stream_t stream)
 {
     Problem pr;
     ssd_status s = check_desc(desc, &pr, true);
@@ -248,12 +329,13 @@ ssd_status ssd_state_passing(const ssd_desc *desc, const float *G, const float *
         (h0 && !aligned(h0, 4)) || (h_final && !aligned(h_final, 4)))
         return SSD_ERR_INVALID_ARG;
     const size_t states = (size_t)(pr.B * pr.nh * pr.nc * pr.H * pr.S);
-    if (overlaps(s_local, states * 4, h_start, states * esize(pr.in_dt))) return SSD_ERR_INVALID_ARG;
-    return cuda_status(ssd::launch_state_passing(pr, G, s_local, h0, h_start, h_final, (cudaStream_t)stream));
+    if (overlaps(s_local, states * 4, h_start, states * 4)) return SSD_ERR_INVALID_ARG;
+    const int nc = (int)pr.nc;
+    return cuda_status(ssd::launch_state_passing(pr, G, s_local, h0, h_start, h_final, 1, nc, nc, (cudaStream_t)stream));
 }
 
 ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, const void *Bm,
-                          const void *Cm, const float *D, const float *G, const void *h_start,
+                          const void *Cm, const float *D, const float *G, const float *h_start,
                           void *y, ssd_stream_t stream)
 {
     Problem pr;
@@ -264,9 +346,15 @@ ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, c
     if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(Bm, 16) || !aligned(Cm, 16) || !aligned(G, 16) ||
         !aligned(h_start, 16) || !aligned(y, 16) || !aligned(D, 4))
         return SSD_ERR_INVALID_ARG;
-    const bool use_tc = !(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr);
-    cudaError_t e = use_tc ? ssd::launch_chunk_scan_tc(pr, x, dt, Bm, Cm, D, G, h_start, y, (cudaStream_t)stream)
-                           : ssd::launch_chunk_scan_simt(pr, x, dt, Bm, Cm, D, G, h_start, y, (cudaStream_t)stream);
+    // one chunk per scan unit: chunk k starts from h_start[k] (chunk 0 included)
+    const int nc = (int)pr.nc;
+    cudaError_t e;
+    if (use_tensor_cores(desc, pr)) {
+        e = ssd::launch_chunk_scan_tc(pr, x, dt, Bm, Cm, D, G, nullptr, h_start, nullptr, y, 1, nc, 0, nullptr,
+                                      (cudaStream_t)stream);
+    } else {
+        e = ssd::launch_chunk_scan_simt(pr, x, dt, Bm, Cm, D, G, h_start, y, (cudaStream_t)stream);
+    }
     return cuda_status(e);
 }
 
@@ -283,8 +371,6 @@ ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, c
 // only a stand-in symbol -- so the device address is looked up once per device
 // with cudaGetSymbolAddress and cached.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BYTES];
 
 namespace {

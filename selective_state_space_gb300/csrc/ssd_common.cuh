@@ -34,11 +34,13 @@ cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *
 cudaError_t launch_chunk_state_simt(const Problem &pr, const void *x, const void *dt,
                                     const void *Bm, const float *G, float *s_local,
                                     cudaStream_t st);
-cudaError_t launch_state_passing(const Problem &pr, const float *G, const float *s_local,
-                                 const float *h0, void *h_start, float *h_final, cudaStream_t st);
+// Super-chunk state passing: h_start[m] for m < nsup (R chunks per super-chunk);
+// s_local is read for m < nm; h_final (nullable) is written when nm == nsup.
+cudaError_t launch_state_passing(const Problem &pr, const float *G, const float *s_local, const float *h0,
+                                 float *h_start, float *h_final, int R, int nsup, int nm, cudaStream_t st);
 cudaError_t launch_chunk_scan_simt(const Problem &pr, const void *x, const void *dt,
                                    const void *Bm, const void *Cm, const float *D, const float *G,
-                                   const void *h_start, void *y, cudaStream_t st);
+                                   const float *h_start, void *y, cudaStream_t st);
 cudaError_t launch_ssd_step(const Problem &pr, const void *x, const void *dt, const float *A,
                             const void *Bm, const void *Cm, const float *D, float *h, void *y,
                             cudaStream_t st);

@@ -8,6 +8,10 @@
 // Method: NVIDIA developer blog "Accelerating Mamba-2 with High-Performance
 // Forward Pass Kernels in NVIDIA CUDA Tile", sections "Mamba-2 architecture"
 // and "Kernel 1" .. "Kernel 3".
+#include <string.h>
+
+#include <type_traits>
+
 #include "ssd_common.cuh"
 
 namespace ssd {
@@ -132,33 +136,59 @@ k_chunk_state_simt(const Tin *__restrict__ x, const Tin *__restrict__ dt,
 
 // ---------------------------------------------------------------------------
 // Stage 3 -- state_passing (blog section "Kernel 2: fwd_pass_state", the
-// sequential loop over chunks).  One thread per state element, walking the
-// chunks in order: store h_k, then h_{k+1} = exp2(G_last,k) h_k + s_local[k].
-// Consecutive threads own consecutive elements, so every step is coalesced.
+// sequential loop over chunks), generalised to super-chunks of R chunks:
+//   h_start[m] = h_m,  h_{m+1} = exp2(sum_{k in m} G_last,k) h_m + s_local[m],
+// for m = 0 .. nsup-1 starting from h0 (NULL: zeros); s_local is read for m < nm
+// only and h_final = h_nm is written when nm == nsup (and h_final is not NULL).
+// With R = 1 this is the blog's per-chunk loop.  VEC consecutive state elements
+// per thread (float4 when H*S allows), consecutive threads on consecutive
+// elements: every step is a coalesced 128-bit stream.
 // ---------------------------------------------------------------------------
-template <typename Tst>
+template <int VEC>
 __global__ void __launch_bounds__(256)
 k_state_passing(const float *__restrict__ G, const float *__restrict__ s_local,
-                const float *__restrict__ h0, Tst *__restrict__ h_start,
-                float *__restrict__ h_final, Problem pr)
+                const float *__restrict__ h0, float *__restrict__ h_start,
+                float *__restrict__ h_final, Problem pr, int R, int nsup, int nm)
 {
+    using V = typename std::conditional<VEC == 4, float4, float>::type;
     const int64_t HS = pr.H * pr.S;
-    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t e = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * VEC;
     const int h = blockIdx.y, b = blockIdx.z;
     if (e >= HS) return;
     const int64_t bh = (int64_t)b * pr.nh + h;
-    float st = h0 ? h0[bh * HS + e] : 0.f;
-    const float *Gh = G + bh * pr.L;
-    const int64_t base = bh * pr.nc * HS + e;
-    float s_next = s_local[base];
-    for (int64_t k = 0; k < pr.nc; ++k) {
-        const float s = s_next;
-        if (k + 1 < pr.nc) s_next = s_local[base + (k + 1) * HS];   // prefetch the next chunk
-        h_start[base + k * HS] = from_f32<Tst>(st);
-        const int64_t last = min(pr.L, (k + 1) * pr.T) - 1;
-        st = fmaf(exp2f(Gh[last]), st, s);
+    float st[VEC];
+    if (h0) {
+        const V v = *reinterpret_cast<const V *>(h0 + bh * HS + e);
+        memcpy(st, &v, sizeof(V));
+    } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) st[i] = 0.f;
     }
-    if (h_final) h_final[bh * HS + e] = st;
+    const float *Gh = G + bh * pr.L;
+    const int64_t base = bh * nsup * HS + e;
+    V s_next;
+    if (nm > 0) s_next = *reinterpret_cast<const V *>(s_local + base);
+    for (int m = 0; m < nsup; ++m) {
+        V out;
+        memcpy(&out, st, sizeof(V));
+        *reinterpret_cast<V *>(h_start + base + (int64_t)m * HS) = out;
+        if (m >= nm) continue;
+        const V sv = s_next;
+        if (m + 1 < nm) s_next = *reinterpret_cast<const V *>(s_local + base + (int64_t)(m + 1) * HS);   // prefetch
+        float dec = 0.f;
+        const int k1 = min((int)pr.nc, (m + 1) * R);
+        for (int k = m * R; k < k1; ++k) dec += Gh[min(pr.L, (int64_t)(k + 1) * pr.T) - 1];
+        const float a = exp2f(dec);
+        float sa[VEC];
+        memcpy(sa, &sv, sizeof(V));
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) st[i] = fmaf(a, st[i], sa[i]);
+    }
+    if (h_final && nm == nsup) {
+        V out;
+        memcpy(&out, st, sizeof(V));
+        *reinterpret_cast<V *>(h_final + bh * HS + e) = out;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -175,7 +205,7 @@ __global__ void __launch_bounds__(256)
 k_chunk_scan_simt(const Tin *__restrict__ x, const Tin *__restrict__ dt,
                   const Tin *__restrict__ Bm, const Tin *__restrict__ Cm,
                   const float *__restrict__ D, const float *__restrict__ G,
-                  const Tin *__restrict__ h_start, Tout *__restrict__ y, Problem pr,
+                  const float *__restrict__ h_start, Tout *__restrict__ y, Problem pr,
                   int rtiles, int ptiles)
 {
     extern __shared__ float smem[];
@@ -252,12 +282,12 @@ k_chunk_scan_simt(const Tin *__restrict__ x, const Tin *__restrict__ dt,
         }
     }
     // carried-state term: C_i . h_k[p]
-    const Tin *hk = h_start + ((((int64_t)b * pr.nh + h) * pr.nc + k) * pr.H) * pr.S;
+    const float *hk = h_start + ((((int64_t)b * pr.nh + h) * pr.nc + k) * pr.H) * pr.S;
     for (int ss = 0; ss < pr.S; ss += 32) {
         __syncthreads();
         for (int pp = warp; pp < kScanCols; pp += 8) {
             const int p = p0 + pp, s = ss + lane;
-            Hs[pp * 33 + lane] = (p < pr.H && s < pr.S) ? to_f32(hk[(int64_t)p * pr.S + s]) : 0.f;
+            Hs[pp * 33 + lane] = (p < pr.H && s < pr.S) ? hk[(int64_t)p * pr.S + s] : 0.f;
         }
         __syncthreads();
         const int send = min(32, (int)pr.S - ss);
@@ -353,21 +383,24 @@ cudaError_t launch_chunk_state_simt(const Problem &pr, const void *x, const void
     return cudaGetLastError();
 }
 
-cudaError_t launch_state_passing(const Problem &pr, const float *G, const float *s_local,
-                                 const float *h0, void *h_start, float *h_final, cudaStream_t st)
+cudaError_t launch_state_passing(const Problem &pr, const float *G, const float *s_local, const float *h0,
+                                 float *h_start, float *h_final, int R, int nsup, int nm, cudaStream_t st)
 {
     const int64_t HS = pr.H * pr.S;
-    dim3 grid((unsigned)((HS + 255) / 256), (unsigned)pr.nh, (unsigned)pr.B);
-    if (pr.in_dt == SSD_BF16)
-        k_state_passing<__nv_bfloat16><<<grid, 256, 0, st>>>(G, s_local, h0, (__nv_bfloat16 *)h_start, h_final, pr);
+    const bool v4 = (HS % 4 == 0) && ((uintptr_t)s_local % 16 == 0) && ((uintptr_t)h_start % 16 == 0) &&
+                    (!h0 || (uintptr_t)h0 % 16 == 0) && (!h_final || (uintptr_t)h_final % 16 == 0);
+    const int vec = v4 ? 4 : 1;
+    dim3 grid((unsigned)((HS / vec + 255) / 256), (unsigned)pr.nh, (unsigned)pr.B);
+    if (v4)
+        k_state_passing<4><<<grid, 256, 0, st>>>(G, s_local, h0, h_start, h_final, pr, R, nsup, nm);
     else
-        k_state_passing<float><<<grid, 256, 0, st>>>(G, s_local, h0, (float *)h_start, h_final, pr);
+        k_state_passing<1><<<grid, 256, 0, st>>>(G, s_local, h0, h_start, h_final, pr, R, nsup, nm);
     return cudaGetLastError();
 }
 
 template <typename Tin, typename Tout>
 static cudaError_t scan_launch(const Problem &pr, const void *x, const void *dt, const void *Bm,
-                               const void *Cm, const float *D, const float *G, const void *h_start,
+                               const void *Cm, const float *D, const float *G, const float *h_start,
                                void *y, cudaStream_t st)
 {
     const int rtiles = (int)((pr.T + kScanRows - 1) / kScanRows);
@@ -378,13 +411,13 @@ static cudaError_t scan_launch(const Problem &pr, const void *x, const void *dt,
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(pr.nc * rtiles), (unsigned)(pr.nh * ptiles), (unsigned)pr.B);
     kern<<<grid, 256, smem, st>>>((const Tin *)x, (const Tin *)dt, (const Tin *)Bm, (const Tin *)Cm, D, G,
-                                  (const Tin *)h_start, (Tout *)y, pr, rtiles, ptiles);
+                                  h_start, (Tout *)y, pr, rtiles, ptiles);
     return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_scan_simt(const Problem &pr, const void *x, const void *dt,
                                    const void *Bm, const void *Cm, const float *D, const float *G,
-                                   const void *h_start, void *y, cudaStream_t st)
+                                   const float *h_start, void *y, cudaStream_t st)
 {
     const bool ib = pr.in_dt == SSD_BF16, ob = pr.out_dt == SSD_BF16;
     if (ib && ob) return scan_launch<__nv_bfloat16, __nv_bfloat16>(pr, x, dt, Bm, Cm, D, G, h_start, y, st);

@@ -9,10 +9,17 @@ namespace ssd {
 // True when the tensor-core kernels handle this problem shape.
 bool tc_supported(const Problem &pr);
 
+// States of super-chunks m < nm (R chunks each) from a zero start, written to
+// s_local[b][h][m] with a super-chunk extent of nsup.  `err` receives error bits.
 cudaError_t launch_chunk_state_tc(const Problem &pr, const void *x, const void *dt, const void *Bm,
-                                  const float *G, float *s_local, cudaStream_t st);
+                                  const float *G, float *s_local, int R, int nsup, int nm, int *err,
+                                  cudaStream_t st);
+// Output y for every super-chunk (R chunks, nsup of them): super-chunks m < hs_from
+// start from h0 (NULL: zeros), the others from h_start[b][h][m]; the last super-chunk
+// also writes h_final when it is not NULL.
 cudaError_t launch_chunk_scan_tc(const Problem &pr, const void *x, const void *dt, const void *Bm,
-                                 const void *Cm, const float *D, const float *G, const void *h_start,
-                                 void *y, cudaStream_t st);
+                                 const void *Cm, const float *D, const float *G, const float *h0,
+                                 const float *h_start, float *h_final, void *y, int R, int nsup, int hs_from,
+                                 int *err, cudaStream_t st);
 
 }  // namespace ssd

@@ -24,21 +24,41 @@ PATHS = {"default": 0, "simt": SSD_FLAG_FORCE_SIMT}
 def run_fwd(inp, flags=0, chunk=None):
     d = to_dev(inp)
     y, hf = api.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], chunk or inp.shape.chunk, d["h0"],
-                        flags=flags)
+                        flags=flags, check_errors=True)
     torch.cuda.synchronize()
     return y, hf
 
 
+def tc_path(shape, flags=0):
+    desc = api.make_desc(shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate, shape.ngroups,
+                         shape.chunk, workloads.torch_dtype(shape.dtype), workloads.torch_dtype(shape.dtype), flags)
+    return api.uses_tensor_cores(desc)
+
+
+# Shapes the oracle finishes in seconds; several 128-row tiles, several chunks and
+# super-chunks, ragged tails, groups > 1, both state widths and both head widths.
 SMALL = [
     workloads.WORKLOADS[0],
     workloads.custom(2, 512, 6, 64, 128, 1, 256, "bf16", h0_recipe="normal", seed=11, name="c1-small"),
+    workloads.custom(1, 1536, 8, 64, 128, 2, 256, "bf16", dt_zero_frac=0.05, seed=12, name="c3-small"),
     workloads.custom(1, 700, 8, 64, 128, 2, 256, "bf16", dt_zero_frac=0.05, seed=12, name="c3-ragged"),
-    workloads.custom(2, 300, 4, 128, 256, 2, 128, "bf16", dt_recipe="loguniform", a_range=(0.5, 8.0),
+    workloads.custom(2, 384, 4, 128, 256, 2, 128, "bf16", dt_recipe="loguniform", a_range=(0.5, 8.0),
                      seed=13, name="c4-small"),
-    workloads.custom(1, 200, 4, 64, 128, 1, 128, "bf16", seed=14, name="blog-small"),
+    workloads.custom(2, 300, 4, 128, 256, 2, 128, "bf16", dt_recipe="loguniform", a_range=(0.5, 8.0),
+                     seed=13, name="c4-ragged"),
+    workloads.custom(1, 640, 4, 64, 128, 1, 128, "bf16", h0_recipe="normal", seed=14, name="blog-small"),
+    workloads.custom(1, 256, 2, 128, 128, 1, 256, "bf16", seed=17, name="h128-s128"),
+    workloads.custom(1, 256, 2, 64, 256, 1, 128, "bf16", seed=18, name="h64-s256"),
     workloads.custom(2, 77, 6, 8, 16, 3, 16, "f32", h0_recipe="normal", seed=15, name="odd-f32"),
     workloads.custom(1, 33, 2, 1, 1, 1, 1, "f32", seed=16, name="scalar-T1"),
 ]
+
+
+def test_tensor_core_path_selected_for_bf16_layer_shapes():
+    for shape in workloads.WORKLOADS[1:] + [workloads.BLOG_SHAPE]:
+        assert tc_path(shape), shape.name
+        assert not tc_path(shape, SSD_FLAG_FORCE_SIMT)
+    assert not tc_path(workloads.WORKLOADS[0])   # float32 inputs run on the CUDA cores
 
 
 @pytest.mark.parametrize("path", sorted(PATHS))
@@ -66,8 +86,19 @@ def test_fwd_full_size_sampled_pairs(shape):
     assert torch.isfinite(y.float()).all() and torch.isfinite(hf).all()
 
 
-def test_stages_against_oracle_intermediates():
-    shape = workloads.custom(2, 640, 4, 64, 128, 2, 256, "bf16", h0_recipe="normal", seed=21)
+STAGE_SHAPES = [
+    workloads.custom(2, 768, 4, 64, 128, 2, 256, "bf16", h0_recipe="normal", seed=21, name="stages-t256"),
+    workloads.custom(1, 512, 2, 128, 256, 1, 128, "bf16", dt_recipe="loguniform", a_range=(0.5, 8.0),
+                     h0_recipe="normal", seed=22, name="stages-wide"),
+    workloads.custom(2, 640, 4, 64, 128, 2, 256, "bf16", h0_recipe="normal", seed=23, name="stages-ragged"),
+]
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("shape", STAGE_SHAPES, ids=lambda s: s.name)
+def test_stages_against_oracle_intermediates(shape, path):
+    """Each stage of the pipeline on its own, against the oracle's chunked-form intermediates."""
+    flags = PATHS[path]
     inp = workloads.make_inputs(shape)
     t = inp.tensors()
     y_ref, hf_ref, g_ref, s_ref, hs_ref = oracle.ssd_fwd_chunked(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"],
@@ -78,16 +109,16 @@ def test_stages_against_oracle_intermediates():
     torch.cuda.synchronize()
     # G holds log2(e) * cumsum; compare in natural-log units
     assert rel_max_err(G.double() * np.log(2.0), g_ref) <= 1e-5
-    s_loc = api.ssd_chunk_state(d["x"], d["dt"], d["B"], G, T)
+    s_loc = api.ssd_chunk_state(d["x"], d["dt"], d["B"], G, T, flags=flags)
     torch.cuda.synchronize()
     assert rel_max_err(s_loc, s_ref) <= TOL["bf16"]
     h_start, h_final = api.ssd_state_passing(G, s_loc, T, torch.bfloat16, d["h0"], ngroups=shape.ngroups)
     torch.cuda.synchronize()
     assert rel_max_err(h_start, hs_ref) <= TOL["bf16"]
     assert rel_max_err(h_final, hf_ref) <= TOL["bf16"]
-    # chunk_scan alone, fed the oracle's chunk-start states (cast to the operand dtype)
-    hs_dev = torch.from_numpy(hs_ref).to(torch.bfloat16).cuda()
-    y = api.ssd_chunk_scan(d["x"], d["dt"], d["B"], d["C"], d["D"], G, hs_dev, T)
+    # chunk_scan alone, fed the oracle's chunk-start states
+    hs_dev = torch.from_numpy(hs_ref).float().cuda()
+    y = api.ssd_chunk_scan(d["x"], d["dt"], d["B"], d["C"], d["D"], G, hs_dev, T, flags=flags)
     torch.cuda.synchronize()
     assert rel_max_err(y, y_ref) <= TOL["bf16"]
 
