@@ -58,15 +58,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase)
     return ok != 0;
 }
 
-// Wait for the phase with parity `phase` to complete; false after `limit_ns`.
+// Wait for the phase with parity `phase` to complete; false once about `limit_ns` has
+// passed.  The bound is kept in SM clock cycles (cheap to read; 2.5 cycles per ns covers
+// clocks up to 2.5 GHz, so at lower clocks the bound is longer, never shorter) and is
+// checked every 64 polls so that polling stays tight.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, phase)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long c0 = clock64();
+    const long long limit = (long long)(limit_ns * 5 / 2);
+    uint32_t spins = 0;
     while (!mbar_try_wait(bar, phase)) {
-        if (globaltimer_ns() - t0 > limit_ns) return false;
+        if ((++spins & 63u) == 0 && clock64() - c0 > limit) return false;
     }
     return true;
+}
+
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32): relative error near
+// 2^-22, results below 2^-126 flushed to zero.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // ---- proxy fences -------------------------------------------------------------
@@ -103,6 +117,22 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
+
+// Bulk tensor store shared -> global (bulk-group completion).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until the shared-memory sources of all committed bulk stores have been read.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Wait until all committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 {

@@ -56,7 +56,10 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u)
 // 128-byte rows with the 128-byte swizzle (the layout TMA writes and the MMA reads).
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + (((c ^ (r & 7u)) & 7u) << 4); }
 
-__device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads)
+// Hardware barrier among `nthreads` threads (named barrier `id`).  Callers keep their
+// control flow uniform -- every participating thread reaches every call, errors or
+// not -- so this never waits on a thread that left.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -237,8 +240,14 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
 // The state lives in TMEM as h^T (lanes s, columns p); a bf16 copy [s][p] in shared
 // memory is the B operand of Ys.  G is the chunk-relative log2 cumsum; G_base is G
 // at the token before the sub-chunk (0 at a chunk start).
-// Warp 0: TMA.  Warp 1: MMA issue and TMEM allocation.  Warps 2..: CUDA-core work,
-// 4*NW warps, NW per TMEM lane quarter, splitting columns.
+//
+// Warp roles: warp 0 issues TMA, warp 1 issues every MMA (and owns TMEM).
+// Warps 2..5 ("state group") hand the state over between sub-chunks and scale the
+// x tile (dt o x in place, w o x into its own tile).  Warps 6..13 ("output group",
+// two warps per TMEM lane quarter splitting the columns) build P and write y.  The two groups run concurrently; the MMA issue order
+// (CB, Ys, state update, Yi, next CB) lets the state chain advance without
+// waiting for P.  Ys/Yi are double-buffered in TMEM so the next sub-chunk's Ys can
+// start while the output group drains the previous one.
 // ===========================================================================
 template <int S>
 struct ScanCfg {
@@ -250,32 +259,32 @@ struct ScanCfg {
     static constexpr uint32_t kXw = kStages * kStage;        // w o x   [t][p]
     static constexpr uint32_t kP = kXw + kAtom;              // P       [i][j], 2 K-atoms
     static constexpr uint32_t kH = kP + 2 * kAtom;           // h bf16  [s][p], S rows
-    static constexpr uint32_t kSmall = kH + S * 128;         // sG[128], sdt[128]
+    static constexpr uint32_t kSmall = kH + S * 128;         // sG[128], sF[128] (output group)
     static constexpr uint32_t kBars = kSmall + 2 * kQ * 4;
     static constexpr uint32_t kSmem = kBars + 256 + 1024;
-    // TMEM columns
-    static constexpr uint32_t kTcb = 0, kTys = 128, kTyi = 192, kTds = 256;
+    // TMEM columns: CB, Ys/Yi in two buffers, state (S/128 blocks of 64 columns)
+    static constexpr uint32_t kTcb = 0, kTys = 128, kTyi = 192, kTyStride = 128, kTds = 384;
     static constexpr uint32_t kTmemCols = 512;
 };
 
-// kGroup: barrier among the CUDA-core warps only (an mbarrier, so its wait is bounded)
-enum ScanBar { kFull0 = 0, kFree0 = 2, kCb = 4, kHReady, kXReady, kPReady, kIntra, kUpdate, kEpi, kGroup, kNumScanBars };
+enum ScanBar {
+    kFull0 = 0, kFree0 = 2, kCb = 4, kHReady, kXReady, kPReady, kIntra, kUpdate, kEpi0, kEpi1, kOutGroup,
+    kYSt0, kYSt1, kNumScanBars
+};
 
-template <int S, int NW>
-__global__ void __launch_bounds__(64 + 128 * NW, 1)
+template <int S>
+__global__ void __launch_bounds__(448, 1)
 k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmX, const float *__restrict__ G,
-                const __nv_bfloat16 *__restrict__ dt, const float *__restrict__ Dp,
-                const float *__restrict__ h0, const float *__restrict__ h_start, float *__restrict__ h_final,
+                const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+                const float *__restrict__ G, const __nv_bfloat16 *__restrict__ dt, const float *__restrict__ Dp,
+                const float *__restrict__ h0,
+                const float *__restrict__ h_start, float *__restrict__ h_final,
                 __nv_bfloat16 *__restrict__ y, Problem pr, int R, int nsup, int hs_from, int *err)
 {
     using Cfg = ScanCfg<S>;
-    constexpr int kSimt = 128 * NW;
-    constexpr int kCols = kPB / NW;                  // p columns per CUDA-core thread
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float *sG = (float *)(smem + Cfg::kSmall);
-    float *sdt = sG + kQ;
     uint64_t *bars = (uint64_t *)(smem + Cfg::kBars);
     uint32_t *tmem_slot = (uint32_t *)(bars + kNumScanBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -299,7 +308,8 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumScanBars; ++i) {
             uint32_t cnt = 1;
-            if (i == kHReady || i == kXReady || i == kPReady || i == kEpi || i == kGroup) cnt = kSimt;
+            if (i == kHReady || i == kXReady) cnt = 128;                                  // state group
+            if (i == kPReady || i == kEpi0 || i == kEpi1 || i == kOutGroup) cnt = 256;    // output group
             mbar_init(smem_u32(&bars[i]), cnt);
         }
         fence_mbar_init();
@@ -312,14 +322,17 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
     bool ok = true;
 
     if (warp == 0) {
+        // ---- TMA producer ---------------------------------------------------------------
         if (lane == 0) {
             prefetch_tmap(&tmC);
             prefetch_tmap(&tmB);
             prefetch_tmap(&tmX);
             for (int q = 0; q < nq && ok; ++q) {
                 const int st = q % Cfg::kStages;
+                // the stage is free once its MMAs completed and the y tile staged in it has been stored
                 if (q >= Cfg::kStages &&
-                    !mbar_wait(smem_u32(&bars[kFree0 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs)) {
+                    (!mbar_wait(smem_u32(&bars[kFree0 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs) ||
+                     !mbar_wait(smem_u32(&bars[kYSt0 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs))) {
                     ok = false; set_error(err, 1); break;
                 }
                 uint8_t *base = smem + st * Cfg::kStage;
@@ -335,98 +348,115 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         }
         __syncwarp();
     } else if (warp == 1) {
+        // ---- MMA issuer -----------------------------------------------------------------
         if (lane == 0) {
             constexpr uint32_t id_cb = idesc_bf16_f32(128, 128, 0, 0);
-            constexpr uint32_t id_ys = idesc_bf16_f32(128, kPB, 0, 1);
-            constexpr uint32_t id_yi = idesc_bf16_f32(128, kPB, 0, 1);
+            constexpr uint32_t id_y = idesc_bf16_f32(128, kPB, 0, 1);
             constexpr uint32_t id_up = idesc_bf16_f32(128, kPB, 1, 1);
-            const uint32_t hbase = smem_u32(smem + Cfg::kH);
-            const uint32_t pbase = smem_u32(smem + Cfg::kP);
-            const uint32_t xwbase = smem_u32(smem + Cfg::kXw);
-            for (int q = 0; q < nq; ++q) {
-                const int st = q % Cfg::kStages;
-                const uint32_t cbase = smem_u32(smem + st * Cfg::kStage);
-                const uint32_t bbase = cbase + Cfg::kCBytes;
-                const uint32_t xbase = bbase + Cfg::kBBytes;
-                if (!mbar_wait(smem_u32(&bars[kFull0 + st]), (q / Cfg::kStages) & 1, kWaitNs)) { ok = false; break; }
-                tc_fence_after();
-                // CB = C B^T (K = s)
+            // Descriptors are built once; inside the loops they advance by compile-time byte
+            // offsets added to the start-address field (all addresses stay below 256 KB).
+            auto adv = [](uint64_t d, uint32_t bytes) -> uint64_t { return d + (uint64_t)(bytes >> 4); };
+            // per stage: C [i][s] K-major, B [j][s] K-major, B^T [s][t] MN-major, dt o x [t][p] MN-major
+            const uint32_t cb0 = smem_u32(smem), cb1 = smem_u32(smem + (1 % Cfg::kStages) * Cfg::kStage);
+            const uint64_t dC0 = smem_desc(cb0, 16, 1024), dC1 = smem_desc(cb1, 16, 1024);
+            const uint64_t dBk0 = smem_desc(cb0 + Cfg::kCBytes, 16, 1024), dBk1 = smem_desc(cb1 + Cfg::kCBytes, 16, 1024);
+            const uint64_t dBm0 = smem_desc(cb0 + Cfg::kCBytes, kAtom, 1024), dBm1 = smem_desc(cb1 + Cfg::kCBytes, kAtom, 1024);
+            const uint64_t dX0 = smem_desc(cb0 + Cfg::kCBytes + Cfg::kBBytes, kAtom, 1024);
+            const uint64_t dX1 = smem_desc(cb1 + Cfg::kCBytes + Cfg::kBBytes, kAtom, 1024);
+            const uint64_t dH = smem_desc(smem_u32(smem + Cfg::kH), kAtom, 1024);   // h bf16 [s][p], MN-major
+            const uint64_t dP = smem_desc(smem_u32(smem + Cfg::kP), 16, 1024);      // P [i][j], K-major
+            const uint64_t dXw = smem_desc(smem_u32(smem + Cfg::kXw), kAtom, 1024); // w o x [t][p], MN-major
+            auto issue_cb = [&](int q) {
+                const bool s1 = (q % Cfg::kStages) != 0;
+                const uint64_t c = s1 ? dC1 : dC0, bk = s1 ? dBk1 : dBk0;
 #pragma unroll
                 for (int kk = 0; kk < S / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                    mma_bf16(tmem + Cfg::kTcb, smem_desc(cbase + off, 16, 1024), smem_desc(bbase + off, 16, 1024),
-                             id_cb, kk > 0 ? 1u : 0u);
+                    mma_bf16(tmem + Cfg::kTcb, adv(c, off), adv(bk, off), id_cb, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&bars[kCb]));
-                // Ys = C h^T (K = s), once the state copy is ready and the last epilogue drained Ys/Yi
-                if (!mbar_wait(smem_u32(&bars[kHReady]), q & 1, kWaitNs)) { ok = false; break; }
-                if (q > 0 && !mbar_wait(smem_u32(&bars[kEpi]), (q - 1) & 1, kWaitNs)) { ok = false; break; }
+            };
+            do {
+                if (nq == 0) break;
+                if (!mbar_wait(smem_u32(&bars[kFull0]), 0, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < S / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                    mma_bf16(tmem + Cfg::kTys, smem_desc(cbase + off, 16, 1024), smem_desc(hbase + kk * 2048, kAtom, 1024),
-                             id_ys, kk > 0 ? 1u : 0u);
-                }
-                // Yi = P (dt o X) (K = j)
-                if (!mbar_wait(smem_u32(&bars[kPReady]), q & 1, kWaitNs)) { ok = false; break; }
-                if (!mbar_wait(smem_u32(&bars[kXReady]), q & 1, kWaitNs)) { ok = false; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kQ / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                    mma_bf16(tmem + Cfg::kTyi, smem_desc(pbase + off, 16, 1024), smem_desc(xbase + kk * 2048, kAtom, 1024),
-                             id_yi, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(smem_u32(&bars[kIntra]));
-                // state update h^T += B^T (w o X) (K = t), on the state pre-scaled by the CUDA-core warps
-                if (q + 1 < nq || write_final) {
-#pragma unroll
-                    for (int lb = 0; lb < S / 128; ++lb) {
-#pragma unroll
-                        for (int kk = 0; kk < kQ / 16; ++kk)
-                            mma_bf16(tmem + Cfg::kTds + lb * kPB, smem_desc(bbase + lb * 2 * kAtom + kk * 2048, kAtom, 1024),
-                                     smem_desc(xwbase + kk * 2048, kAtom, 1024), id_up, 1u);
+                issue_cb(0);
+                for (int q = 0; q < nq; ++q) {
+                    const int st = q % Cfg::kStages;
+                    const bool s1 = st != 0;
+                    const uint64_t c = s1 ? dC1 : dC0, bm = s1 ? dBm1 : dBm0, xs = s1 ? dX1 : dX0;
+                    const uint32_t yb = (uint32_t)(q & 1) * Cfg::kTyStride;
+                    // Ys = C h^T (K = s): needs the state copy and a drained Ys/Yi buffer
+                    if (!mbar_wait(smem_u32(&bars[kHReady]), q & 1, kWaitNs)) { ok = false; break; }
+                    if (q >= 2 && !mbar_wait(smem_u32(&bars[kEpi0 + (q & 1)]), ((q >> 1) - 1) & 1, kWaitNs)) {
+                        ok = false; break;
                     }
-                    mma_commit(smem_u32(&bars[kUpdate]));
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < S / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+                        mma_bf16(tmem + Cfg::kTys + yb, adv(c, off), adv(dH, kk * 2048), id_y, kk > 0 ? 1u : 0u);
+                    }
+                    // state update h^T += B^T (w o X) (K = t) on the state pre-scaled by the state group
+                    if (!mbar_wait(smem_u32(&bars[kXReady]), q & 1, kWaitNs)) { ok = false; break; }
+                    tc_fence_after();
+                    if (q + 1 < nq || write_final) {
+#pragma unroll
+                        for (int lb = 0; lb < S / 128; ++lb) {
+#pragma unroll
+                            for (int kk = 0; kk < kQ / 16; ++kk)
+                                mma_bf16(tmem + Cfg::kTds + lb * kPB, adv(bm, lb * 2 * kAtom + kk * 2048),
+                                         adv(dXw, kk * 2048), id_up, 1u);
+                        }
+                        mma_commit(smem_u32(&bars[kUpdate]));
+                    }
+                    // Yi = D x + P (dt o X) (K = j): the state group stored D x in the accumulator
+                    if (!mbar_wait(smem_u32(&bars[kPReady]), q & 1, kWaitNs)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kQ / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+                        mma_bf16(tmem + Cfg::kTyi + yb, adv(dP, off), adv(xs, kk * 2048), id_y, 1u);
+                    }
+                    mma_commit(smem_u32(&bars[kIntra]));
+                    mma_commit(smem_u32(&bars[kFree0 + st]));     // every MMA reading this stage is issued
+                    // next CB as early as possible (the output group has read this one: P is ready)
+                    if (q + 1 < nq) {
+                        const int st1 = (q + 1) % Cfg::kStages;
+                        if (!mbar_wait(smem_u32(&bars[kFull0 + st1]), ((q + 1) / Cfg::kStages) & 1, kWaitNs)) {
+                            ok = false; break;
+                        }
+                        tc_fence_after();
+                        issue_cb(q + 1);
+                    }
                 }
-                mma_commit(smem_u32(&bars[kFree0 + st]));
-            }
+            } while (0);
             if (!ok) set_error(err, 1);
         }
         __syncwarp();
-    } else {
-        // ---- CUDA-core warps --------------------------------------------------------
-        const int sw = warp - 2;
-        const int gw = sw >> 2;                        // column group
-        const int r = 32 * (warp & 3) + lane;          // TMEM lane = tile row
-        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    } else if (warp < 6) {
+        // ---- state group: state hand-off and x scaling ------------------------------------
         const float dh = Dp[h];
+        const int r = 32 * (warp & 3) + lane;          // TMEM lane = tile row / state row
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         uint8_t *xw = smem + Cfg::kXw;
-        uint8_t *pt = smem + Cfg::kP;
         uint8_t *ht = smem + Cfg::kH;
-        uint32_t xr[kCols / 2];                        // this thread's row of x (raw bf16 pairs)
-        uint32_t grp_phase = 0;
-        auto group_sync = [&]() -> bool {              // all CUDA-core threads; bounded
-            mbar_arrive(smem_u32(&bars[kGroup]));
-            const bool done = mbar_wait(smem_u32(&bars[kGroup]), grp_phase, kWaitNs);
-            grp_phase ^= 1u;
-            return done;
+        // per-sub-chunk scalars, loaded one sub-chunk ahead
+        float n_gr = 0.f, n_dt = 0.f, n_glast = 0.f, n_gbase = 0.f;
+        auto load_scalars = [&](int q) {
+            const int64_t t0 = t_begin + (int64_t)q * kQ;
+            n_gr = Gh[t0 + r];
+            n_dt = __bfloat162float(dt[((int64_t)b * pr.L + t0 + r) * pr.nh + h]);
+            n_glast = Gh[t0 + kQ - 1];
+            n_gbase = (q % qpc == 0) ? 0.f : Gh[t0 - 1];
         };
+        if (nq > 0) load_scalars(0);
         for (int q = 0; q < nq && ok; ++q) {
             const int st = q % Cfg::kStages;
-            const int qin = q % qpc;                   // sub-chunk index inside its chunk
-            const int64_t t0 = t_begin + (int64_t)q * kQ;
-            const float gbase = (qin == 0) ? 0.f : Gh[t0 - 1];
-            const float glast = Gh[t0 + kQ - 1];
-            if (gw == 0) {
-                sG[r] = Gh[t0 + r];
-                sdt[r] = __bfloat162float(dt[((int64_t)b * pr.L + t0 + r) * pr.nh + h]);
-            }
-            if (!group_sync()) { ok = false; set_error(err, 1); break; }
-            const float gr = sG[r], dtr = sdt[r];
+            const float gr = n_gr, dtr = n_dt, glast = n_glast, gbase = n_gbase;
+            if (q + 1 < nq) load_scalars(q + 1);
 
-            // (C) state hand-off: h (fp32) -> bf16 copy [s][p] for Ys, and h * exp2(glast - gbase) -> TMEM
+            // h (fp32) -> bf16 copy [s][p] for Ys, and h * exp2(glast - gbase) back to TMEM
             {
                 const float dec = exp2f(glast - gbase);
                 if (q > 0) {
@@ -436,157 +466,232 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
 #pragma unroll
                 for (int lb = 0; lb < S / 128; ++lb) {
                     const int s = lb * 128 + r;
+                    uint32_t v[64];
+                    if (q == 0) {
+                        // entering state: h0 (zeros if absent) for super-chunks m < hs_from, else h_start[m]
+                        const float *src = (m < hs_from) ? (h0 ? h0 + bh * (int64_t)(pr.H * S) : nullptr)
+                                                         : h_start + (bh * nsup + m) * (int64_t)(pr.H * S);
+                        if (src) {
+                            src += (int64_t)(pb * kPB) * S + s;
 #pragma unroll
-                    for (int c0 = 0; c0 < kCols; c0 += 16) {
-                        const int p0 = gw * kCols + c0;
-                        uint32_t v[16];
-                        if (q == 0) {
-                            // entering state: h0 (zeros if absent) for super-chunks m < hs_from, else h_start[m]
-                            const float *src = (m < hs_from) ? (h0 ? h0 + bh * (int64_t)(pr.H * S) : nullptr)
-                                                             : h_start + (bh * nsup + m) * (int64_t)(pr.H * S);
-                            if (src) {
-                                src += (int64_t)(pb * kPB + p0) * S + s;
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(src[(int64_t)j * S]);
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) v[j] = 0u;
-                            }
+                            for (int j = 0; j < 64; ++j) v[j] = __float_as_uint(src[(int64_t)j * S]);
                         } else {
-                            tmem_ld16(tmem + lane_base + Cfg::kTds + lb * kPB + p0, v);
-                            tmem_ld_wait();
-                        }
-                        uint4 lo, hi;
-                        lo.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
-                        lo.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
-                        lo.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
-                        lo.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
-                        hi.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
-                        hi.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
-                        hi.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
-                        hi.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
-                        *(uint4 *)(ht + sw128(s, p0 >> 3)) = lo;
-                        *(uint4 *)(ht + sw128(s, (p0 >> 3) + 1)) = hi;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * dec);
-                        tmem_st16(tmem + lane_base + Cfg::kTds + lb * kPB + p0, v);
+                            for (int j = 0; j < 64; ++j) v[j] = 0u;
+                        }
+                    } else {
+                        const uint32_t ta = tmem + lane_base + Cfg::kTds + lb * kPB;
+                        tmem_ld16(ta + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                        tmem_ld16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                        tmem_ld16(ta + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
+                        tmem_ld16(ta + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
+                        tmem_ld_wait();
                     }
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(v[8 * c + 0]), __uint_as_float(v[8 * c + 1]));
+                        o.y = pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3]));
+                        o.z = pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5]));
+                        o.w = pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7]));
+                        *(uint4 *)(ht + sw128(s, c)) = o;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * dec);
+                    const uint32_t ta = tmem + lane_base + Cfg::kTds + lb * kPB;
+                    tmem_st16(ta + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_st16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_st16(ta + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
+                    tmem_st16(ta + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
                 }
                 tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(smem_u32(&bars[kHReady]));
             }
-
-            // (A) x tile: keep raw row, write dt o x in place and w o x to the Xw tile
+            // x tile: dt o x in place (Yi operand), w o x into the Xw tile (state-update operand),
+            // and D x into this sub-chunk's Yi accumulator (the Yi MMAs accumulate on top of it)
             {
                 if (!mbar_wait(smem_u32(&bars[kFull0 + st]), (q / Cfg::kStages) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
+                // the Yi buffer of this sub-chunk is free once the epilogue of sub-chunk q - 2 read it
+                if (q >= 2 && !mbar_wait(smem_u32(&bars[kEpi0 + (q & 1)]), ((q >> 1) - 1) & 1, kWaitNs)) {
+                    ok = false; set_error(err, 1); break;
+                }
+                tc_fence_after();
                 uint8_t *xt = smem + st * Cfg::kStage + Cfg::kCBytes + Cfg::kBBytes;
                 const float wr = dtr * exp2f(glast - gr);
+                const uint32_t tyi = tmem + lane_base + Cfg::kTyi + (uint32_t)(q & 1) * Cfg::kTyStride;
 #pragma unroll
-                for (int cc = 0; cc < kCols / 8; ++cc) {
-                    const int c = gw * (kCols / 8) + cc;
-                    const uint32_t off = sw128(r, c);
-                    uint4 v = *(uint4 *)(xt + off);
-                    xr[4 * cc + 0] = v.x; xr[4 * cc + 1] = v.y; xr[4 * cc + 2] = v.z; xr[4 * cc + 3] = v.w;
-                    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-                    uint32_t os[4], ow[4];
+                for (int cp = 0; cp < 4; ++cp) {
+                    uint32_t dx[16];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = unpack_bf16x2(in[e]);
-                        os[e] = pack_bf16x2(f.x * dtr, f.y * dtr);
-                        ow[e] = pack_bf16x2(f.x * wr, f.y * wr);
+                    for (int ch = 0; ch < 2; ++ch) {
+                        const int c = 2 * cp + ch;
+                        const uint32_t off = sw128(r, c);
+                        const uint4 v = *(const uint4 *)(xt + off);
+                        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t os[4], ow[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_bf16x2(in[e]);
+                            os[e] = pack_bf16x2(f.x * dtr, f.y * dtr);
+                            ow[e] = pack_bf16x2(f.x * wr, f.y * wr);
+                            dx[8 * ch + 2 * e] = __float_as_uint(dh * f.x);
+                            dx[8 * ch + 2 * e + 1] = __float_as_uint(dh * f.y);
+                        }
+                        *(uint4 *)(xt + off) = make_uint4(os[0], os[1], os[2], os[3]);
+                        *(uint4 *)(xw + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
                     }
-                    *(uint4 *)(xt + off) = make_uint4(os[0], os[1], os[2], os[3]);
-                    *(uint4 *)(xw + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                    tmem_st16(tyi + 16 * cp, dx);
                 }
+                tmem_st_wait();
                 fence_proxy_async_smem();
+                tc_fence_before();
                 mbar_arrive(smem_u32(&bars[kXReady]));
             }
-
-            // (B) P = CB o exp2(G_i - G_j) o [j <= i], bf16, K-major swizzled [i][j]
-            {
-                if (!mbar_wait(smem_u32(&bars[kCb]), q & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
-                tc_fence_after();
-                const int wrow_hi = 32 * (warp & 3) + 31;   // largest row of this warp
-                for (int jb = gw; jb < kQ / 16; jb += NW) {
-                    const int j0 = jb * 16;
-                    uint32_t pk[8];
-                    if (j0 > wrow_hi) {                    // whole block above the diagonal: zeros
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) pk[e] = 0u;
-                    } else {
-                        uint32_t v[16];
-                        tmem_ld16(tmem + lane_base + Cfg::kTcb + j0, v);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = j0 + 2 * e;
-                            const float a0 = (j <= r) ? __uint_as_float(v[2 * e]) * exp2f(gr - sG[j]) : 0.f;
-                            const float a1 = (j + 1 <= r) ? __uint_as_float(v[2 * e + 1]) * exp2f(gr - sG[j + 1]) : 0.f;
-                            pk[e] = pack_bf16x2(a0, a1);
-                        }
-                    }
-                    const int a = j0 >> 6, c = (j0 & 63) >> 3;
-                    *(uint4 *)(pt + a * kAtom + sw128(r, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *(uint4 *)(pt + a * kAtom + sw128(r, c + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(smem_u32(&bars[kPReady]));
-            }
-
-            // (D) epilogue: y = exp2(G_i - G_base) Ys + Yi + D x
-            {
-                if (!mbar_wait(smem_u32(&bars[kIntra]), q & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
-                tc_fence_after();
-                const float eg = exp2f(gr - gbase);
-                __nv_bfloat16 *yrow = y + ((((int64_t)b * pr.L + t0 + r) * pr.nh + h) * pr.H + pb * kPB);
-#pragma unroll
-                for (int c0 = 0; c0 < kCols; c0 += 16) {
-                    const int p0 = gw * kCols + c0;
-                    uint32_t vs[16], vi[16];
-                    tmem_ld16(tmem + lane_base + Cfg::kTys + p0, vs);
-                    tmem_ld16(tmem + lane_base + Cfg::kTyi + p0, vi);
-                    tmem_ld_wait();
-                    uint32_t o[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float2 xv = unpack_bf16x2(xr[(c0 >> 1) + e]);
-                        const float y0 = fmaf(eg, __uint_as_float(vs[2 * e]), __uint_as_float(vi[2 * e])) + dh * xv.x;
-                        const float y1 = fmaf(eg, __uint_as_float(vs[2 * e + 1]), __uint_as_float(vi[2 * e + 1])) + dh * xv.y;
-                        o[e] = pack_bf16x2(y0, y1);
-                    }
-                    *(uint4 *)(yrow + p0) = make_uint4(o[0], o[1], o[2], o[3]);
-                    *(uint4 *)(yrow + p0 + 8) = make_uint4(o[4], o[5], o[6], o[7]);
-                }
-                tc_fence_before();
-                mbar_arrive(smem_u32(&bars[kEpi]));
-            }
-            // sG / sdt are rewritten by the next sub-chunk
-            if (!group_sync()) { ok = false; set_error(err, 1); break; }
         }
-        // final state of the sequence, from the last unit of each (batch, head)
-        if (ok && write_final) {
+        // final state of the sequence, from the last super-chunk of each (batch, head)
+        if (ok && write_final && nq > 0) {
             if (!mbar_wait(smem_u32(&bars[kUpdate]), (nq - 1) & 1, kWaitNs)) { ok = false; set_error(err, 1); }
             if (ok) {
                 tc_fence_after();
 #pragma unroll
                 for (int lb = 0; lb < S / 128; ++lb) {
                     const int s = lb * 128 + r;
+                    float *dst = h_final + bh * (int64_t)(pr.H * S) + (int64_t)(pb * kPB) * S + s;
 #pragma unroll
-                    for (int c0 = 0; c0 < kCols; c0 += 16) {
-                        const int p0 = gw * kCols + c0;
+                    for (int c0 = 0; c0 < kPB; c0 += 16) {
                         uint32_t v[16];
-                        tmem_ld16(tmem + lane_base + Cfg::kTds + lb * kPB + p0, v);
+                        tmem_ld16(tmem + lane_base + Cfg::kTds + lb * kPB + c0, v);
                         tmem_ld_wait();
-                        float *dst = h_final + bh * (int64_t)(pr.H * S) + (int64_t)(pb * kPB + p0) * S + s;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) dst[(int64_t)j * S] = __uint_as_float(v[j]);
+                        for (int j = 0; j < 16; ++j) dst[(int64_t)(c0 + j) * S] = __uint_as_float(v[j]);
                     }
                 }
             }
         }
+    } else {
+        // ---- output group: P and y (8 warps: two per TMEM lane quarter, splitting columns) --------
+        const int half = (warp - 6) >> 2;              // 0 or 1: which half of the columns
+        const int r = 32 * (warp & 3) + lane;          // TMEM lane = tile row i
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const int wrow_lo = 32 * (warp & 3), wrow_hi = wrow_lo + 31;   // rows of this warp
+        uint8_t *pa = smem + Cfg::kP + half * kAtom;   // P columns [64 half, 64 half + 64)
+        float *sF = sG + kQ;
+        // the 256 output-group threads run every iteration (work is skipped after an error),
+        // so the named barrier below is always reached by all of them
+        auto group_sync = [&]() { named_bar_sync(1, 256); };
+        float n_gr = 0.f, n_gend = 0.f, n_gbase = 0.f;
+        auto load_scalars = [&](int q) {
+            const int64_t t0 = t_begin + (int64_t)q * kQ;
+            n_gr = Gh[t0 + r];
+            n_gend = Gh[t0 + (r | 15)];                // G at the end of row r's 16-token block
+            n_gbase = (q % qpc == 0) ? 0.f : Gh[t0 - 1];
+        };
+        if (nq > 0) load_scalars(0);
+        for (int q = 0; q < nq; ++q) {
+            const int64_t t0 = t_begin + (int64_t)q * kQ;
+            const float gr = n_gr, gend = n_gend, gbase = n_gbase;
+            const uint32_t yb = (uint32_t)(q & 1) * Cfg::kTyStride;
+            if (half == 0) {
+                sG[r] = gr;
+                sF[r] = ex2_approx(gend - gr);          // 2^(G_blockend - G_j) <= 1 for A dt >= 0
+            }
+            group_sync();
+            if (q + 1 < nq) load_scalars(q + 1);
+
+            // P[i][j] = CB[i][j] 2^(G_i - G_j) for j <= i, else 0; bf16, K-major swizzled [i][j].
+            // Blocks of 16 columns entirely left of this warp's rows use the factored form
+            // 2^(G_i - G_e) 2^(G_e - G_j) (G_e = G at the block's last column; both factors
+            // <= 1); blocks that meet the diagonal evaluate 2^(G_i - G_j) per element.
+            if (ok && !mbar_wait(smem_u32(&bars[kCb]), q & 1, kWaitNs)) { ok = false; set_error(err, 1); }
+            if (ok) {
+                tc_fence_after();
+                const int jh = 64 * half;
+                if (jh > wrow_hi) {                     // whole half above the diagonal: zeros
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) *(uint4 *)(pa + sw128(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+                } else {
+                    uint32_t v[64];
+                    const uint32_t ta = tmem + lane_base + Cfg::kTcb + jh;
+                    tmem_ld16(ta + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_ld16(ta + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
+                    tmem_ld16(ta + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int blk = 0; blk < 4; ++blk) {
+                        const int j0 = jh + 16 * blk;
+                        float f[16];
+                        if (j0 > wrow_hi) {                       // above the diagonal for the whole warp
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) f[e] = 0.f;
+                        } else if (j0 + 15 < wrow_lo) {           // left of every row of the warp: factored
+                            const float ei = ex2_approx(gr - sG[j0 + 15]);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[16 * blk + e]) * ei * sF[j0 + e];
+                        } else {                                  // meets the diagonal: exact, selected
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int j = j0 + e;
+                                const float val = __uint_as_float(v[16 * blk + e]) * ex2_approx(gr - sG[j]);
+                                f[e] = (j <= r) ? val : 0.f;
+                            }
+                        }
+                        const int c = 2 * blk;
+                        *(uint4 *)(pa + sw128(r, c)) = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                                                  pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                        *(uint4 *)(pa + sw128(r, c + 1)) =
+                            make_uint4(pack_bf16x2(f[8], f[9]), pack_bf16x2(f[10], f[11]),
+                                       pack_bf16x2(f[12], f[13]), pack_bf16x2(f[14], f[15]));
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars[kPReady]));
+            }
+            // y = 2^(G_i - G_base) Ys + Yi   (Yi already holds D x; this thread: 32 columns).
+            // y is staged in the x tile of this stage (its last reader, the Yi MMA, has completed)
+            // in the same swizzled [t][p] layout, then written by one bulk tensor store.
+            uint8_t *ystage = smem + (q % Cfg::kStages) * Cfg::kStage + Cfg::kCBytes + Cfg::kBBytes;
+            if (ok && !mbar_wait(smem_u32(&bars[kIntra]), q & 1, kWaitNs)) { ok = false; set_error(err, 1); }
+            if (ok) {
+                tc_fence_after();
+                const float eg = ex2_approx(gr - gbase);
+                uint32_t vs[32], vi[32];
+                const uint32_t c0 = 32 * half;
+                tmem_ld16(tmem + lane_base + Cfg::kTys + yb + c0, *reinterpret_cast<uint32_t(*)[16]>(&vs[0]));
+                tmem_ld16(tmem + lane_base + Cfg::kTys + yb + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&vs[16]));
+                tmem_ld16(tmem + lane_base + Cfg::kTyi + yb + c0, *reinterpret_cast<uint32_t(*)[16]>(&vi[0]));
+                tmem_ld16(tmem + lane_base + Cfg::kTyi + yb + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&vi[16]));
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = 8 * c + 2 * e;
+                        o[e] = pack_bf16x2(fmaf(eg, __uint_as_float(vs[k]), __uint_as_float(vi[k])),
+                                           fmaf(eg, __uint_as_float(vs[k + 1]), __uint_as_float(vi[k + 1])));
+                    }
+                    *(uint4 *)(ystage + sw128(r, 4 * half + c)) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars[kEpi0 + (q & 1)]));
+            }
+            // all rows staged (and sG / sF free for the next sub-chunk)
+            group_sync();
+            if (warp == 6 && lane == 0) {
+                if (ok) {
+                    tma_store_4d(&tmY, smem_u32(ystage), pb * kPB, h, (int)t0, b);
+                    bulk_commit();
+                    bulk_wait_read();
+                }
+                mbar_arrive(smem_u32(&bars[kYSt0 + (q % Cfg::kStages)]));
+            }
+        }
+        if (warp == 6 && lane == 0) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -640,22 +745,22 @@ cudaError_t state_launch(const Problem &pr, const void *x, const void *dt, const
     return cudaGetLastError();
 }
 
-template <int S, int NW>
+template <int S>
 cudaError_t scan_launch(const Problem &pr, const void *x, const void *dt, const void *Bm, const void *Cm, const float *D,
                         const float *G, const float *h0, const float *h_start, float *h_final, void *y, int R, int nsup,
                         int hs_from, int *err, cudaStream_t st)
 {
-    CUtensorMap mC, mB, mX;
+    CUtensorMap mC, mB, mX, mY;
     if (!make_map_4d(&mC, Cm, pr.S, pr.G, pr.L, pr.B, kQ) || !make_map_4d(&mB, Bm, pr.S, pr.G, pr.L, pr.B, kQ) ||
-        !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, kQ))
+        !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, kQ) || !make_map_4d(&mY, y, pr.H, pr.nh, pr.L, pr.B, kQ))
         return cudaErrorInvalidValue;
     using Cfg = ScanCfg<S>;
-    auto kern = k_chunk_scan_tc<S, NW>;
+    auto kern = k_chunk_scan_tc<S>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(pr.B * nsup * pr.nh * (pr.H / kPB));
-    kern<<<grid, 64 + 128 * NW, Cfg::kSmem, st>>>(mC, mB, mX, G, (const __nv_bfloat16 *)dt, D, h0, h_start, h_final,
-                                                  (__nv_bfloat16 *)y, pr, R, nsup, hs_from, err);
+    kern<<<grid, 448, Cfg::kSmem, st>>>(mC, mB, mX, mY, G, (const __nv_bfloat16 *)dt, D, h0,
+                                        h_start, h_final, (__nv_bfloat16 *)y, pr, R, nsup, hs_from, err);
     return cudaGetLastError();
 }
 
@@ -687,8 +792,8 @@ cudaError_t launch_chunk_scan_tc(const Problem &pr, const void *x, const void *d
                                  const float *D, const float *G, const float *h0, const float *h_start, float *h_final,
                                  void *y, int R, int nsup, int hs_from, int *err, cudaStream_t st)
 {
-    if (pr.S == 128) return scan_launch<128, 2>(pr, x, dt, Bm, Cm, D, G, h0, h_start, h_final, y, R, nsup, hs_from, err, st);
-    if (pr.S == 256) return scan_launch<256, 2>(pr, x, dt, Bm, Cm, D, G, h0, h_start, h_final, y, R, nsup, hs_from, err, st);
+    if (pr.S == 128) return scan_launch<128>(pr, x, dt, Bm, Cm, D, G, h0, h_start, h_final, y, R, nsup, hs_from, err, st);
+    if (pr.S == 256) return scan_launch<256>(pr, x, dt, Bm, Cm, D, G, h0, h_start, h_final, y, R, nsup, hs_from, err, st);
     return cudaErrorNotSupported;
 }
 
