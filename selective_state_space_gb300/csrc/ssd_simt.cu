@@ -20,48 +20,57 @@ namespace {
 // ---------------------------------------------------------------------------
 // Stage 1 -- chunk_cumsum (blog section "Kernel 1: cumulative sum").
 // G[b][h][t] = log2(e) * sum_{s in chunk(t), s <= t} A[h] dt[b][s][h].
-// One block per (chunk, 32-head tile, batch); one warp-scan per (head, 32 tokens),
-// carried across the chunk.  dt is read as [token][head] tiles and G is written
-// transposed, [head][token], so both sides are coalesced.
+// One block per (chunk, 32-head tile, batch).  Lane = head, so every dt row of 32
+// heads is one coalesced load.  Warp w takes runs of 32 consecutive tokens: each lane
+// loads its run (independent loads), forms the running sum in registers, and records
+// the run total; after one barrier every run adds the totals of the runs before it.
+// G is staged as [token][head] and written transposed, [head][token], coalesced.
 // ---------------------------------------------------------------------------
 template <typename Tin>
 __global__ void __launch_bounds__(256)
 k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *__restrict__ G,
                int64_t L, int nh, int T)
 {
-    __shared__ float tile[32][33];
+    extern __shared__ float tile[];   // [T][33]
+    __shared__ float run_sum[32][33]; // [run][head]
     const int k = blockIdx.x, hbase = blockIdx.y * 32, b = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t0 = (int64_t)k * T;
     const int n = (int)((int64_t)T < L - t0 ? (int64_t)T : L - t0);
-    float carry[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int seg = 0; seg < n; seg += 32) {
-        for (int r = warp; r < 32; r += 8) {
-            const int t = seg + r, h = hbase + lane;
-            float v = 0.f;   // zero padding past the end of the chunk
-            if (t < n && h < nh) v = A[h] * to_f32(dt[((int64_t)b * L + t0 + t) * nh + h]);
-            tile[r][lane] = v;
-        }
-        __syncthreads();
+    const int runs = (n + 31) / 32;
+    const int h = hbase + lane;
+    const float a = (h < nh) ? A[h] : 0.f;
+    for (int r = warp; r < runs; r += 8) {
+        float v[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int j = warp * 4 + q;
-            float v = tile[lane][j];
+        for (int i = 0; i < 32; ++i) {
+            const int t = 32 * r + i;       // zero padding past the end of the chunk
+            v[i] = (t < n && h < nh) ? to_f32(dt[((int64_t)b * L + t0 + t) * nh + h]) : 0.f;
+        }
+        float acc = 0.f;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, v, off);
-                if (lane >= off) v += u;
-            }
-            v += carry[q];
-            carry[q] = __shfl_sync(0xffffffffu, v, 31);
-            tile[lane][j] = v;
+        for (int i = 0; i < 32; ++i) {
+            acc += a * v[i];
+            if (32 * r + i < n) tile[(32 * r + i) * 33 + lane] = acc;
         }
-        __syncthreads();
-        for (int j = warp; j < 32; j += 8) {
-            const int h = hbase + j, t = seg + lane;
-            if (h < nh && t < n) G[((int64_t)b * nh + h) * L + t0 + t] = tile[lane][j] * kLog2e;
+        run_sum[r][lane] = acc;
+    }
+    __syncthreads();
+    for (int r = warp; r < runs; r += 8) {
+        float off = 0.f;
+        for (int rr = 0; rr < r; ++rr) off += run_sum[rr][lane];
+        if (r > 0) {
+#pragma unroll 8
+            for (int i = 0; i < 32; ++i)
+                if (32 * r + i < n) tile[(32 * r + i) * 33 + lane] += off;
         }
-        __syncthreads();
+    }
+    __syncthreads();
+    for (int j = warp; j < 32; j += 8) {
+        const int hh = hbase + j;
+        if (hh >= nh) continue;
+        float *dst = G + ((int64_t)b * nh + hh) * L + t0;
+        for (int t = lane; t < n; t += 32) dst[t] = tile[t * 33 + j] * kLog2e;
     }
 }
 
@@ -151,39 +160,56 @@ k_state_passing(const float *__restrict__ G, const float *__restrict__ s_local,
                 float *__restrict__ h_final, Problem pr, int R, int nsup, int nm)
 {
     using V = typename std::conditional<VEC == 4, float4, float>::type;
+    constexpr int kBatch = 8;                     // states loaded together (independent loads)
+    constexpr int kWin = 1024;                    // super-chunks whose decays are staged at once
+    __shared__ float sdec[kWin];                  // exp2 of each super-chunk's total log2 decay
     const int64_t HS = pr.H * pr.S;
     const int64_t e = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * VEC;
+    const bool active = e < HS;
     const int h = blockIdx.y, b = blockIdx.z;
-    if (e >= HS) return;
     const int64_t bh = (int64_t)b * pr.nh + h;
+    const float *Gh = G + bh * pr.L;
     float st[VEC];
-    if (h0) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) st[i] = 0.f;
+    if (active && h0) {
         const V v = *reinterpret_cast<const V *>(h0 + bh * HS + e);
         memcpy(st, &v, sizeof(V));
-    } else {
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) st[i] = 0.f;
     }
-    const float *Gh = G + bh * pr.L;
     const int64_t base = bh * nsup * HS + e;
-    V s_next;
-    if (nm > 0) s_next = *reinterpret_cast<const V *>(s_local + base);
-    for (int m = 0; m < nsup; ++m) {
-        V out;
-        memcpy(&out, st, sizeof(V));
-        *reinterpret_cast<V *>(h_start + base + (int64_t)m * HS) = out;
-        if (m >= nm) continue;
-        const V sv = s_next;
-        if (m + 1 < nm) s_next = *reinterpret_cast<const V *>(s_local + base + (int64_t)(m + 1) * HS);   // prefetch
-        float dec = 0.f;
-        const int k1 = min((int)pr.nc, (m + 1) * R);
-        for (int k = m * R; k < k1; ++k) dec += Gh[min(pr.L, (int64_t)(k + 1) * pr.T) - 1];
-        const float a = exp2f(dec);
-        float sa[VEC];
-        memcpy(sa, &sv, sizeof(V));
+    for (int w0 = 0; w0 < nsup; w0 += kWin) {
+        const int w1 = min(nsup, w0 + kWin);
+        __syncthreads();                          // the previous window's decays are no longer read
+        for (int m = w0 + threadIdx.x; m < min(w1, nm); m += blockDim.x) {
+            float dec = 0.f;
+            const int k1 = min((int)pr.nc, (m + 1) * R);
+            for (int k = m * R; k < k1; ++k) dec += Gh[min(pr.L, (int64_t)(k + 1) * pr.T) - 1];
+            sdec[m - w0] = exp2f(dec);
+        }
+        __syncthreads();
+        if (!active) continue;
+        for (int m0 = w0; m0 < w1; m0 += kBatch) {
+            V sv[kBatch];
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) st[i] = fmaf(a, st[i], sa[i]);
+            for (int i = 0; i < kBatch; ++i)
+                if (m0 + i < min(w1, nm)) sv[i] = *reinterpret_cast<const V *>(s_local + base + (int64_t)(m0 + i) * HS);
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const int m = m0 + i;
+                if (m >= w1) break;
+                V out;
+                memcpy(&out, st, sizeof(V));
+                *reinterpret_cast<V *>(h_start + base + (int64_t)m * HS) = out;
+                if (m >= nm) continue;
+                const float a = sdec[m - w0];
+                float sa[VEC];
+                memcpy(sa, &sv[i], sizeof(V));
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) st[j] = fmaf(a, st[j], sa[j]);
+            }
+        }
     }
+    if (!active) return;
     if (h_final && nm == nsup) {
         V out;
         memcpy(&out, st, sizeof(V));
@@ -361,10 +387,17 @@ cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *
                                 cudaStream_t st)
 {
     dim3 grid((unsigned)pr.nc, (unsigned)((pr.nh + 31) / 32), (unsigned)pr.B);
-    if (pr.in_dt == SSD_BF16)
-        k_chunk_cumsum<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)dt, A, G, pr.L, (int)pr.nh, (int)pr.T);
-    else
-        k_chunk_cumsum<float><<<grid, 256, 0, st>>>((const float *)dt, A, G, pr.L, (int)pr.nh, (int)pr.T);
+    const size_t smem = sizeof(float) * 33 * (size_t)pr.T;
+    cudaError_t e;
+    if (pr.in_dt == SSD_BF16) {
+        auto kern = k_chunk_cumsum<__nv_bfloat16>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
+        kern<<<grid, 256, smem, st>>>((const __nv_bfloat16 *)dt, A, G, pr.L, (int)pr.nh, (int)pr.T);
+    } else {
+        auto kern = k_chunk_cumsum<float>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
+        kern<<<grid, 256, smem, st>>>((const float *)dt, A, G, pr.L, (int)pr.nh, (int)pr.T);
+    }
     return cudaGetLastError();
 }
 

@@ -74,57 +74,66 @@ __device__ __forceinline__ void set_error(int *err, int bit)
 //   s^T[s][p] = sum_{t in super-chunk m} w_t B_t[s] x_t[p],
 //   w_t = dt_t exp2(decay from t to the end of the super-chunk)
 //       = dt_t exp2((G_last(k) - G_t) + sum_{k' > k in m} G_last(k')).
-// MMA: D[s][p] (TMEM lanes s, columns p) += B^T (A: M = s, K = t, MN-major, from the TMA
-// tile of B) x (w o X) (B operand: K = t, N = p, MN-major, x tile scaled in place).
-// One CTA per (batch, head, super-chunk); warp 0 issues TMA, warp 1 issues MMAs,
-// warps 2..5 scale x and drain the accumulator.
+// One CTA per (batch, super-chunk, HG consecutive heads of one B/C group): the heads
+// share the B tile, and their scaled x tiles sit side by side as one N = HG*H operand.
+// MMA: D[s][hh*H + p] (TMEM lanes s) += B^T (A: M = s, K = t, MN-major, the TMA tile of
+// B) x (w o X) (B operand: K = t, N = HG*H, MN-major, x tiles scaled in place).
+// Warp 0 issues TMA, warp 1 issues MMAs, warps 2..5 scale x and drain the accumulator.
 // ===========================================================================
-template <int S, int H>
+template <int S, int H, int HG>
 struct StateCfg {
     static constexpr int kStages = 2;
+    static constexpr int kN = HG * H;                      // MMA N: all heads' p columns
     static constexpr uint32_t kBBytes = (S / 64) * kAtom;
-    static constexpr uint32_t kXBytes = (H / 64) * kAtom;
+    static constexpr uint32_t kXBytes = (kN / 64) * kAtom;
     static constexpr uint32_t kStage = kBBytes + kXBytes;
     static constexpr int kMaxR = 256;
-    static constexpr uint32_t kSmem = kStages * kStage + kMaxR * 4 + 256 + 1024;
-    static constexpr uint32_t kTmemCols = (S / 128) * H <= 32 ? 32 : ((S / 128) * H <= 64 ? 64 : ((S / 128) * H <= 128 ? 128 : 256));
+    static constexpr uint32_t kSmem = kStages * kStage + HG * kMaxR * 4 + 256 + 1024;
+    static constexpr uint32_t kCols = (S / 128) * kN;
+    static constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : (kCols <= 64 ? 64 : (kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512)));
 };
 
-template <int S, int H>
+template <int S, int H, int HG>
 __global__ void __launch_bounds__(192, 1)
 k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmX,
                  const float *__restrict__ G, const __nv_bfloat16 *__restrict__ dt, float *__restrict__ s_out,
                  Problem pr, int R, int nsup, int nm, int *err)
 {
-    using Cfg = StateCfg<S, H>;
+    using Cfg = StateCfg<S, H, HG>;
+    constexpr int kN = Cfg::kN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    float *sGl = (float *)(smem + Cfg::kStages * Cfg::kStage);                    // G_last of each chunk
-    uint64_t *bars = (uint64_t *)(smem + Cfg::kStages * Cfg::kStage + Cfg::kMaxR * 4);
+    float *sGl = (float *)(smem + Cfg::kStages * Cfg::kStage);                    // [HG][kMaxR] G_last per chunk
+    uint64_t *bars = (uint64_t *)(smem + Cfg::kStages * Cfg::kStage + HG * Cfg::kMaxR * 4);
     uint32_t *tmem_slot = (uint32_t *)(bars + 8);
     // bars: [0,1] full, [2,3] free, [4,5] x_ready (per stage), [6] done
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // unit = (b, m, h) for m < nm, h fastest so heads sharing B tiles run together
+    // unit = (b, m, head group hq) for m < nm; head groups fastest
+    const int nhq = (int)(pr.nh / HG);
     int u = blockIdx.x;
-    const int h = u % pr.nh; u /= pr.nh;
+    const int hq = u % nhq; u /= nhq;
     const int m = u % nm;
     const int b = u / nm;
-    const int g = (int)(h / pr.hpg);
+    const int h0 = hq * HG;
+    const int g = (int)(h0 / pr.hpg);
     const int k_begin = m * R;
     const int k_end = min((int)pr.nc, k_begin + R);
     const int nk = k_end - k_begin;
     const int qpc = (int)(pr.T / kQ);                    // sub-chunks per chunk
     const int nq = nk * qpc;
     const int64_t t_begin = (int64_t)k_begin * pr.T;
-    const float *Gh = G + ((int64_t)b * pr.nh + h) * pr.L;
+    const float *G0 = G + ((int64_t)b * pr.nh + h0) * pr.L;   // head h0 + hh: G0 + hh * L
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 7; ++i) mbar_init(smem_u32(&bars[i]), (i >= 4 && i < 6) ? 128 : 1);
         fence_mbar_init();
     }
     if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols); tmem_relinquish(); }
-    for (int i = threadIdx.x; i < nk; i += blockDim.x) sGl[i] = Gh[(int64_t)(k_begin + i) * pr.T + pr.T - 1];
+    for (int i = threadIdx.x; i < HG * nk; i += blockDim.x) {
+        const int hh = i / nk, kk = i % nk;
+        sGl[hh * Cfg::kMaxR + kk] = G0[(int64_t)hh * pr.L + (int64_t)(k_begin + kk) * pr.T + pr.T - 1];
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -145,28 +154,28 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
                 mbar_arrive_expect_tx(full, Cfg::kStage);
                 const int t0 = (int)(t_begin + (int64_t)q * kQ);
                 for (int a = 0; a < S / 64; ++a) tma_load_4d(smem_u32(base + a * kAtom), &tmB, full, 64 * a, g, t0, b);
-                for (int a = 0; a < H / 64; ++a)
-                    tma_load_4d(smem_u32(base + Cfg::kBBytes + a * kAtom), &tmX, full, 64 * a, h, t0, b);
+                for (int a = 0; a < kN / 64; ++a)   // atom a: head h0 + a / (H/64), columns 64 * (a % (H/64))
+                    tma_load_4d(smem_u32(base + Cfg::kBBytes + a * kAtom), &tmX, full, 64 * (a % (H / 64)),
+                                h0 + a / (H / 64), t0, b);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, H, 1, 1);
+            constexpr uint32_t idesc = idesc_bf16_f32(128, kN, 1, 1);
             for (int q = 0; q < nq && ok; ++q) {
                 const int st = q % Cfg::kStages;
                 if (!mbar_wait(smem_u32(&bars[4 + st]), (q / Cfg::kStages) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
                 tc_fence_after();
                 const uint32_t bbase = smem_u32(smem + st * Cfg::kStage);
                 const uint32_t xbase = bbase + Cfg::kBBytes;
+                const uint64_t ad0 = smem_desc(bbase, kAtom, 1024), bd0 = smem_desc(xbase, kAtom, 1024);
 #pragma unroll
                 for (int lb = 0; lb < S / 128; ++lb) {
 #pragma unroll
-                    for (int kk = 0; kk < kQ / 16; ++kk) {
-                        const uint64_t ad = smem_desc(bbase + lb * 2 * kAtom + kk * 2048, kAtom, 1024);
-                        const uint64_t bd = smem_desc(xbase + kk * 2048, kAtom, 1024);
-                        mma_bf16(tmem + lb * H, ad, bd, idesc, (q > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < kQ / 16; ++kk)
+                        mma_bf16(tmem + lb * kN, ad0 + (uint64_t)((lb * 2 * kAtom + kk * 2048) >> 4),
+                                 bd0 + (uint64_t)((kk * 2048) >> 4), idesc, (q > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&bars[2 + st]));
             }
@@ -174,29 +183,47 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
         }
         __syncwarp();
     } else {
-        // warps 2..5: scale x rows in place, then drain the accumulator
+        // warps 2..5: scale x rows in place (each head by its own w), then drain the accumulator
         const int r = 32 * (warp & 3) + lane;       // token row of the tile / TMEM lane
+        // this row's dt and G for every head, loaded one sub-chunk ahead
+        float n_dt[HG], n_g[HG];
+        auto load_row = [&](int q) {
+            const int64_t t = t_begin + (int64_t)q * kQ + r;
+#pragma unroll
+            for (int hh = 0; hh < HG; ++hh) {
+                n_dt[hh] = __bfloat162float(dt[((int64_t)b * pr.L + t) * pr.nh + h0 + hh]);
+                n_g[hh] = G0[(int64_t)hh * pr.L + t];
+            }
+        };
+        if (nq > 0) load_row(0);
         for (int q = 0; q < nq && ok; ++q) {
             const int st = q % Cfg::kStages;
-            if (!mbar_wait(smem_u32(&bars[st]), (q / Cfg::kStages) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
+            float dtr[HG], gr[HG];
+#pragma unroll
+            for (int hh = 0; hh < HG; ++hh) { dtr[hh] = n_dt[hh]; gr[hh] = n_g[hh]; }
+            if (q + 1 < nq) load_row(q + 1);
             const int kl = q / qpc;                          // chunk index inside the super-chunk
-            float suffix = 0.f;
-            for (int kk = kl + 1; kk < nk; ++kk) suffix += sGl[kk];
-            const int64_t t = t_begin + (int64_t)q * kQ + r;
-            const float wr = __bfloat162float(dt[((int64_t)b * pr.L + t) * pr.nh + h]) *
-                             exp2f((sGl[kl] - Gh[t]) + suffix);
+            float wr[HG];
+#pragma unroll
+            for (int hh = 0; hh < HG; ++hh) {
+                float suffix = 0.f;
+                for (int kk = kl + 1; kk < nk; ++kk) suffix += sGl[hh * Cfg::kMaxR + kk];
+                wr[hh] = dtr[hh] * exp2f((sGl[hh * Cfg::kMaxR + kl] - gr[hh]) + suffix);
+            }
+            if (!mbar_wait(smem_u32(&bars[st]), (q / Cfg::kStages) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
             uint8_t *xt = smem + st * Cfg::kStage + Cfg::kBBytes;
 #pragma unroll
-            for (int a = 0; a < H / 64; ++a) {
+            for (int a = 0; a < kN / 64; ++a) {
+                const float w = wr[a / (H / 64)];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint4 *p = (uint4 *)(xt + a * kAtom + sw128(r, c));
                     uint4 v = *p;
                     float2 f0 = unpack_bf16x2(v.x), f1 = unpack_bf16x2(v.y), f2 = unpack_bf16x2(v.z), f3 = unpack_bf16x2(v.w);
-                    v.x = pack_bf16x2(f0.x * wr, f0.y * wr);
-                    v.y = pack_bf16x2(f1.x * wr, f1.y * wr);
-                    v.z = pack_bf16x2(f2.x * wr, f2.y * wr);
-                    v.w = pack_bf16x2(f3.x * wr, f3.y * wr);
+                    v.x = pack_bf16x2(f0.x * w, f0.y * w);
+                    v.y = pack_bf16x2(f1.x * w, f1.y * w);
+                    v.z = pack_bf16x2(f2.x * w, f2.y * w);
+                    v.w = pack_bf16x2(f3.x * w, f3.y * w);
                     *p = v;
                 }
             }
@@ -207,17 +234,18 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
         if (ok) {
             tc_fence_after();
             const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-            float *dst = s_out + (((int64_t)b * pr.nh + h) * nsup + m) * (int64_t)(H * S);
 #pragma unroll
             for (int lb = 0; lb < S / 128; ++lb) {
                 const int s = lb * 128 + r;
 #pragma unroll
-                for (int c0 = 0; c0 < H; c0 += 16) {
+                for (int c0 = 0; c0 < kN; c0 += 16) {
+                    const int hh = c0 / H, p0 = c0 % H;
+                    float *dst = s_out + (((int64_t)b * pr.nh + h0 + hh) * nsup + m) * (int64_t)(H * S);
                     uint32_t v[16];
-                    tmem_ld16(tmem + lane_base + lb * H + c0, v);
+                    tmem_ld16(tmem + lane_base + lb * kN + c0, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) dst[(int64_t)(c0 + j) * S + s] = __uint_as_float(v[j]);
+                    for (int j = 0; j < 16; ++j) dst[(int64_t)(p0 + j) * S + s] = __uint_as_float(v[j]);
                 }
             }
         }
@@ -267,9 +295,11 @@ struct ScanCfg {
     static constexpr uint32_t kTmemCols = 512;
 };
 
+// kFull/kFree: the C and B tiles of a stage; kXFull/kXFree: its x tile (also the y staging
+// tile, released to the producer only after kYSt: the bulk store has read it).
 enum ScanBar {
     kFull0 = 0, kFree0 = 2, kCb = 4, kHReady, kXReady, kPReady, kIntra, kUpdate, kEpi0, kEpi1, kOutGroup,
-    kYSt0, kYSt1, kNumScanBars
+    kYSt0, kYSt1, kXFull0, kXFull1, kXFree0, kXFree1, kNumScanBars
 };
 
 template <int S>
@@ -329,21 +359,28 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             prefetch_tmap(&tmX);
             for (int q = 0; q < nq && ok; ++q) {
                 const int st = q % Cfg::kStages;
-                // the stage is free once its MMAs completed and the y tile staged in it has been stored
+                // C and B tiles: free once the MMAs reading them (CB, Ys, state update) are done
                 if (q >= Cfg::kStages &&
-                    (!mbar_wait(smem_u32(&bars[kFree0 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs) ||
-                     !mbar_wait(smem_u32(&bars[kYSt0 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs))) {
+                    !mbar_wait(smem_u32(&bars[kFree0 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs)) {
                     ok = false; set_error(err, 1); break;
                 }
                 uint8_t *base = smem + st * Cfg::kStage;
                 const uint32_t full = smem_u32(&bars[kFull0 + st]);
-                mbar_arrive_expect_tx(full, Cfg::kStage);
+                mbar_arrive_expect_tx(full, Cfg::kCBytes + Cfg::kBBytes);
                 const int t0 = (int)(t_begin + (int64_t)q * kQ);
                 for (int a = 0; a < S / 64; ++a) {
                     tma_load_4d(smem_u32(base + a * kAtom), &tmC, full, 64 * a, g, t0, b);
                     tma_load_4d(smem_u32(base + Cfg::kCBytes + a * kAtom), &tmB, full, 64 * a, g, t0, b);
                 }
-                tma_load_4d(smem_u32(base + Cfg::kCBytes + Cfg::kBBytes), &tmX, full, pb * kPB, h, t0, b);
+                // x tile: free once the Yi MMA has read it and the y tile staged in it has been stored
+                if (q >= Cfg::kStages &&
+                    (!mbar_wait(smem_u32(&bars[kXFree0 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs) ||
+                     !mbar_wait(smem_u32(&bars[kYSt0 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs))) {
+                    ok = false; set_error(err, 1); break;
+                }
+                const uint32_t xfull = smem_u32(&bars[kXFull0 + st]);
+                mbar_arrive_expect_tx(xfull, Cfg::kXBytes);
+                tma_load_4d(smem_u32(base + Cfg::kCBytes + Cfg::kBBytes), &tmX, xfull, pb * kPB, h, t0, b);
             }
         }
         __syncwarp();
@@ -410,6 +447,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                         }
                         mma_commit(smem_u32(&bars[kUpdate]));
                     }
+                    mma_commit(smem_u32(&bars[kFree0 + st]));     // CB, Ys and the update have read C and B
                     // Yi = D x + P (dt o X) (K = j): the state group stored D x in the accumulator
                     if (!mbar_wait(smem_u32(&bars[kPReady]), q & 1, kWaitNs)) { ok = false; break; }
                     tc_fence_after();
@@ -419,7 +457,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                         mma_bf16(tmem + Cfg::kTyi + yb, adv(dP, off), adv(xs, kk * 2048), id_y, 1u);
                     }
                     mma_commit(smem_u32(&bars[kIntra]));
-                    mma_commit(smem_u32(&bars[kFree0 + st]));     // every MMA reading this stage is issued
+                    mma_commit(smem_u32(&bars[kXFree0 + st]));    // Yi has read the x tile
                     // next CB as early as possible (the output group has read this one: P is ready)
                     if (q + 1 < nq) {
                         const int st1 = (q + 1) % Cfg::kStages;
@@ -512,7 +550,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             // x tile: dt o x in place (Yi operand), w o x into the Xw tile (state-update operand),
             // and D x into this sub-chunk's Yi accumulator (the Yi MMAs accumulate on top of it)
             {
-                if (!mbar_wait(smem_u32(&bars[kFull0 + st]), (q / Cfg::kStages) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
+                if (!mbar_wait(smem_u32(&bars[kXFull0 + st]), (q / Cfg::kStages) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
                 // the Yi buffer of this sub-chunk is free once the epilogue of sub-chunk q - 2 read it
                 if (q >= 2 && !mbar_wait(smem_u32(&bars[kEpi0 + (q & 1)]), ((q >> 1) - 1) & 1, kWaitNs)) {
                     ok = false; set_error(err, 1); break;
@@ -728,18 +766,18 @@ bool make_map_4d(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, ui
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int S, int H>
+template <int S, int H, int HG>
 cudaError_t state_launch(const Problem &pr, const void *x, const void *dt, const void *Bm, const float *G, float *s_out,
                          int R, int nsup, int nm, int *err, cudaStream_t st)
 {
     CUtensorMap mB, mX;
     if (!make_map_4d(&mB, Bm, pr.S, pr.G, pr.L, pr.B, kQ) || !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, kQ))
         return cudaErrorInvalidValue;
-    using Cfg = StateCfg<S, H>;
-    auto kern = k_chunk_state_tc<S, H>;
+    using Cfg = StateCfg<S, H, HG>;
+    auto kern = k_chunk_state_tc<S, H, HG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(pr.B * nm * pr.nh);
+    const unsigned grid = (unsigned)(pr.B * nm * (pr.nh / HG));
     if (grid == 0) return cudaSuccess;
     kern<<<grid, 192, Cfg::kSmem, st>>>(mB, mX, G, (const __nv_bfloat16 *)dt, s_out, pr, R, nsup, nm, err);
     return cudaGetLastError();
@@ -780,11 +818,20 @@ bool tc_supported(const Problem &pr)
 cudaError_t launch_chunk_state_tc(const Problem &pr, const void *x, const void *dt, const void *Bm, const float *G,
                                   float *s_out, int R, int nsup, int nm, int *err, cudaStream_t st)
 {
-    if (R < 1 || R > StateCfg<128, 64>::kMaxR) return cudaErrorInvalidValue;
-    if (pr.S == 128 && pr.H == 64) return state_launch<128, 64>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
-    if (pr.S == 128 && pr.H == 128) return state_launch<128, 128>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
-    if (pr.S == 256 && pr.H == 64) return state_launch<256, 64>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
-    if (pr.S == 256 && pr.H == 128) return state_launch<256, 128>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
+    if (R < 1 || R > 256) return cudaErrorInvalidValue;
+    // heads per CTA: as many heads of one group as fit N = HG * H <= 256 (S = 128)
+    const int hpg = (int)pr.hpg;
+    if (pr.S == 128 && pr.H == 64) {
+        if (hpg % 4 == 0) return state_launch<128, 64, 4>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
+        if (hpg % 2 == 0) return state_launch<128, 64, 2>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
+        return state_launch<128, 64, 1>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
+    }
+    if (pr.S == 128 && pr.H == 128) {
+        if (hpg % 2 == 0) return state_launch<128, 128, 2>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
+        return state_launch<128, 128, 1>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
+    }
+    if (pr.S == 256 && pr.H == 64) return state_launch<256, 64, 1>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
+    if (pr.S == 256 && pr.H == 128) return state_launch<256, 128, 1>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
     return cudaErrorNotSupported;
 }
 
