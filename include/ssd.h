@@ -87,8 +87,9 @@ typedef struct {
 const char *ssd_status_string(ssd_status s);
 
 /* Bytes of device workspace ssd_fwd needs for `desc` (written to *bytes).
- * The workspace holds an error word, the in-chunk cumsum G, the local
- * (super-)chunk states and the (super-)chunk-start states, all float32.
+ * The workspace holds an error word, the in-chunk cumsum G, a float32 copy
+ * of dt in G's [b][h][L] layout, the local (super-)chunk states and the
+ * (super-)chunk-start states, all float32.
  * Errors: SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED. */
 ssd_status ssd_fwd_workspace_size(const ssd_desc *desc, size_t *bytes);
 

@@ -57,6 +57,7 @@ size_t esize(int dt) { return dt == SSD_BF16 ? 2 : 4; }
 struct Workspace {
     int *err;
     float *G;
+    float *dtT;       // dt as float32, [b][h][L] (written by the cumsum, read by chunk_state)
     float *s_local;
     float *h_start;
     size_t bytes;
@@ -72,9 +73,10 @@ Workspace carve(const Problem &pr, void *base)
     char *p = (char *)base;
     w.err = (int *)p;
     w.G = (float *)(p + e_bytes);
-    w.s_local = (float *)(p + e_bytes + g_bytes);
-    w.h_start = (float *)(p + e_bytes + g_bytes + s_bytes);
-    w.bytes = e_bytes + g_bytes + 2 * s_bytes;
+    w.dtT = (float *)(p + e_bytes + g_bytes);
+    w.s_local = (float *)(p + e_bytes + 2 * g_bytes);
+    w.h_start = (float *)(p + e_bytes + 2 * g_bytes + s_bytes);
+    w.bytes = e_bytes + 2 * g_bytes + 2 * s_bytes;
     return w;
 }
 
@@ -172,15 +174,19 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
     if (!workspace || !aligned(workspace, kWsAlign) || ws_bytes < w.bytes) return SSD_ERR_WORKSPACE;
 
     auto rec = [&](int i) -> bool { return !events || cudaEventRecord((cudaEvent_t)events[i], st) == cudaSuccess; };
+    const bool tc = use_tensor_cores(desc, pr);
     if (cudaMemsetAsync(w.err, 0, sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
-    if (!rec(0) || ssd::launch_chunk_cumsum(pr, dt, A, w.G, st) != cudaSuccess || !rec(1)) return SSD_ERR_CUDA;
+    if (!rec(0) || ssd::launch_chunk_cumsum(pr, dt, A, w.G, tc ? w.dtT : nullptr, st) != cudaSuccess ||
+        !rec(1))
+        return SSD_ERR_CUDA;
 
-    if (use_tensor_cores(desc, pr)) {
+    if (tc) {
         const int R = choose_chunks_per_super(pr);
         const int nsup = (int)((pr.nc + R - 1) / R);
         // states of super-chunks 0 .. nsup-2 (the last one's state is produced by the scan)
         if (!rec(2)) return SSD_ERR_CUDA;
-        if (nsup > 1 && ssd::launch_chunk_state_tc(pr, x, dt, Bm, w.G, w.s_local, R, nsup, nsup - 1, w.err, st) != cudaSuccess)
+        if (nsup > 1 && ssd::launch_chunk_state_tc(pr, x, dt, w.dtT, Bm, w.G, w.s_local, R, nsup, nsup - 1, w.err, st) !=
+                            cudaSuccess)
             return SSD_ERR_CUDA;
         if (!rec(3) || !rec(4)) return SSD_ERR_CUDA;
         if (nsup > 1 &&
@@ -297,7 +303,7 @@ ssd_status ssd_chunk_cumsum(const ssd_desc *desc, const void *dt, const float *A
     if (s != SSD_OK) return s;
     if (!nonempty(pr)) return SSD_OK;
     if (!dt || !A || !G || !aligned(G, 4) || !aligned(A, 4)) return SSD_ERR_INVALID_ARG;
-    return cuda_status(ssd::launch_chunk_cumsum(pr, dt, A, G, (cudaStream_t)stream));
+    return cuda_status(ssd::launch_chunk_cumsum(pr, dt, A, G, nullptr, (cudaStream_t)stream));
 }
 
 ssd_status ssd_chunk_state(const ssd_desc *desc, const void *x, const void *dt, const void *Bm,
@@ -312,7 +318,7 @@ ssd_status ssd_chunk_state(const ssd_desc *desc, const void *x, const void *dt, 
         return SSD_ERR_INVALID_ARG;
     const int nc = (int)pr.nc;
     cudaError_t e = use_tensor_cores(desc, pr)
-                        ? ssd::launch_chunk_state_tc(pr, x, dt, Bm, G, s_local, 1, nc, nc, nullptr, (cudaStream_t)stream)
+                        ? ssd::launch_chunk_state_tc(pr, x, dt, nullptr, Bm, G, s_local, 1, nc, nc, nullptr, (cudaStream_t)stream)
                         : ssd::launch_chunk_state_simt(pr, x, dt, Bm, G, s_local, (cudaStream_t)stream);
     return cuda_status(e);
 }

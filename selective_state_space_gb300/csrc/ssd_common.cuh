@@ -29,8 +29,9 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 }
 
 // Host-side launchers (one per stage).  Each returns the launch status.
+// dtT (nullable): also write dt as float32 in the [b][h][L] layout of G.
 cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *A, float *G,
-                                cudaStream_t st);
+                                float *dtT, cudaStream_t st);
 cudaError_t launch_chunk_state_simt(const Problem &pr, const void *x, const void *dt,
                                     const void *Bm, const float *G, float *s_local,
                                     cudaStream_t st);

@@ -29,9 +29,9 @@ namespace {
 template <typename Tin>
 __global__ void __launch_bounds__(256)
 k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *__restrict__ G,
-               int64_t L, int nh, int T)
+               float *__restrict__ dtT, int64_t L, int nh, int T)
 {
-    extern __shared__ float tile[];   // [T][33]
+    extern __shared__ float tile[];   // [T][33] G, then (dtT only) [T][33] dt
     __shared__ float run_sum[32][33]; // [run][head]
     const int k = blockIdx.x, hbase = blockIdx.y * 32, b = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -53,6 +53,11 @@ k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *_
             acc += a * v[i];
             if (32 * r + i < n) tile[(32 * r + i) * 33 + lane] = acc;
         }
+        if (dtT) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (32 * r + i < n) tile[(T + 32 * r + i) * 33 + lane] = v[i];
+        }
         run_sum[r][lane] = acc;
     }
     __syncthreads();
@@ -71,6 +76,10 @@ k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *_
         if (hh >= nh) continue;
         float *dst = G + ((int64_t)b * nh + hh) * L + t0;
         for (int t = lane; t < n; t += 32) dst[t] = tile[t * 33 + j] * kLog2e;
+        if (dtT) {
+            float *dd = dtT + ((int64_t)b * nh + hh) * L + t0;
+            for (int t = lane; t < n; t += 32) dd[t] = tile[(T + t) * 33 + j];
+        }
     }
 }
 
@@ -384,19 +393,19 @@ size_t scan_smem_bytes(const Problem &pr)
 }  // namespace
 
 cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *A, float *G,
-                                cudaStream_t st)
+                                float *dtT, cudaStream_t st)
 {
     dim3 grid((unsigned)pr.nc, (unsigned)((pr.nh + 31) / 32), (unsigned)pr.B);
-    const size_t smem = sizeof(float) * 33 * (size_t)pr.T;
+    const size_t smem = sizeof(float) * 33 * (size_t)pr.T * (dtT ? 2 : 1);
     cudaError_t e;
     if (pr.in_dt == SSD_BF16) {
         auto kern = k_chunk_cumsum<__nv_bfloat16>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
-        kern<<<grid, 256, smem, st>>>((const __nv_bfloat16 *)dt, A, G, pr.L, (int)pr.nh, (int)pr.T);
+        kern<<<grid, 256, smem, st>>>((const __nv_bfloat16 *)dt, A, G, dtT, pr.L, (int)pr.nh, (int)pr.T);
     } else {
         auto kern = k_chunk_cumsum<float>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
-        kern<<<grid, 256, smem, st>>>((const float *)dt, A, G, pr.L, (int)pr.nh, (int)pr.T);
+        kern<<<grid, 256, smem, st>>>((const float *)dt, A, G, dtT, pr.L, (int)pr.nh, (int)pr.T);
     }
     return cudaGetLastError();
 }

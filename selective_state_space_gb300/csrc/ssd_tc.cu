@@ -74,66 +74,91 @@ __device__ __forceinline__ void set_error(int *err, int bit)
 //   s^T[s][p] = sum_{t in super-chunk m} w_t B_t[s] x_t[p],
 //   w_t = dt_t exp2(decay from t to the end of the super-chunk)
 //       = dt_t exp2((G_last(k) - G_t) + sum_{k' > k in m} G_last(k')).
-// One CTA per (batch, super-chunk, HG consecutive heads of one B/C group): the heads
+// Work unit = (batch, super-chunk m, HG consecutive heads of one B/C group): the heads
 // share the B tile, and their scaled x tiles sit side by side as one N = HG*H operand.
+// The kernel is persistent: the units' 64-token stages are laid end to end and each
+// CTA takes an equal contiguous slice of them, so every SM streams the same number of
+// bytes through a 4..8-deep TMA ring.  A slice covers pieces of one or more units; a
+// unit cut by a slice boundary is finished by two CTAs that each add their part of the
+// sum into s_out (zeroed by the host beforehand), a unit inside one slice is stored.
 // MMA: D[s][hh*H + p] (TMEM lanes s) += B^T (A: M = s, K = t, MN-major, the TMA tile of
 // B) x (w o X) (B operand: K = t, N = HG*H, MN-major, x tiles scaled in place).
 // Warp 0 issues TMA, warp 1 issues MMAs, warps 2..5 scale x and drain the accumulator.
 // ===========================================================================
 template <int S, int H, int HG>
 struct StateCfg {
-    static constexpr int kStages = 2;
+    static constexpr int kTok = 64;                        // tokens per stage (MMA K per stage)
+    static constexpr uint32_t kAtomT = kTok * 128;         // one 64-row x 128-byte swizzled region
     static constexpr int kN = HG * H;                      // MMA N: all heads' p columns
-    static constexpr uint32_t kBBytes = (S / 64) * kAtom;
-    static constexpr uint32_t kXBytes = (kN / 64) * kAtom;
-    static constexpr uint32_t kStage = kBBytes + kXBytes;
+    static constexpr uint32_t kBBytes = (S / 64) * kAtomT;
+    static constexpr uint32_t kXBytes = (kN / 64) * kAtomT;
+    // G and dt rows of the stage, [2][HG][kTok] f32, padded to keep stages 1024-byte aligned
+    static constexpr uint32_t kSideBytes = (2 * HG * kTok * 4 + 1023) / 1024 * 1024;
+    static constexpr uint32_t kStage = kBBytes + kXBytes + kSideBytes;   // a multiple of 1024
+    static constexpr int kStages = (204 * 1024) / kStage < 8 ? (204 * 1024) / kStage : 8;
     static constexpr int kMaxR = 256;
-    static constexpr uint32_t kSmem = kStages * kStage + HG * kMaxR * 4 + 256 + 1024;
+    // per chunk k of the unit: sum of G_last over chunks k..R-1, [2 pieces][HG][kMaxR], and a
+    // staging copy of the G_last values themselves, [HG][kMaxR]
+    static constexpr uint32_t kGl = kStages * kStage;
+    static constexpr uint32_t kGraw = kGl + 2 * HG * kMaxR * 4;
+    static constexpr uint32_t kBars = kGraw + HG * kMaxR * 4;
+    // barriers: full[kStages], free[kStages], x_ready[kStages], done, drained; then the TMEM slot
+    static constexpr int kNumBars = 3 * kStages + 2;
+    static constexpr uint32_t kSmem = kBars + kNumBars * 8 + 8 + 1024;
     static constexpr uint32_t kCols = (S / 128) * kN;
     static constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : (kCols <= 64 ? 64 : (kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512)));
+    static_assert(kStages >= 4, "TMA ring too shallow");
+    static_assert(kStage % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 };
+
+// (batch, super-chunk, first head) of a chunk_state unit; head groups vary fastest.
+struct StateUnit {
+    int b, m, h0;
+};
+
+__device__ __forceinline__ StateUnit state_unit(int64_t u, int nhq, int nm, int HG)
+{
+    StateUnit r;
+    r.h0 = (int)(u % nhq) * HG;
+    u /= nhq;
+    r.m = (int)(u % nm);
+    r.b = (int)(u / nm);
+    return r;
+}
 
 template <int S, int H, int HG>
 __global__ void __launch_bounds__(192, 1)
 k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmX,
-                 const float *__restrict__ G, const __nv_bfloat16 *__restrict__ dt, float *__restrict__ s_out,
-                 Problem pr, int R, int nsup, int nm, int *err)
+                 const float *__restrict__ G, const __nv_bfloat16 *__restrict__ dt, const float *__restrict__ dtT,
+                 float *__restrict__ s_out, Problem pr, int R, int nsup, int nm, int *err)
 {
     using Cfg = StateCfg<S, H, HG>;
-    constexpr int kN = Cfg::kN;
+    constexpr int kN = Cfg::kN, kS = Cfg::kStages, kTok = Cfg::kTok;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    float *sGl = (float *)(smem + Cfg::kStages * Cfg::kStage);                    // [HG][kMaxR] G_last per chunk
-    uint64_t *bars = (uint64_t *)(smem + Cfg::kStages * Cfg::kStage + HG * Cfg::kMaxR * 4);
-    uint32_t *tmem_slot = (uint32_t *)(bars + 8);
-    // bars: [0,1] full, [2,3] free, [4,5] x_ready (per stage), [6] done
+    float *sGl = (float *)(smem + Cfg::kGl);
+    float *sGraw = (float *)(smem + Cfg::kGraw);
+    uint64_t *bars = (uint64_t *)(smem + Cfg::kBars);
+    uint32_t *tmem_slot = (uint32_t *)(bars + Cfg::kNumBars);
+    constexpr int kFullB = 0, kFreeB = kS, kReadyB = 2 * kS, kDoneB = 3 * kS, kDrainedB = 3 * kS + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // unit = (b, m, head group hq) for m < nm; head groups fastest
     const int nhq = (int)(pr.nh / HG);
-    int u = blockIdx.x;
-    const int hq = u % nhq; u /= nhq;
-    const int m = u % nm;
-    const int b = u / nm;
-    const int h0 = hq * HG;
-    const int g = (int)(h0 / pr.hpg);
-    const int k_begin = m * R;
-    const int k_end = min((int)pr.nc, k_begin + R);
-    const int nk = k_end - k_begin;
-    const int qpc = (int)(pr.T / kQ);                    // sub-chunks per chunk
-    const int nq = nk * qpc;
-    const int64_t t_begin = (int64_t)k_begin * pr.T;
-    const float *G0 = G + ((int64_t)b * pr.nh + h0) * pr.L;   // head h0 + hh: G0 + hh * L
+    const int qpc = (int)(pr.T / kTok);                      // stages per chunk
+    const int64_t nq_u = (int64_t)R * qpc;                   // stages per unit (every unit holds R chunks)
+    const int64_t total = (int64_t)pr.B * nm * nhq * nq_u;
+    const int64_t q_lo = total * blockIdx.x / gridDim.x;
+    const int64_t q_hi = total * (blockIdx.x + 1) / gridDim.x;
+    // staged: the TMA thread also copies each stage's G and dt rows (dt from the float32
+    // [b][h][L] copy) into the stage; otherwise every thread loads its row one stage ahead
+    const bool staged = dtT != nullptr;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 7; ++i) mbar_init(smem_u32(&bars[i]), (i >= 4 && i < 6) ? 128 : 1);
+        for (int i = 0; i < Cfg::kNumBars; ++i)
+            mbar_init(smem_u32(&bars[i]), ((i >= kReadyB && i < kDoneB) || i == kDrainedB) ? 128 : 1);
         fence_mbar_init();
     }
     if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols); tmem_relinquish(); }
-    for (int i = threadIdx.x; i < HG * nk; i += blockDim.x) {
-        const int hh = i / nk, kk = i % nk;
-        sGl[hh * Cfg::kMaxR + kk] = G0[(int64_t)hh * pr.L + (int64_t)(k_begin + kk) * pr.T + pr.T - 1];
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -144,109 +169,173 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
         if (lane == 0) {
             prefetch_tmap(&tmB);
             prefetch_tmap(&tmX);
-            for (int q = 0; q < nq && ok; ++q) {
-                const int st = q % Cfg::kStages;
-                if (q >= Cfg::kStages && !mbar_wait(smem_u32(&bars[2 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs)) {
+            for (int64_t gq = q_lo; gq < q_hi; ++gq) {
+                const int i = (int)(gq - q_lo), st = i % kS;
+                if (i >= kS && !mbar_wait(smem_u32(&bars[kFreeB + st]), ((i / kS) - 1) & 1, kWaitNs)) {
                     ok = false; set_error(err, 1); break;
                 }
+                const StateUnit un = state_unit(gq / nq_u, nhq, nm, HG);
+                const int g = (int)(un.h0 / pr.hpg);
+                const int t0 = (int)((int64_t)un.m * R * pr.T + (gq % nq_u) * kTok);
                 uint8_t *base = smem + st * Cfg::kStage;
-                const uint32_t full = smem_u32(&bars[st]);
-                mbar_arrive_expect_tx(full, Cfg::kStage);
-                const int t0 = (int)(t_begin + (int64_t)q * kQ);
-                for (int a = 0; a < S / 64; ++a) tma_load_4d(smem_u32(base + a * kAtom), &tmB, full, 64 * a, g, t0, b);
+                const uint32_t full = smem_u32(&bars[kFullB + st]);
+                mbar_arrive_expect_tx(full, Cfg::kBBytes + Cfg::kXBytes + (staged ? Cfg::kSideBytes : 0u));
+                if (staged) {
+                    uint8_t *side = base + Cfg::kBBytes + Cfg::kXBytes;
+                    for (int hh = 0; hh < HG; ++hh) {
+                        const int64_t row = ((int64_t)un.b * pr.nh + un.h0 + hh) * pr.L + t0;
+                        bulk_load(smem_u32(side + hh * kTok * 4), G + row, kTok * 4, full);
+                        bulk_load(smem_u32(side + (HG + hh) * kTok * 4), dtT + row, kTok * 4, full);
+                    }
+                }
+                for (int a = 0; a < S / 64; ++a)
+                    tma_load_4d(smem_u32(base + a * Cfg::kAtomT), &tmB, full, 64 * a, g, t0, un.b);
                 for (int a = 0; a < kN / 64; ++a)   // atom a: head h0 + a / (H/64), columns 64 * (a % (H/64))
-                    tma_load_4d(smem_u32(base + Cfg::kBBytes + a * kAtom), &tmX, full, 64 * (a % (H / 64)),
-                                h0 + a / (H / 64), t0, b);
+                    tma_load_4d(smem_u32(base + Cfg::kBBytes + a * Cfg::kAtomT), &tmX, full, 64 * (a % (H / 64)),
+                                un.h0 + a / (H / 64), t0, un.b);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, kN, 1, 1);
-            for (int q = 0; q < nq && ok; ++q) {
-                const int st = q % Cfg::kStages;
-                if (!mbar_wait(smem_u32(&bars[4 + st]), (q / Cfg::kStages) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
+            int piece = 0;
+            for (int64_t gq = q_lo; gq < q_hi; ++gq) {
+                const int i = (int)(gq - q_lo), st = i % kS;
+                const bool first = gq == q_lo || gq % nq_u == 0;
+                const bool last = gq + 1 == q_hi || (gq + 1) % nq_u == 0;
+                // a new piece overwrites the accumulator: the previous one must be drained
+                if (first && piece > 0 && !mbar_wait(smem_u32(&bars[kDrainedB]), (piece - 1) & 1, kWaitNs)) {
+                    ok = false; set_error(err, 1); break;
+                }
+                if (!mbar_wait(smem_u32(&bars[kReadyB + st]), (i / kS) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
                 tc_fence_after();
                 const uint32_t bbase = smem_u32(smem + st * Cfg::kStage);
                 const uint32_t xbase = bbase + Cfg::kBBytes;
-                const uint64_t ad0 = smem_desc(bbase, kAtom, 1024), bd0 = smem_desc(xbase, kAtom, 1024);
+                const uint64_t ad0 = smem_desc(bbase, Cfg::kAtomT, 1024), bd0 = smem_desc(xbase, Cfg::kAtomT, 1024);
 #pragma unroll
                 for (int lb = 0; lb < S / 128; ++lb) {
 #pragma unroll
-                    for (int kk = 0; kk < kQ / 16; ++kk)
-                        mma_bf16(tmem + lb * kN, ad0 + (uint64_t)((lb * 2 * kAtom + kk * 2048) >> 4),
-                                 bd0 + (uint64_t)((kk * 2048) >> 4), idesc, (q > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kTok / 16; ++kk)
+                        mma_bf16(tmem + lb * kN, ad0 + (uint64_t)((lb * 2 * Cfg::kAtomT + kk * 2048) >> 4),
+                                 bd0 + (uint64_t)((kk * 2048) >> 4), idesc, (!first || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(smem_u32(&bars[2 + st]));
+                mma_commit(smem_u32(&bars[kFreeB + st]));
+                if (last) { mma_commit(smem_u32(&bars[kDoneB])); ++piece; }
             }
-            if (ok) mma_commit(smem_u32(&bars[6]));
         }
         __syncwarp();
     } else {
-        // warps 2..5: scale x rows in place (each head by its own w), then drain the accumulator
-        const int r = 32 * (warp & 3) + lane;       // token row of the tile / TMEM lane
-        // this row's dt and G for every head, loaded one sub-chunk ahead
+        // warps 2..5: scale x rows in place (each head by its own w), then drain the accumulator.
+        // All 128 threads walk the same pieces and stages (work is skipped after an error), so
+        // the named barrier below is always reached by all of them.
+        const int tid = threadIdx.x - 64;
+        const int r = 32 * (warp & 3) + lane;       // TMEM lane (state row s in the epilogue)
+        const int xr = r & (kTok - 1);              // token row of the stage this thread scales
+        const int xc0 = (r / kTok) * 4;             // first of its four 16-byte chunks per row
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        // this row's dt and G for every head, loaded one stage ahead
         float n_dt[HG], n_g[HG];
-        auto load_row = [&](int q) {
-            const int64_t t = t_begin + (int64_t)q * kQ + r;
+        auto load_row = [&](int64_t gq) {
+            const StateUnit un = state_unit(gq / nq_u, nhq, nm, HG);
+            const int64_t t = (int64_t)un.m * R * pr.T + (gq % nq_u) * kTok + xr;
 #pragma unroll
             for (int hh = 0; hh < HG; ++hh) {
-                n_dt[hh] = __bfloat162float(dt[((int64_t)b * pr.L + t) * pr.nh + h0 + hh]);
-                n_g[hh] = G0[(int64_t)hh * pr.L + t];
+                n_dt[hh] = __bfloat162float(dt[((int64_t)un.b * pr.L + t) * pr.nh + un.h0 + hh]);
+                n_g[hh] = G[((int64_t)un.b * pr.nh + un.h0 + hh) * pr.L + t];
             }
         };
-        if (nq > 0) load_row(0);
-        for (int q = 0; q < nq && ok; ++q) {
-            const int st = q % Cfg::kStages;
-            float dtr[HG], gr[HG];
-#pragma unroll
-            for (int hh = 0; hh < HG; ++hh) { dtr[hh] = n_dt[hh]; gr[hh] = n_g[hh]; }
-            if (q + 1 < nq) load_row(q + 1);
-            const int kl = q / qpc;                          // chunk index inside the super-chunk
-            float wr[HG];
-#pragma unroll
-            for (int hh = 0; hh < HG; ++hh) {
-                float suffix = 0.f;
-                for (int kk = kl + 1; kk < nk; ++kk) suffix += sGl[hh * Cfg::kMaxR + kk];
-                wr[hh] = dtr[hh] * exp2f((sGl[hh * Cfg::kMaxR + kl] - gr[hh]) + suffix);
+        if (!staged && q_lo < q_hi) load_row(q_lo);
+        int piece = 0;
+        for (int64_t gq = q_lo; gq < q_hi; ++piece) {
+            const int64_t u = gq / nq_u;
+            const int64_t p_begin = gq, p_end = q_hi < (u + 1) * nq_u ? q_hi : (u + 1) * nq_u;
+            const StateUnit un = state_unit(u, nhq, nm, HG);
+            // log2 decay from the end of chunk k to the end of the super-chunk, plus chunk k's own
+            // G_last: gl[hh][k] = sum_{k' >= k} G_last(k'), per head (double-buffered by piece)
+            float *gl = sGl + (piece & 1) * (HG * Cfg::kMaxR);
+            for (int idx = tid; idx < HG * R; idx += 128) {
+                const int hh = idx / R, kk = idx % R;
+                sGraw[hh * Cfg::kMaxR + kk] =
+                    G[((int64_t)un.b * pr.nh + un.h0 + hh) * pr.L + ((int64_t)un.m * R + kk) * pr.T + pr.T - 1];
             }
-            if (!mbar_wait(smem_u32(&bars[st]), (q / Cfg::kStages) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
-            uint8_t *xt = smem + st * Cfg::kStage + Cfg::kBBytes;
+            named_bar_sync(1, 128);
+            for (int idx = tid; idx < HG * R; idx += 128) {
+                const int hh = idx / R, kk = idx % R;
+                float acc = 0.f;
+                for (int k2 = R - 1; k2 >= kk; --k2) acc += sGraw[hh * Cfg::kMaxR + k2];
+                gl[hh * Cfg::kMaxR + kk] = acc;
+            }
+            named_bar_sync(1, 128);
+            for (; gq < p_end; ++gq) {
+                const int i = (int)(gq - q_lo), st = i % kS;
+                float dtr[HG], gr[HG];
+                if (!staged) {
 #pragma unroll
-            for (int a = 0; a < kN / 64; ++a) {
-                const float w = wr[a / (H / 64)];
+                    for (int hh = 0; hh < HG; ++hh) { dtr[hh] = n_dt[hh]; gr[hh] = n_g[hh]; }
+                    if (gq + 1 < q_hi) load_row(gq + 1);
+                }
+                const int kl = (int)((gq % nq_u) / qpc);           // chunk index inside the super-chunk
+                float lw[HG];                                       // log2 of w / dt, without this row's G
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 *p = (uint4 *)(xt + a * kAtom + sw128(r, c));
-                    uint4 v = *p;
-                    float2 f0 = unpack_bf16x2(v.x), f1 = unpack_bf16x2(v.y), f2 = unpack_bf16x2(v.z), f3 = unpack_bf16x2(v.w);
-                    v.x = pack_bf16x2(f0.x * w, f0.y * w);
-                    v.y = pack_bf16x2(f1.x * w, f1.y * w);
-                    v.z = pack_bf16x2(f2.x * w, f2.y * w);
-                    v.w = pack_bf16x2(f3.x * w, f3.y * w);
-                    *p = v;
+                for (int hh = 0; hh < HG; ++hh) lw[hh] = gl[hh * Cfg::kMaxR + kl];
+                if (ok && !mbar_wait(smem_u32(&bars[kFullB + st]), (i / kS) & 1, kWaitNs)) { ok = false; set_error(err, 1); }
+                if (ok) {
+                    if (staged) {
+                        const float *side = (const float *)(smem + st * Cfg::kStage + Cfg::kBBytes + Cfg::kXBytes);
+#pragma unroll
+                        for (int hh = 0; hh < HG; ++hh) { gr[hh] = side[hh * kTok + xr]; dtr[hh] = side[(HG + hh) * kTok + xr]; }
+                    }
+                    float wr[HG];
+#pragma unroll
+                    for (int hh = 0; hh < HG; ++hh) wr[hh] = dtr[hh] * exp2f(lw[hh] - gr[hh]);
+                    uint8_t *xt = smem + st * Cfg::kStage + Cfg::kBBytes;
+#pragma unroll
+                    for (int a = 0; a < kN / 64; ++a) {
+                        const float w = wr[a / (H / 64)];
+#pragma unroll
+                        for (int c = xc0; c < xc0 + 4; ++c) {
+                            uint4 *p = (uint4 *)(xt + a * Cfg::kAtomT + sw128(xr, c));
+                            uint4 v = *p;
+                            float2 f0 = unpack_bf16x2(v.x), f1 = unpack_bf16x2(v.y), f2 = unpack_bf16x2(v.z),
+                                   f3 = unpack_bf16x2(v.w);
+                            v.x = pack_bf16x2(f0.x * w, f0.y * w);
+                            v.y = pack_bf16x2(f1.x * w, f1.y * w);
+                            v.z = pack_bf16x2(f2.x * w, f2.y * w);
+                            v.w = pack_bf16x2(f3.x * w, f3.y * w);
+                            *p = v;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(smem_u32(&bars[kReadyB + st]));
                 }
             }
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bars[4 + st]));
-        }
-        if (ok && !mbar_wait(smem_u32(&bars[6]), 0, kWaitNs)) { ok = false; set_error(err, 1); }
-        if (ok) {
-            tc_fence_after();
-            const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+            // drain the piece: a whole unit is stored, a part of one is added
+            const bool whole = p_begin % nq_u == 0 && p_end % nq_u == 0;
+            if (ok && !mbar_wait(smem_u32(&bars[kDoneB]), piece & 1, kWaitNs)) { ok = false; set_error(err, 1); }
+            if (ok) {
+                tc_fence_after();
 #pragma unroll
-            for (int lb = 0; lb < S / 128; ++lb) {
-                const int s = lb * 128 + r;
+                for (int lb = 0; lb < S / 128; ++lb) {
+                    const int s = lb * 128 + r;
+#pragma unroll 4
+                    for (int c0 = 0; c0 < kN; c0 += 16) {
+                        const int hh = c0 / H, p0 = c0 % H;
+                        float *dst = s_out + (((int64_t)un.b * pr.nh + un.h0 + hh) * nsup + un.m) * (int64_t)(H * S) + s;
+                        uint32_t v[16];
+                        tmem_ld16(tmem + lane_base + lb * kN + c0, v);
+                        tmem_ld_wait();
+                        if (whole) {
 #pragma unroll
-                for (int c0 = 0; c0 < kN; c0 += 16) {
-                    const int hh = c0 / H, p0 = c0 % H;
-                    float *dst = s_out + (((int64_t)b * pr.nh + h0 + hh) * nsup + m) * (int64_t)(H * S);
-                    uint32_t v[16];
-                    tmem_ld16(tmem + lane_base + lb * kN + c0, v);
-                    tmem_ld_wait();
+                            for (int j = 0; j < 16; ++j) dst[(int64_t)(p0 + j) * S] = __uint_as_float(v[j]);
+                        } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) dst[(int64_t)(p0 + j) * S + s] = __uint_as_float(v[j]);
+                            for (int j = 0; j < 16; ++j) atomicAdd(dst + (int64_t)(p0 + j) * S, __uint_as_float(v[j]));
+                        }
+                    }
                 }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars[kDrainedB]));
             }
         }
     }
@@ -766,20 +855,42 @@ bool make_map_4d(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, ui
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int S, int H, int HG>
-cudaError_t state_launch(const Problem &pr, const void *x, const void *dt, const void *Bm, const float *G, float *s_out,
-                         int R, int nsup, int nm, int *err, cudaStream_t st)
+int current_sms()
 {
-    CUtensorMap mB, mX;
-    if (!make_map_4d(&mB, Bm, pr.S, pr.G, pr.L, pr.B, kQ) || !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, kQ))
-        return cudaErrorInvalidValue;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    return sms > 0 ? sms : 1;
+}
+
+template <int S, int H, int HG>
+cudaError_t state_launch(const Problem &pr, const void *x, const void *dt, const float *dtT, const void *Bm,
+                         const float *G, float *s_out, int R, int nsup, int nm, int *err, cudaStream_t st)
+{
     using Cfg = StateCfg<S, H, HG>;
+    if (R > Cfg::kMaxR) return cudaErrorInvalidValue;
+    // every unit must hold R whole chunks (a short last super-chunk is left to the scan)
+    if ((int64_t)nm * R > pr.nc) return cudaErrorInvalidValue;
+    const int64_t nq_u = (int64_t)R * (pr.T / Cfg::kTok);
+    const int64_t total = pr.B * (int64_t)nm * (pr.nh / HG) * nq_u;
+    if (total == 0) return cudaSuccess;
+    CUtensorMap mB, mX;
+    if (!make_map_4d(&mB, Bm, pr.S, pr.G, pr.L, pr.B, Cfg::kTok) || !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, Cfg::kTok))
+        return cudaErrorInvalidValue;
     auto kern = k_chunk_state_tc<S, H, HG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(pr.B * nm * (pr.nh / HG));
-    if (grid == 0) return cudaSuccess;
-    kern<<<grid, 192, Cfg::kSmem, st>>>(mB, mX, G, (const __nv_bfloat16 *)dt, s_out, pr, R, nsup, nm, err);
+    const int64_t sms = current_sms();
+    const int64_t grid = total < sms ? total : sms;
+    // a slice boundary inside a unit: both parts add into a zeroed s_out
+    bool split = false;
+    for (int64_t c = 1; c < grid && !split; ++c) split = (total * c / grid) % nq_u != 0;
+    if (split) {
+        e = cudaMemsetAsync(s_out, 0, (size_t)(pr.B * pr.nh * nsup) * (size_t)(pr.H * pr.S) * sizeof(float), st);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<(unsigned)grid, 192, Cfg::kSmem, st>>>(mB, mX, G, (const __nv_bfloat16 *)dt, dtT, s_out, pr, R, nsup, nm,
+                                                   err);
     return cudaGetLastError();
 }
 
@@ -815,23 +926,23 @@ bool tc_supported(const Problem &pr)
     return true;
 }
 
-cudaError_t launch_chunk_state_tc(const Problem &pr, const void *x, const void *dt, const void *Bm, const float *G,
-                                  float *s_out, int R, int nsup, int nm, int *err, cudaStream_t st)
+cudaError_t launch_chunk_state_tc(const Problem &pr, const void *x, const void *dt, const float *dtT, const void *Bm,
+                                  const float *G, float *s_out, int R, int nsup, int nm, int *err, cudaStream_t st)
 {
     if (R < 1 || R > 256) return cudaErrorInvalidValue;
     // heads per CTA: as many heads of one group as fit N = HG * H <= 256 (S = 128)
     const int hpg = (int)pr.hpg;
     if (pr.S == 128 && pr.H == 64) {
-        if (hpg % 4 == 0) return state_launch<128, 64, 4>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
-        if (hpg % 2 == 0) return state_launch<128, 64, 2>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
-        return state_launch<128, 64, 1>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
+        if (hpg % 4 == 0) return state_launch<128, 64, 4>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+        if (hpg % 2 == 0) return state_launch<128, 64, 2>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+        return state_launch<128, 64, 1>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
     }
     if (pr.S == 128 && pr.H == 128) {
-        if (hpg % 2 == 0) return state_launch<128, 128, 2>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
-        return state_launch<128, 128, 1>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
+        if (hpg % 2 == 0) return state_launch<128, 128, 2>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+        return state_launch<128, 128, 1>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
     }
-    if (pr.S == 256 && pr.H == 64) return state_launch<256, 64, 1>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
-    if (pr.S == 256 && pr.H == 128) return state_launch<256, 128, 1>(pr, x, dt, Bm, G, s_out, R, nsup, nm, err, st);
+    if (pr.S == 256 && pr.H == 64) return state_launch<256, 64, 1>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+    if (pr.S == 256 && pr.H == 128) return state_launch<256, 128, 1>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
     return cudaErrorNotSupported;
 }
 

@@ -10,10 +10,12 @@ namespace ssd {
 bool tc_supported(const Problem &pr);
 
 // States of super-chunks m < nm (R chunks each) from a zero start, written to
-// s_local[b][h][m] with a super-chunk extent of nsup.  `err` receives error bits.
-cudaError_t launch_chunk_state_tc(const Problem &pr, const void *x, const void *dt, const void *Bm,
-                                  const float *G, float *s_local, int R, int nsup, int nm, int *err,
-                                  cudaStream_t st);
+// s_local[b][h][m] with a super-chunk extent of nsup.  dtT (nullable) is dt as float32
+// in the [b][h][L] layout of G; with it, dt and G reach the kernel by bulk copies
+// instead of per-thread loads.  `err` receives error bits.
+cudaError_t launch_chunk_state_tc(const Problem &pr, const void *x, const void *dt, const float *dtT,
+                                  const void *Bm, const float *G, float *s_local, int R, int nsup, int nm,
+                                  int *err, cudaStream_t st);
 // Output y for every super-chunk (R chunks, nsup of them): super-chunks m < hs_from
 // start from h0 (NULL: zeros), the others from h_start[b][h][m]; the last super-chunk
 // also writes h_final when it is not NULL.

@@ -66,7 +66,7 @@ def test_workspace_size_arithmetic(lib):
     nc = (L + T - 1) // T
     al = lambda v: (v + 255) // 256 * 256
     # error word + G + local states + chunk-start states (float32)
-    assert n == 256 + al(4 * B * nh * L) + 2 * al(4 * B * nh * nc * H * S)
+    assert n == 256 + 2 * al(4 * B * nh * L) + 2 * al(4 * B * nh * nc * H * S)
     rc, n = ws_size(lib, desc(seqlen=0))
     assert rc == 0 and n == 0
     rc, n = ws_size(lib, desc(seqlen=513))   # ragged: one more chunk
