@@ -349,9 +349,9 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
 // (batch, head, 64-column p block), 128 tokens at a time, carrying the state.
 // For a sub-chunk with rows i, j (tokens) and entering state h (H x S):
 //   CB      = C B^T                                   (TMEM, fp32; M = i, N = j, K = s)
-//   P[i][j] = CB[i][j] exp2(G_i - G_j) if j <= i else 0  (CUDA cores, bf16, swizzled)
+//   P[i][j] = CB[i][j] exp2(G_i - G_j) if j <= i else 0  (CUDA cores; bf16, back into TMEM)
 //   Ys      = C h^T                                   (M = i, N = p, K = s)
-//   Yi      = P (dt o X)                              (M = i, N = p, K = j)
+//   Yi      = P (dt o X)                              (M = i, N = p, K = j; A operand from TMEM)
 //   y_i     = exp2(G_i - G_base) Ys_i + Yi_i + D x_i
 //   h'^T    = exp2(G_last - G_base) h^T + B^T (w o X),  w_t = dt_t exp2(G_last - G_t)
 // The state lives in TMEM as h^T (lanes s, columns p); a bf16 copy [s][p] in shared
@@ -360,35 +360,46 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
 //
 // Warp roles: warp 0 issues TMA, warp 1 issues every MMA (and owns TMEM).
 // Warps 2..5 ("state group") hand the state over between sub-chunks and scale the
-// x tile (dt o x in place, w o x into its own tile).  Warps 6..13 ("output group",
-// two warps per TMEM lane quarter splitting the columns) build P and write y.  The two groups run concurrently; the MMA issue order
-// (CB, Ys, state update, Yi, next CB) lets the state chain advance without
-// waiting for P.  Ys/Yi are double-buffered in TMEM so the next sub-chunk's Ys can
-// start while the output group drains the previous one.
+// x tile (dt o x in place, w o x into its own tile).  Warps 6..13 ("output group", two warps per TMEM lane quarter
+// splitting the columns) build P and write y.  MMA
+// issue order per sub-chunk: Ys, state update, Yi, next CB; the state chain therefore
+// never waits for P, and the tensor pipe runs Ys and the update while P is built.
+// Buffers: C/B tiles in a 2-stage ring (1 stage for S = 256), x tiles in a 4-stage ring
+// (3 for S = 256) whose slots also stage y for its bulk tensor store, Ys (S = 128) and
+// Yi double-buffered in TMEM so one sub-chunk's epilogue overlaps the next sub-chunk's
+// MMAs.  The tensor cores read shared memory at 128 B per clock, the same port TMA and
+// the CUDA cores use; P lives in TMEM (the A operand of Yi), which keeps it off that
+// port.  y goes through shared memory because a bulk store writes whole lines of it;
+// stores from the row-per-lane TMEM layout would touch 32 rows per instruction.
 // ===========================================================================
 template <int S>
 struct ScanCfg {
-    static constexpr int kStages = (S <= 128) ? 2 : 1;
-    static constexpr uint32_t kCBytes = (S / 64) * kAtom;    // C tile [i][s], K-major
-    static constexpr uint32_t kBBytes = (S / 64) * kAtom;    // B tile [j][s]
-    static constexpr uint32_t kXBytes = kAtom;               // x tile [t][p], 64 p
-    static constexpr uint32_t kStage = kCBytes + kBBytes + kXBytes;
-    static constexpr uint32_t kXw = kStages * kStage;        // w o x   [t][p]
-    static constexpr uint32_t kP = kXw + kAtom;              // P       [i][j], 2 K-atoms
-    static constexpr uint32_t kH = kP + 2 * kAtom;           // h bf16  [s][p], S rows
-    static constexpr uint32_t kSmall = kH + S * 128;         // sG[128], sF[128] (output group)
+    static constexpr int kCBStages = (S <= 128) ? 2 : 1;     // C and B tiles
+    static constexpr int kXStages = (S <= 128) ? 4 : 3;       // x tiles, then y staging
+    static constexpr int kYsBufs = (S <= 128) ? 2 : 1;
+    static constexpr uint32_t kCBytes = (S / 64) * kAtom;     // C tile [i][s], K-major
+    static constexpr uint32_t kBBytes = (S / 64) * kAtom;     // B tile [j][s]
+    static constexpr uint32_t kCBStage = kCBytes + kBBytes;
+    static constexpr uint32_t kX = kCBStages * kCBStage;      // x ring: [t][p], 64 p per tile
+    static constexpr uint32_t kXw = kX + kXStages * kAtom;    // w o x   [t][p]
+    static constexpr uint32_t kH = kXw + kAtom;               // h bf16  [s][p], S rows
+    // output group, per column j of the sub-chunk: G_j and 2^(G_blockend - G_j)
+    static constexpr uint32_t kSmall = kH + S * 128;
     static constexpr uint32_t kBars = kSmall + 2 * kQ * 4;
     static constexpr uint32_t kSmem = kBars + 256 + 1024;
-    // TMEM columns: CB, Ys/Yi in two buffers, state (S/128 blocks of 64 columns)
-    static constexpr uint32_t kTcb = 0, kTys = 128, kTyi = 192, kTyStride = 128, kTds = 384;
+    // TMEM columns: CB, P (bf16 pairs), Ys buffers, two Yi buffers, state (S/128 blocks of 64)
+    static constexpr uint32_t kTcb = 0, kTp = 128, kTys = 192, kTyi = kTys + 64 * kYsBufs, kTds = kTyi + 128;
     static constexpr uint32_t kTmemCols = 512;
+    static_assert(kTds + (S / 128) * kPB <= kTmemCols, "TMEM columns");
+    static_assert(kSmem <= 227 * 1024, "shared memory");
+    static_assert(kXStages <= 4, "x-slot barriers");
 };
 
-// kFull/kFree: the C and B tiles of a stage; kXFull/kXFree: its x tile (also the y staging
-// tile, released to the producer only after kYSt: the bulk store has read it).
+// kFull/kFree: the C and B tiles of a C/B stage; kXFull: an x tile; kYSt: the y staged
+// in an x slot has been read by its bulk store (the slot may be reloaded).
 enum ScanBar {
-    kFull0 = 0, kFree0 = 2, kCb = 4, kHReady, kXReady, kPReady, kIntra, kUpdate, kEpi0, kEpi1, kOutGroup,
-    kYSt0, kYSt1, kXFull0, kXFull1, kXFree0, kXFree1, kNumScanBars
+    kFull0 = 0, kFree0 = 2, kCb = 4, kHReady, kXReady, kPReady, kIntra, kUpdate, kEpi0, kEpi1,
+    kXFull0, kYSt0 = kXFull0 + 4, kNumScanBars = kYSt0 + 4
 };
 
 template <int S>
@@ -401,6 +412,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 __nv_bfloat16 *__restrict__ y, Problem pr, int R, int nsup, int hs_from, int *err)
 {
     using Cfg = ScanCfg<S>;
+    constexpr int kCBS = Cfg::kCBStages, kXS = Cfg::kXStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float *sG = (float *)(smem + Cfg::kSmall);
@@ -427,8 +439,8 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumScanBars; ++i) {
             uint32_t cnt = 1;
-            if (i == kHReady || i == kXReady) cnt = 128;                                  // state group
-            if (i == kPReady || i == kEpi0 || i == kEpi1 || i == kOutGroup) cnt = 256;    // output group
+            if (i == kHReady || i == kXReady) cnt = 128;                 // state group
+            if (i == kPReady || i == kEpi0 || i == kEpi1) cnt = 256;     // output group
             mbar_init(smem_u32(&bars[i]), cnt);
         }
         fence_mbar_init();
@@ -447,29 +459,27 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             prefetch_tmap(&tmB);
             prefetch_tmap(&tmX);
             for (int q = 0; q < nq && ok; ++q) {
-                const int st = q % Cfg::kStages;
+                const int t0 = (int)(t_begin + (int64_t)q * kQ);
                 // C and B tiles: free once the MMAs reading them (CB, Ys, state update) are done
-                if (q >= Cfg::kStages &&
-                    !mbar_wait(smem_u32(&bars[kFree0 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs)) {
+                const int cs = q % kCBS;
+                if (q >= kCBS && !mbar_wait(smem_u32(&bars[kFree0 + cs]), ((q / kCBS) - 1) & 1, kWaitNs)) {
                     ok = false; set_error(err, 1); break;
                 }
-                uint8_t *base = smem + st * Cfg::kStage;
-                const uint32_t full = smem_u32(&bars[kFull0 + st]);
-                mbar_arrive_expect_tx(full, Cfg::kCBytes + Cfg::kBBytes);
-                const int t0 = (int)(t_begin + (int64_t)q * kQ);
+                uint8_t *base = smem + cs * Cfg::kCBStage;
+                const uint32_t full = smem_u32(&bars[kFull0 + cs]);
+                mbar_arrive_expect_tx(full, Cfg::kCBStage);
                 for (int a = 0; a < S / 64; ++a) {
                     tma_load_4d(smem_u32(base + a * kAtom), &tmC, full, 64 * a, g, t0, b);
                     tma_load_4d(smem_u32(base + Cfg::kCBytes + a * kAtom), &tmB, full, 64 * a, g, t0, b);
                 }
-                // x tile: free once the Yi MMA has read it and the y tile staged in it has been stored
-                if (q >= Cfg::kStages &&
-                    (!mbar_wait(smem_u32(&bars[kXFree0 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs) ||
-                     !mbar_wait(smem_u32(&bars[kYSt0 + st]), ((q / Cfg::kStages) - 1) & 1, kWaitNs))) {
+                // x tile: its slot is free once the y staged there kXS sub-chunks ago is stored
+                const int xs = q % kXS;
+                if (q >= kXS && !mbar_wait(smem_u32(&bars[kYSt0 + xs]), ((q / kXS) - 1) & 1, kWaitNs)) {
                     ok = false; set_error(err, 1); break;
                 }
-                const uint32_t xfull = smem_u32(&bars[kXFull0 + st]);
-                mbar_arrive_expect_tx(xfull, Cfg::kXBytes);
-                tma_load_4d(smem_u32(base + Cfg::kCBytes + Cfg::kBBytes), &tmX, xfull, pb * kPB, h, t0, b);
+                const uint32_t xfull = smem_u32(&bars[kXFull0 + xs]);
+                mbar_arrive_expect_tx(xfull, kAtom);
+                tma_load_4d(smem_u32(smem + Cfg::kX + xs * kAtom), &tmX, xfull, pb * kPB, h, t0, b);
             }
         }
         __syncwarp();
@@ -479,26 +489,22 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             constexpr uint32_t id_cb = idesc_bf16_f32(128, 128, 0, 0);
             constexpr uint32_t id_y = idesc_bf16_f32(128, kPB, 0, 1);
             constexpr uint32_t id_up = idesc_bf16_f32(128, kPB, 1, 1);
-            // Descriptors are built once; inside the loops they advance by compile-time byte
-            // offsets added to the start-address field (all addresses stay below 256 KB).
+            // Descriptors are built once; they advance by byte offsets added to the
+            // start-address field (all shared addresses stay below 256 KB).
             auto adv = [](uint64_t d, uint32_t bytes) -> uint64_t { return d + (uint64_t)(bytes >> 4); };
-            // per stage: C [i][s] K-major, B [j][s] K-major, B^T [s][t] MN-major, dt o x [t][p] MN-major
-            const uint32_t cb0 = smem_u32(smem), cb1 = smem_u32(smem + (1 % Cfg::kStages) * Cfg::kStage);
-            const uint64_t dC0 = smem_desc(cb0, 16, 1024), dC1 = smem_desc(cb1, 16, 1024);
-            const uint64_t dBk0 = smem_desc(cb0 + Cfg::kCBytes, 16, 1024), dBk1 = smem_desc(cb1 + Cfg::kCBytes, 16, 1024);
-            const uint64_t dBm0 = smem_desc(cb0 + Cfg::kCBytes, kAtom, 1024), dBm1 = smem_desc(cb1 + Cfg::kCBytes, kAtom, 1024);
-            const uint64_t dX0 = smem_desc(cb0 + Cfg::kCBytes + Cfg::kBBytes, kAtom, 1024);
-            const uint64_t dX1 = smem_desc(cb1 + Cfg::kCBytes + Cfg::kBBytes, kAtom, 1024);
-            const uint64_t dH = smem_desc(smem_u32(smem + Cfg::kH), kAtom, 1024);   // h bf16 [s][p], MN-major
-            const uint64_t dP = smem_desc(smem_u32(smem + Cfg::kP), 16, 1024);      // P [i][j], K-major
-            const uint64_t dXw = smem_desc(smem_u32(smem + Cfg::kXw), kAtom, 1024); // w o x [t][p], MN-major
+            const uint32_t s0 = smem_u32(smem);
+            const uint64_t dC0 = smem_desc(s0, 16, 1024);                          // C [i][s], K-major
+            const uint64_t dBk0 = smem_desc(s0 + Cfg::kCBytes, 16, 1024);          // B [j][s], K-major
+            const uint64_t dBm0 = smem_desc(s0 + Cfg::kCBytes, kAtom, 1024);       // B^T [s][t], MN-major
+            const uint64_t dX0 = smem_desc(s0 + Cfg::kX, kAtom, 1024);             // dt o x [t][p], MN-major
+            const uint64_t dH = smem_desc(s0 + Cfg::kH, kAtom, 1024);              // h bf16 [s][p], MN-major
+            const uint64_t dXw = smem_desc(s0 + Cfg::kXw, kAtom, 1024);            // w o x [t][p], MN-major
             auto issue_cb = [&](int q) {
-                const bool s1 = (q % Cfg::kStages) != 0;
-                const uint64_t c = s1 ? dC1 : dC0, bk = s1 ? dBk1 : dBk0;
+                const uint32_t so = (uint32_t)(q % kCBS) * Cfg::kCBStage;
 #pragma unroll
                 for (int kk = 0; kk < S / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                    mma_bf16(tmem + Cfg::kTcb, adv(c, off), adv(bk, off), id_cb, kk > 0 ? 1u : 0u);
+                    const uint32_t off = so + (kk >> 2) * kAtom + (kk & 3) * 32;
+                    mma_bf16(tmem + Cfg::kTcb, adv(dC0, off), adv(dBk0, off), id_cb, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&bars[kCb]));
             };
@@ -508,20 +514,21 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 tc_fence_after();
                 issue_cb(0);
                 for (int q = 0; q < nq; ++q) {
-                    const int st = q % Cfg::kStages;
-                    const bool s1 = st != 0;
-                    const uint64_t c = s1 ? dC1 : dC0, bm = s1 ? dBm1 : dBm0, xs = s1 ? dX1 : dX0;
-                    const uint32_t yb = (uint32_t)(q & 1) * Cfg::kTyStride;
-                    // Ys = C h^T (K = s): needs the state copy and a drained Ys/Yi buffer
+                    const int cs = q % kCBS, xs = q % kXS;
+                    const uint32_t so = (uint32_t)cs * Cfg::kCBStage;
+                    const uint32_t ys = Cfg::kTys + (uint32_t)(q % Cfg::kYsBufs) * kPB;
+                    const uint32_t yi = Cfg::kTyi + (uint32_t)(q & 1) * kPB;
+                    // Ys = C h^T (K = s): needs the state copy and a drained Ys buffer
                     if (!mbar_wait(smem_u32(&bars[kHReady]), q & 1, kWaitNs)) { ok = false; break; }
-                    if (q >= 2 && !mbar_wait(smem_u32(&bars[kEpi0 + (q & 1)]), ((q >> 1) - 1) & 1, kWaitNs)) {
-                        ok = false; break;
+                    if (q >= Cfg::kYsBufs) {
+                        const int e = q - Cfg::kYsBufs;
+                        if (!mbar_wait(smem_u32(&bars[kEpi0 + (e & 1)]), (e >> 1) & 1, kWaitNs)) { ok = false; break; }
                     }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < S / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                        mma_bf16(tmem + Cfg::kTys + yb, adv(c, off), adv(dH, kk * 2048), id_y, kk > 0 ? 1u : 0u);
+                        const uint32_t off = so + (kk >> 2) * kAtom + (kk & 3) * 32;
+                        mma_bf16(tmem + ys, adv(dC0, off), adv(dH, kk * 2048), id_y, kk > 0 ? 1u : 0u);
                     }
                     // state update h^T += B^T (w o X) (K = t) on the state pre-scaled by the state group
                     if (!mbar_wait(smem_u32(&bars[kXReady]), q & 1, kWaitNs)) { ok = false; break; }
@@ -531,28 +538,23 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                         for (int lb = 0; lb < S / 128; ++lb) {
 #pragma unroll
                             for (int kk = 0; kk < kQ / 16; ++kk)
-                                mma_bf16(tmem + Cfg::kTds + lb * kPB, adv(bm, lb * 2 * kAtom + kk * 2048),
+                                mma_bf16(tmem + Cfg::kTds + lb * kPB, adv(dBm0, so + lb * 2 * kAtom + kk * 2048),
                                          adv(dXw, kk * 2048), id_up, 1u);
                         }
                         mma_commit(smem_u32(&bars[kUpdate]));
                     }
-                    mma_commit(smem_u32(&bars[kFree0 + st]));     // CB, Ys and the update have read C and B
-                    // Yi = D x + P (dt o X) (K = j): the state group stored D x in the accumulator
+                    mma_commit(smem_u32(&bars[kFree0 + cs]));     // CB, Ys and the update have read C and B
+                    // Yi = D x + P (dt o X) (K = j), P from TMEM: the state group stored D x in the accumulator
                     if (!mbar_wait(smem_u32(&bars[kPReady]), q & 1, kWaitNs)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < kQ / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                        mma_bf16(tmem + Cfg::kTyi + yb, adv(dP, off), adv(xs, kk * 2048), id_y, 1u);
-                    }
+                    for (int kk = 0; kk < kQ / 16; ++kk)
+                        mma_bf16_ts(tmem + yi, tmem + Cfg::kTp + 8 * kk, adv(dX0, xs * kAtom + kk * 2048), id_y, 1u);
                     mma_commit(smem_u32(&bars[kIntra]));
-                    mma_commit(smem_u32(&bars[kXFree0 + st]));    // Yi has read the x tile
-                    // next CB as early as possible (the output group has read this one: P is ready)
+                    // next CB (the output group has read this one: P is built)
                     if (q + 1 < nq) {
-                        const int st1 = (q + 1) % Cfg::kStages;
-                        if (!mbar_wait(smem_u32(&bars[kFull0 + st1]), ((q + 1) / Cfg::kStages) & 1, kWaitNs)) {
-                            ok = false; break;
-                        }
+                        const int c1 = (q + 1) % kCBS;
+                        if (!mbar_wait(smem_u32(&bars[kFull0 + c1]), ((q + 1) / kCBS) & 1, kWaitNs)) { ok = false; break; }
                         tc_fence_after();
                         issue_cb(q + 1);
                     }
@@ -579,7 +581,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         };
         if (nq > 0) load_scalars(0);
         for (int q = 0; q < nq && ok; ++q) {
-            const int st = q % Cfg::kStages;
+            const int xs = q % kXS;
             const float gr = n_gr, dtr = n_dt, glast = n_glast, gbase = n_gbase;
             if (q + 1 < nq) load_scalars(q + 1);
 
@@ -639,15 +641,15 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             // x tile: dt o x in place (Yi operand), w o x into the Xw tile (state-update operand),
             // and D x into this sub-chunk's Yi accumulator (the Yi MMAs accumulate on top of it)
             {
-                if (!mbar_wait(smem_u32(&bars[kXFull0 + st]), (q / Cfg::kStages) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
+                if (!mbar_wait(smem_u32(&bars[kXFull0 + xs]), (q / kXS) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
                 // the Yi buffer of this sub-chunk is free once the epilogue of sub-chunk q - 2 read it
                 if (q >= 2 && !mbar_wait(smem_u32(&bars[kEpi0 + (q & 1)]), ((q >> 1) - 1) & 1, kWaitNs)) {
                     ok = false; set_error(err, 1); break;
                 }
                 tc_fence_after();
-                uint8_t *xt = smem + st * Cfg::kStage + Cfg::kCBytes + Cfg::kBBytes;
+                uint8_t *xt = smem + Cfg::kX + xs * kAtom;
                 const float wr = dtr * exp2f(glast - gr);
-                const uint32_t tyi = tmem + lane_base + Cfg::kTyi + (uint32_t)(q & 1) * Cfg::kTyStride;
+                const uint32_t tyi = tmem + lane_base + Cfg::kTyi + (uint32_t)(q & 1) * kPB;
 #pragma unroll
                 for (int cp = 0; cp < 4; ++cp) {
                     uint32_t dx[16];
@@ -703,8 +705,9 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         const int r = 32 * (warp & 3) + lane;          // TMEM lane = tile row i
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const int wrow_lo = 32 * (warp & 3), wrow_hi = wrow_lo + 31;   // rows of this warp
-        uint8_t *pa = smem + Cfg::kP + half * kAtom;   // P columns [64 half, 64 half + 64)
-        float *sF = sG + kQ;
+        const bool storer = warp == 6 && lane == 0;    // issues the bulk stores of y
+        // column arrays of the current sub-chunk
+        float *cG = sG, *cF = cG + kQ;
         // the 256 output-group threads run every iteration (work is skipped after an error),
         // so the named barrier below is always reached by all of them
         auto group_sync = [&]() { named_bar_sync(1, 256); };
@@ -718,26 +721,27 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         if (nq > 0) load_scalars(0);
         for (int q = 0; q < nq; ++q) {
             const int64_t t0 = t_begin + (int64_t)q * kQ;
+            const int xs = q % kXS;
             const float gr = n_gr, gend = n_gend, gbase = n_gbase;
-            const uint32_t yb = (uint32_t)(q & 1) * Cfg::kTyStride;
             if (half == 0) {
-                sG[r] = gr;
-                sF[r] = ex2_approx(gend - gr);          // 2^(G_blockend - G_j) <= 1 for A dt >= 0
+                cG[r] = gr;
+                cF[r] = ex2_approx(gend - gr);          // 2^(G_blockend - G_j) <= 1 for A dt >= 0
             }
             group_sync();
             if (q + 1 < nq) load_scalars(q + 1);
 
-            // P[i][j] = CB[i][j] 2^(G_i - G_j) for j <= i, else 0; bf16, K-major swizzled [i][j].
-            // Blocks of 16 columns entirely left of this warp's rows use the factored form
-            // 2^(G_i - G_e) 2^(G_e - G_j) (G_e = G at the block's last column; both factors
-            // <= 1); blocks that meet the diagonal evaluate 2^(G_i - G_j) per element.
+            // P[i][j] = CB[i][j] 2^(G_i - G_j) for j <= i, else 0, as bf16 pairs in TMEM (the
+            // A operand of Yi).  Blocks of 16 columns entirely left of this warp's rows use the
+            // factored form 2^(G_i - G_e) 2^(G_e - G_j) (G_e = G at the block's last column; both
+            // factors <= 1); blocks that meet the diagonal evaluate 2^(G_i - G_j) per element.
             if (ok && !mbar_wait(smem_u32(&bars[kCb]), q & 1, kWaitNs)) { ok = false; set_error(err, 1); }
             if (ok) {
                 tc_fence_after();
                 const int jh = 64 * half;
+                uint32_t pk[32];
                 if (jh > wrow_hi) {                     // whole half above the diagonal: zeros
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) *(uint4 *)(pa + sw128(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+                    for (int e = 0; e < 32; ++e) pk[e] = 0u;
                 } else {
                     uint32_t v[64];
                     const uint32_t ta = tmem + lane_base + Cfg::kTcb + jh;
@@ -754,44 +758,60 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
 #pragma unroll
                             for (int e = 0; e < 16; ++e) f[e] = 0.f;
                         } else if (j0 + 15 < wrow_lo) {           // left of every row of the warp: factored
-                            const float ei = ex2_approx(gr - sG[j0 + 15]);
+                            const float ei = ex2_approx(gr - cG[j0 + 15]);
+                            const float4 *f4 = reinterpret_cast<const float4 *>(cF + j0);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[16 * blk + e]) * ei * sF[j0 + e];
+                            for (int e4 = 0; e4 < 4; ++e4) {
+                                const float4 fj = f4[e4];
+                                f[4 * e4 + 0] = __uint_as_float(v[16 * blk + 4 * e4 + 0]) * ei * fj.x;
+                                f[4 * e4 + 1] = __uint_as_float(v[16 * blk + 4 * e4 + 1]) * ei * fj.y;
+                                f[4 * e4 + 2] = __uint_as_float(v[16 * blk + 4 * e4 + 2]) * ei * fj.z;
+                                f[4 * e4 + 3] = __uint_as_float(v[16 * blk + 4 * e4 + 3]) * ei * fj.w;
+                            }
                         } else {                                  // meets the diagonal: exact, selected
+                            const float4 *g4 = reinterpret_cast<const float4 *>(cG + j0);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int j = j0 + e;
-                                const float val = __uint_as_float(v[16 * blk + e]) * ex2_approx(gr - sG[j]);
-                                f[e] = (j <= r) ? val : 0.f;
+                            for (int e4 = 0; e4 < 4; ++e4) {
+                                const float4 gj = g4[e4];
+                                const float gjs[4] = {gj.x, gj.y, gj.z, gj.w};
+#pragma unroll
+                                for (int c = 0; c < 4; ++c) {
+                                    const int e = 4 * e4 + c, j = j0 + e;
+                                    const float val = __uint_as_float(v[16 * blk + e]) * ex2_approx(gr - gjs[c]);
+                                    f[e] = (j <= r) ? val : 0.f;
+                                }
                             }
                         }
-                        const int c = 2 * blk;
-                        *(uint4 *)(pa + sw128(r, c)) = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                                                  pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-                        *(uint4 *)(pa + sw128(r, c + 1)) =
-                            make_uint4(pack_bf16x2(f[8], f[9]), pack_bf16x2(f[10], f[11]),
-                                       pack_bf16x2(f[12], f[13]), pack_bf16x2(f[14], f[15]));
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) pk[8 * blk + e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
                     }
                 }
-                fence_proxy_async_smem();
+                const uint32_t tp = tmem + lane_base + Cfg::kTp + 32 * half;
+                tmem_st16(tp, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                tmem_st16(tp + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(smem_u32(&bars[kPReady]));
             }
             // y = 2^(G_i - G_base) Ys + Yi   (Yi already holds D x; this thread: 32 columns).
-            // y is staged in the x tile of this stage (its last reader, the Yi MMA, has completed)
+            // y is staged in this sub-chunk's x slot (its last reader, the Yi MMA, has completed)
             // in the same swizzled [t][p] layout, then written by one bulk tensor store.
-            uint8_t *ystage = smem + (q % Cfg::kStages) * Cfg::kStage + Cfg::kCBytes + Cfg::kBBytes;
+            uint8_t *ystage = smem + Cfg::kX + xs * kAtom;
             if (ok && !mbar_wait(smem_u32(&bars[kIntra]), q & 1, kWaitNs)) { ok = false; set_error(err, 1); }
             if (ok) {
                 tc_fence_after();
                 const float eg = ex2_approx(gr - gbase);
                 uint32_t vs[32], vi[32];
                 const uint32_t c0 = 32 * half;
-                tmem_ld16(tmem + lane_base + Cfg::kTys + yb + c0, *reinterpret_cast<uint32_t(*)[16]>(&vs[0]));
-                tmem_ld16(tmem + lane_base + Cfg::kTys + yb + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&vs[16]));
-                tmem_ld16(tmem + lane_base + Cfg::kTyi + yb + c0, *reinterpret_cast<uint32_t(*)[16]>(&vi[0]));
-                tmem_ld16(tmem + lane_base + Cfg::kTyi + yb + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&vi[16]));
+                const uint32_t ys = Cfg::kTys + (uint32_t)(q % Cfg::kYsBufs) * kPB + c0;
+                const uint32_t yi = Cfg::kTyi + (uint32_t)(q & 1) * kPB + c0;
+                tmem_ld16(tmem + lane_base + ys, *reinterpret_cast<uint32_t(*)[16]>(&vs[0]));
+                tmem_ld16(tmem + lane_base + ys + 16, *reinterpret_cast<uint32_t(*)[16]>(&vs[16]));
+                tmem_ld16(tmem + lane_base + yi, *reinterpret_cast<uint32_t(*)[16]>(&vi[0]));
+                tmem_ld16(tmem + lane_base + yi + 16, *reinterpret_cast<uint32_t(*)[16]>(&vi[16]));
                 tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars[kEpi0 + (q & 1)]));
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[4];
@@ -804,21 +824,24 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                     *(uint4 *)(ystage + sw128(r, 4 * half + c)) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
                 fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(smem_u32(&bars[kEpi0 + (q & 1)]));
             }
-            // all rows staged (and sG / sF free for the next sub-chunk)
+            // all rows staged (and the column arrays free for the next sub-chunk)
             group_sync();
-            if (warp == 6 && lane == 0) {
+            if (storer) {
+                // the store of sub-chunk q stays in flight; the slot of sub-chunk q - 1 is
+                // released once its store has read it
                 if (ok) {
                     tma_store_4d(&tmY, smem_u32(ystage), pb * kPB, h, (int)t0, b);
                     bulk_commit();
-                    bulk_wait_read();
                 }
-                mbar_arrive(smem_u32(&bars[kYSt0 + (q % Cfg::kStages)]));
+                bulk_wait_read_1();
+                if (q > 0) mbar_arrive(smem_u32(&bars[kYSt0 + (q - 1) % kXS]));
             }
         }
-        if (warp == 6 && lane == 0) bulk_wait_all();
+        if (storer) {
+            bulk_wait_all();
+            if (nq > 0) mbar_arrive(smem_u32(&bars[kYSt0 + (nq - 1) % kXS]));
+        }
     }
     tc_fence_before();
     __syncthreads();
