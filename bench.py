@@ -55,29 +55,38 @@ def esize(dtype: str) -> int:
     return 2 if dtype == "bf16" else 4
 
 
-def stage_bytes(s: workloads.Shape):
-    """Algorithmic bytes per launch of each stage: its own compulsory inputs read
-    once and outputs written once (intermediates G, s_local, h_start count as that
-    stage's inputs/outputs), and the whole-step compulsory I/O."""
+def stage_bytes(s: workloads.Shape, plan: dict):
+    """Algorithmic bytes per launch of each stage as the library runs it (``plan`` is
+    ssd_fwd_plan): its own compulsory inputs read once and outputs written once, with
+    the intermediates (G, the super-chunk states, the super-chunk-start states, all
+    float32) counted as that stage's inputs/outputs; 0 for a stage that does not launch.
+    Also the whole-step compulsory I/O ("step")."""
     e = esize(s.dtype)
-    Bsz, L, nh, H, S, G, nc = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups, s.nchunks
+    Bsz, L, nh, H, S, G, T, nc = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups, s.chunk, s.nchunks
     x = Bsz * L * nh * H * e
     dt = Bsz * L * nh * e
     bc = Bsz * L * G * S * e
     g = Bsz * nh * L * 4
-    states32 = Bsz * nh * nc * H * S * 4
-    states_in = Bsz * nh * nc * H * S * e
-    h = Bsz * nh * H * S * 4
-    h0 = h if s.h0_recipe != "none" else 0
+    state = Bsz * nh * H * S * 4                       # one float32 state per (batch, head)
+    h0 = state if s.h0_recipe != "none" else 0
     y = Bsz * L * nh * H * e
     ad = 2 * nh * 4
-    return {
-        "chunk_cumsum": dt + nh * 4 + g,
-        "chunk_state": x + dt + bc + g + states32,
-        "state_passing": states32 + (Bsz * nh * nc * 4) + h0 + states_in + h,
-        "chunk_scan": x + dt + 2 * bc + g + states_in + nh * 4 + y,
-        "step": x + dt + 2 * bc + ad + h0 + y + h,
+    R, nsup = plan["chunks_per_super"], plan["n_super"]
+    # super-chunks whose state chunk_state produces: all but the last on the tensor-core
+    # path (the scan carries the last one itself), every chunk on the CUDA-core path
+    nm = nsup - 1 if plan["tensor_cores"] else nc
+    frac = min(nm * R * T, L) / L if L else 0.0       # share of the sequence chunk_state reads
+    out = {
+        "chunk_cumsum": dt + nh * 4 + g + (g if plan["tensor_cores"] else 0),   # + the float32 copy of dt
+        "chunk_state": (frac * (x + dt + bc + g) + nm * state) if nm else 0,
+        "state_passing": (nm * state + Bsz * nh * nc * 4 + h0 + nm * state) if nm else 0,
+        "chunk_scan": x + dt + 2 * bc + g + h0 + (nsup - 1) * state + nh * 4 + y + state,
+        "step": x + dt + 2 * bc + ad + h0 + y + state,
     }
+    if not plan["tensor_cores"]:
+        out["state_passing"] += state                  # the CUDA-core path writes h_final there
+        out["chunk_scan"] -= state
+    return out
 
 
 def alg_flops(s: workloads.Shape) -> float:
@@ -269,6 +278,7 @@ def main():
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.tensors().items()}
     desc = api.desc_for(d["x"], d["B"], shape.chunk)
     tc = api.uses_tensor_cores(desc)
+    plan = api.fwd_plan(desc)
     ws = api.alloc_workspace(desc, dev)
     y = torch.empty_like(d["x"])
     hf = torch.empty((shape.batch, shape.nheads, shape.headdim, shape.dstate), dtype=torch.float32, device=dev)
@@ -343,8 +353,8 @@ def main():
         return
 
     peaks, peak_kind = load_peaks()
-    sb = stage_bytes(shape)
-    top = max(STAGES, key=lambda s_: stage_ms[s_])
+    sb = stage_bytes(shape, plan)
+    top = max(STAGES, key=lambda s_: stage_ms[s_] if sb[s_] else -1.0)
     achieved = sb[top] / (stage_ms[top] * 1e-3) / 1e9
     # a kernel timed inside a long step: burst copy bandwidth is the only HBM figure measured
     peak = float(peaks["hbm_gbs"])
@@ -363,11 +373,12 @@ def main():
         "step_roofline": {"alg_bytes": sb["step"], "alg_flops": flops,
                           "roofline_ms": max(sb["step"] / (peak * 1e9), flops / (float(peaks["bf16_tflops"]) * 1e12)) * 1e3,
                           "frac": max(sb["step"] / (peak * 1e9), flops / (float(peaks["bf16_tflops"]) * 1e12)) * 1e3 / ms_per_step},
-        "stages_ms": stage_ms,
-        "stages_gbs": {s_: sb[s_] / (stage_ms[s_] * 1e-3) / 1e9 for s_ in STAGES},
+        "plan": plan,
+        "stages_ms": {s_: (stage_ms[s_] if sb[s_] else None) for s_ in STAGES},
+        "stages_gbs": {s_: (sb[s_] / (stage_ms[s_] * 1e-3) / 1e9 if sb[s_] else None) for s_ in STAGES},
         "e2e": {"value": world * shape.tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": plan["kernel_launches"] * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

@@ -15,7 +15,8 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
           4: "SSD_ERR_CUDA", 5: "SSD_ERR_TOO_LARGE", 6: "SSD_ERR_TIMEOUT"}
 
 # Every symbol include/ssd.h declares.
-EXPORTS = ("ssd_status_string", "ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd", "ssd_fwd_timed", "ssd_fwd_check",
+EXPORTS = ("ssd_status_string", "ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd_plan", "ssd_fwd", "ssd_fwd_timed",
+           "ssd_fwd_check",
            "ssd_step",
            "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_fwd_noalloc")
 
@@ -25,6 +26,11 @@ class Desc(ctypes.Structure):
                 ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
                 ("chunk", ctypes.c_int64), ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
                 ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("tensor_cores", ctypes.c_int32), ("chunks_per_super", ctypes.c_int32), ("n_super", ctypes.c_int32),
+                ("kernel_launches", ctypes.c_int32), ("memsets", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 class SSDError(RuntimeError):
@@ -54,6 +60,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ssd_fwd_workspace_size.restype = st
         lib.ssd_fwd_path.argtypes = [DP, ctypes.POINTER(ctypes.c_int32)]
         lib.ssd_fwd_path.restype = st
+        lib.ssd_fwd_plan.argtypes = [DP, ctypes.POINTER(Plan)]
+        lib.ssd_fwd_plan.restype = st
         lib.ssd_fwd.argtypes = [DP] + [P] * 10 + [ctypes.c_size_t, P]
         lib.ssd_fwd.restype = st
         lib.ssd_fwd_timed.argtypes = [DP] + [P] * 10 + [ctypes.c_size_t, P, ctypes.POINTER(P)]

@@ -72,6 +72,15 @@ def uses_tensor_cores(desc: Desc) -> bool:
     return bool(v.value)
 
 
+def fwd_plan(desc: Desc) -> dict:
+    """How ssd_fwd runs ``desc`` on the current device (ssd_fwd_plan): path, chunks per
+    super-chunk, super-chunks per sequence, kernel launches and memsets per call."""
+    p = _native.Plan()
+    check("ssd_fwd_plan", _native.load().ssd_fwd_plan(ctypes.byref(desc), ctypes.byref(p)))
+    return {"tensor_cores": bool(p.tensor_cores), "chunks_per_super": int(p.chunks_per_super),
+            "n_super": int(p.n_super), "kernel_launches": int(p.kernel_launches), "memsets": int(p.memsets)}
+
+
 def alloc_workspace(desc: Desc, device) -> torch.Tensor:
     n = workspace_size(desc)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)

@@ -250,6 +250,37 @@ ssd_status ssd_fwd_path(const ssd_desc *desc, int32_t *uses_tensor_cores)
     return SSD_OK;
 }
 
+ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan)
+{
+    Problem pr;
+    if (!plan) return SSD_ERR_INVALID_ARG;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    ssd_plan p = {};
+    p.tensor_cores = use_tensor_cores(desc, pr) ? 1 : 0;
+    if (pr.B == 0 || pr.nh == 0 || pr.L == 0) {
+        // nothing to scan: at most one copy or memset of h_final, issued only if h_final is given
+        p.chunks_per_super = 1;
+        *plan = p;
+        return SSD_OK;
+    }
+    if (p.tensor_cores) {
+        const int R = choose_chunks_per_super(pr);
+        const int nsup = (int)((pr.nc + R - 1) / R);
+        p.chunks_per_super = R;
+        p.n_super = nsup;
+        p.kernel_launches = nsup > 1 ? 4 : 2;
+        p.memsets = 1 + ((nsup > 1 && ssd::chunk_state_tc_memsets(pr, R, nsup - 1)) ? 1 : 0);
+    } else {
+        p.chunks_per_super = 1;
+        p.n_super = (int32_t)pr.nc;
+        p.kernel_launches = 4;
+        p.memsets = 1;
+    }
+    *plan = p;
+    return SSD_OK;
+}
+
 ssd_status ssd_fwd(const ssd_desc *desc, const void *x, const void *dt, const float *A,
                    const void *Bm, const void *Cm, const float *D, const float *h0, void *y,
                    float *h_final, void *workspace, size_t ws_bytes, ssd_stream_t stream)

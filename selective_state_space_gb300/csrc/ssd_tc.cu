@@ -878,6 +878,15 @@ bool make_map_4d(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, ui
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Whether cutting `total` stages into `grid` equal slices puts a cut inside a unit of
+// `nq_u` stages.
+bool slices_split_units(int64_t total, int64_t grid, int64_t nq_u)
+{
+    for (int64_t c = 1; c < grid; ++c)
+        if ((total * c / grid) % nq_u != 0) return true;
+    return false;
+}
+
 int current_sms()
 {
     int dev = 0, sms = 0;
@@ -906,9 +915,7 @@ cudaError_t state_launch(const Problem &pr, const void *x, const void *dt, const
     const int64_t sms = current_sms();
     const int64_t grid = total < sms ? total : sms;
     // a slice boundary inside a unit: both parts add into a zeroed s_out
-    bool split = false;
-    for (int64_t c = 1; c < grid && !split; ++c) split = (total * c / grid) % nq_u != 0;
-    if (split) {
+    if (slices_split_units(total, grid, nq_u)) {
         e = cudaMemsetAsync(s_out, 0, (size_t)(pr.B * pr.nh * nsup) * (size_t)(pr.H * pr.S) * sizeof(float), st);
         if (e != cudaSuccess) return e;
     }
@@ -949,19 +956,36 @@ bool tc_supported(const Problem &pr)
     return true;
 }
 
+// Heads per chunk_state CTA: as many heads of one group as fit N = HG * H <= 256 (S = 128).
+int state_heads_per_cta(const Problem &pr)
+{
+    const int hpg = (int)pr.hpg;
+    if (pr.S == 128 && pr.H == 64) return hpg % 4 == 0 ? 4 : (hpg % 2 == 0 ? 2 : 1);
+    if (pr.S == 128 && pr.H == 128) return hpg % 2 == 0 ? 2 : 1;
+    return 1;
+}
+
+bool chunk_state_tc_memsets(const Problem &pr, int R, int nm)
+{
+    const int64_t nq_u = (int64_t)R * (pr.T / 64);
+    const int64_t total = pr.B * (int64_t)nm * (pr.nh / state_heads_per_cta(pr)) * nq_u;
+    if (total == 0) return false;
+    const int64_t sms = current_sms();
+    return slices_split_units(total, total < sms ? total : sms, nq_u);
+}
+
 cudaError_t launch_chunk_state_tc(const Problem &pr, const void *x, const void *dt, const float *dtT, const void *Bm,
                                   const float *G, float *s_out, int R, int nsup, int nm, int *err, cudaStream_t st)
 {
     if (R < 1 || R > 256) return cudaErrorInvalidValue;
-    // heads per CTA: as many heads of one group as fit N = HG * H <= 256 (S = 128)
-    const int hpg = (int)pr.hpg;
+    const int hg = state_heads_per_cta(pr);
     if (pr.S == 128 && pr.H == 64) {
-        if (hpg % 4 == 0) return state_launch<128, 64, 4>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
-        if (hpg % 2 == 0) return state_launch<128, 64, 2>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+        if (hg == 4) return state_launch<128, 64, 4>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+        if (hg == 2) return state_launch<128, 64, 2>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
         return state_launch<128, 64, 1>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
     }
     if (pr.S == 128 && pr.H == 128) {
-        if (hpg % 2 == 0) return state_launch<128, 128, 2>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+        if (hg == 2) return state_launch<128, 128, 2>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
         return state_launch<128, 128, 1>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
     }
     if (pr.S == 256 && pr.H == 64) return state_launch<256, 64, 1>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);

@@ -13,6 +13,9 @@ bool tc_supported(const Problem &pr);
 // s_local[b][h][m] with a super-chunk extent of nsup.  dtT (nullable) is dt as float32
 // in the [b][h][L] layout of G; with it, dt and G reach the kernel by bulk copies
 // instead of per-thread loads.  `err` receives error bits.
+// Whether launch_chunk_state_tc with these arguments zeroes s_local first (one
+// cudaMemsetAsync): it does when a CTA's slice of stages cuts a super-chunk.
+bool chunk_state_tc_memsets(const Problem &pr, int R, int nm);
 cudaError_t launch_chunk_state_tc(const Problem &pr, const void *x, const void *dt, const float *dtT,
                                   const void *Bm, const float *G, float *s_local, int R, int nsup, int nm,
                                   int *err, cudaStream_t st);

@@ -129,6 +129,28 @@ def test_step_and_stage_validation(lib):
     assert lib.ssd_fwd_path(ctypes.byref(d), None) == 1
 
 
+def test_fwd_plan_is_consistent(lib):
+    """ssd_fwd_plan: host-side query; the plan must be self-consistent for every path."""
+    P = _native.Plan
+    # bf16 layer shape on the tensor-core path: nc = 16 chunks
+    d = desc(batch=4, seqlen=4096, nheads=80, headdim=64, dstate=128, ngroups=1, chunk=256,
+             in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16)
+    p = P()
+    assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0
+    assert p.tensor_cores == 1
+    nc = 16
+    assert 1 <= p.chunks_per_super <= nc and p.n_super == -(-nc // p.chunks_per_super)
+    assert p.kernel_launches == (4 if p.n_super > 1 else 2) and p.memsets in (1, 2)
+    # forced CUDA-core path: one chunk per super-chunk, four stages
+    d.flags = 1
+    assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0
+    assert (p.tensor_cores, p.chunks_per_super, p.n_super, p.kernel_launches, p.memsets) == (0, 1, nc, 4, 1)
+    # empty sequence: nothing launched
+    d = desc(seqlen=0)
+    assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0 and p.kernel_launches == 0
+    assert lib.ssd_fwd_plan(ctypes.byref(d), None) == 1
+
+
 def test_timed_variant_requires_events(lib):
     d = desc()
     a = 1 << 20
