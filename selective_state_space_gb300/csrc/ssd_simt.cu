@@ -23,59 +23,70 @@ namespace {
 // One block per (chunk, 32-head tile, batch).  Lane = head, so every dt row of 32
 // heads is one coalesced load.  Warp w takes runs of 32 consecutive tokens: each lane
 // loads its run (independent loads), forms the running sum in registers, and records
-// the run total; after one barrier every run adds the totals of the runs before it.
-// G is staged as [token][head] and written transposed, [head][token], coalesced.
+// the run total; after one barrier, one thread per (run, head) sums the totals of the
+// runs before it into an offset table, and after a second barrier G is written
+// transposed, [head][token], coalesced, with the offset of its run added on the way out.
 // ---------------------------------------------------------------------------
 template <typename Tin>
 __global__ void __launch_bounds__(256)
 k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *__restrict__ G,
                float *__restrict__ dtT, int64_t L, int nh, int T)
 {
-    extern __shared__ float tile[];   // [T][33] G, then (dtT only) [T][33] dt
-    __shared__ float run_sum[32][33]; // [run][head]
+    extern __shared__ float tile[];   // [T][33] in-run cumsum, then (dtT only) [T][33] dt
+    __shared__ float run_sum[32][33]; // [run][head] run totals (T <= 1024: at most 32 runs)
+    __shared__ float run_off[32][33]; // [run][head] sum of the totals of the runs before
     const int k = blockIdx.x, hbase = blockIdx.y * 32, b = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t0 = (int64_t)k * T;
     const int n = (int)((int64_t)T < L - t0 ? (int64_t)T : L - t0);
     const int runs = (n + 31) / 32;
     const int h = hbase + lane;
-    const float a = (h < nh) ? A[h] : 0.f;
+    // lanes past the last head load head 0 (a valid address) with a = 0; their rows are never written out
+    const float a = h < nh ? __ldg(A + h) : 0.f;
     for (int r = warp; r < runs; r += 8) {
         float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int t = 32 * r + i;       // zero padding past the end of the chunk
-            v[i] = (t < n && h < nh) ? to_f32(dt[((int64_t)b * L + t0 + t) * nh + h]) : 0.f;
-        }
+        const Tin *src = dt + ((int64_t)b * L + t0 + 32 * r) * nh + (h < nh ? h : 0);
+        float *trow = tile + (32 * r) * 33 + lane;
         float acc = 0.f;
+        if (32 * r + 32 <= n) {                // whole run inside the chunk: no per-token checks
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            acc += a * v[i];
-            if (32 * r + i < n) tile[(32 * r + i) * 33 + lane] = acc;
-        }
-        if (dtT) {
+            for (int i = 0; i < 32; ++i) v[i] = to_f32(__ldg(src + (int64_t)i * nh));
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (32 * r + i < n) tile[(T + 32 * r + i) * 33 + lane] = v[i];
+            for (int i = 0; i < 32; ++i) {
+                acc += a * v[i];
+                trow[i * 33] = acc;
+            }
+            if (dtT) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) trow[(T + i) * 33] = v[i];
+            }
+        } else {                               // the chunk ends inside this run
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = (32 * r + i < n) ? to_f32(__ldg(src + (int64_t)i * nh)) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                acc += a * v[i];
+                if (32 * r + i < n) {
+                    trow[i * 33] = acc;
+                    if (dtT) trow[(T + i) * 33] = v[i];
+                }
+            }
         }
         run_sum[r][lane] = acc;
     }
     __syncthreads();
-    for (int r = warp; r < runs; r += 8) {
+    for (int idx = threadIdx.x; idx < 32 * runs; idx += blockDim.x) {
+        const int r = idx >> 5, j = idx & 31;
         float off = 0.f;
-        for (int rr = 0; rr < r; ++rr) off += run_sum[rr][lane];
-        if (r > 0) {
-#pragma unroll 8
-            for (int i = 0; i < 32; ++i)
-                if (32 * r + i < n) tile[(32 * r + i) * 33 + lane] += off;
-        }
+        for (int rr = 0; rr < r; ++rr) off += run_sum[rr][j];
+        run_off[r][j] = off;
     }
     __syncthreads();
     for (int j = warp; j < 32; j += 8) {
         const int hh = hbase + j;
         if (hh >= nh) continue;
         float *dst = G + ((int64_t)b * nh + hh) * L + t0;
-        for (int t = lane; t < n; t += 32) dst[t] = tile[t * 33 + j] * kLog2e;
+        for (int t = lane; t < n; t += 32) dst[t] = (tile[t * 33 + j] + run_off[t >> 5][j]) * kLog2e;
         if (dtT) {
             float *dd = dtT + ((int64_t)b * nh + hh) * L + t0;
             for (int t = lane; t < n; t += 32) dd[t] = tile[(T + t) * 33 + j];
