@@ -36,9 +36,10 @@ METRIC = "ssd_fwd_tokens_per_s"
 UNIT = "tokens/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")
-KERNEL_SOURCES = {  # the file that holds each stage's kernels (for the traffic record's freshness check)
+KERNEL_SOURCES = {  # the file that holds each stage's kernels (for the traffic record's freshness check);
+    # the traffic records are of the tensor-core path, whose chunk_state / chunk_scan live in ssd_tc.cu
     "chunk_cumsum": ["ssd_simt.cu"], "state_passing": ["ssd_simt.cu"],
-    "chunk_state": ["ssd_simt.cu", "ssd_tc.cu"], "chunk_scan": ["ssd_simt.cu", "ssd_tc.cu"],
+    "chunk_state": ["ssd_tc.cu", "sm100_ptx.cuh"], "chunk_scan": ["ssd_tc.cu", "sm100_ptx.cuh"],
 }
 
 
