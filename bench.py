@@ -17,6 +17,7 @@ bounded sample of the same workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -263,6 +264,85 @@ def config_of(shape):
             "input_dtype": shape.dtype, "state_dtype": "f32", "l2": l2}
 
 
+DECODE_METRIC = "ssd_step_tokens_per_s"
+
+
+def parse_decode(name: str):
+    """decode-<layer workload>-b<batch>: single-token decode steps of that layer's heads at that batch."""
+    if not name.startswith("decode-") or "-b" not in name:
+        return None
+    layer, batch = name[len("decode-"):].rsplit("-b", 1)
+    base = workloads.by_name(layer)
+    return dataclasses.replace(base, name=name, batch=int(batch), seqlen=1, chunk=1, h0_recipe="normal",
+                               dt_zero_frac=0.0)
+
+
+def run_decode(args, shape):
+    """ssd_step throughput: each step reads and writes the float32 state once (HBM-bound)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from selective_state_space_gb300 import api
+    from selective_state_space_gb300.build import build
+    build()
+    inp = workloads.make_inputs(shape)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.tensors().items()}
+    x, dt, Bm, Cm = d["x"][:, 0], d["dt"][:, 0], d["B"][:, 0], d["C"][:, 0]
+    h = d["h0"].clone()
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        api.ssd_step(x, dt, d["A"], Bm, Cm, d["D"], h, y=y, stream=stream)
+
+    e = esize(shape.dtype)
+    state = shape.batch * shape.nheads * shape.headdim * shape.dstate * 4
+    alg = (2 * state + 2 * shape.batch * shape.nheads * shape.headdim * e + shape.batch * shape.nheads * e
+           + 2 * shape.batch * shape.ngroups * shape.dstate * e + 2 * shape.nheads * 4)
+    flush = alg < 2 * L2_BYTES
+    scrub = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev) if flush else None
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        if not flush:
+            start.record(stream)
+            for _ in range(args.steps):
+                step()
+            end.record(stream)
+            torch.cuda.synchronize()
+            ms = start.elapsed_time(end)
+        else:
+            ms = 0.0
+            for i in range(args.steps):
+                scrub.fill_(i & 0xff)
+                start.record(stream)
+                step()
+                end.record(stream)
+                torch.cuda.synchronize()
+                ms += start.elapsed_time(end)
+    ms_per_step = ms / args.steps
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["hbm_gbs"])
+    achieved = alg / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": DECODE_METRIC, "value": shape.batch / (ms_per_step * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (state), " + shape.dtype + " (x, B, C)",
+        "data": "synthetic",
+        "config": {"workload": shape.name, "batch": shape.batch, "nheads": shape.nheads, "headdim": shape.headdim,
+                   "dstate": shape.dstate, "ngroups": shape.ngroups, "input_dtype": shape.dtype,
+                   "l2": ("flushed between steps: each step timed alone after writing a 512 MB buffer" if flush
+                          else "no flush: the state read and written per step exceeds twice the 129 MB L2")},
+        "roofline": {"kernel": "ssd_step", "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs", "alg_bytes_per_launch": alg,
+                     "traffic": None},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -275,6 +355,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    dshape = parse_decode(args.workload)
+    if dshape is not None:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the decode workloads time ssd_step only"}))
+            return
+        run_decode(args, dshape)
+        return
     shape = workloads.by_name(args.workload)
     if args.impl == "reference":
         run_reference(args, shape)

@@ -361,14 +361,84 @@ k_chunk_scan_simt(const Tin *__restrict__ x, const Tin *__restrict__ dt,
 
 // ---------------------------------------------------------------------------
 // Decode step (blog section "Mamba-2 architecture", the recurrent form).
-// One warp per state row (b, h, p): h[p][s] = exp(A dt) h[p][s] + dt x[p] B[s],
-// y[p] = sum_s C[s] h[p][s] + D x[p].  Rows are contiguous in s: coalesced.
+// h[p][s] = exp(A dt) h[p][s] + dt x[p] B[s],  y[p] = sum_s C[s] h[p][s] + D x[p].
+// The state is read and written once: the kernel is bound by HBM.  One block per
+// (batch, head); warp w takes rows p = w, w + 8, ...; each lane holds a run of S/32
+// consecutive s, so a row is one 16-byte access per lane per 128 floats, and B, C are
+// loaded once per block.  Rows are processed kRows at a time with every state load
+// issued before the first use, to keep enough bytes in flight.
 // ---------------------------------------------------------------------------
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, int SV>   // SV: float4 per lane per row (S = 128 SV)
 __global__ void __launch_bounds__(256)
 k_ssd_step(const Tin *__restrict__ x, const Tin *__restrict__ dt, const float *__restrict__ A,
            const Tin *__restrict__ Bm, const Tin *__restrict__ Cm, const float *__restrict__ D,
            float *__restrict__ hst, Tout *__restrict__ y, Problem pr)
+{
+    constexpr int kRows = 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int hh = blockIdx.x, b = blockIdx.y;
+    const int g = (int)(hh / pr.hpg);
+    const int64_t bh = (int64_t)b * pr.nh + hh;
+    const float dtv = to_f32(dt[bh]);
+    const float alpha = exp2f(A[hh] * dtv * kLog2e);
+    const float dh = D[hh];
+    const Tin *Bv = Bm + ((int64_t)b * pr.G + g) * pr.S;
+    const Tin *Cv = Cm + ((int64_t)b * pr.G + g) * pr.S;
+    float bv[4 * SV], cv[4 * SV];
+#pragma unroll
+    for (int k = 0; k < SV; ++k)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int s = 128 * k + 4 * lane + e;
+            bv[4 * k + e] = to_f32(Bv[s]);
+            cv[4 * k + e] = to_f32(Cv[s]);
+        }
+    float4 *hrow = reinterpret_cast<float4 *>(hst + bh * pr.H * pr.S);
+    const int rows_per_warp = (int)((pr.H + 7) / 8);
+    for (int r0 = 0; r0 < rows_per_warp; r0 += kRows) {
+        float4 hv[kRows][SV];
+        float xp[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const int p = warp + 8 * (r0 + i);
+            const bool valid = r0 + i < rows_per_warp && p < pr.H;
+            xp[i] = valid ? to_f32(x[bh * pr.H + p]) : 0.f;
+#pragma unroll
+            for (int k = 0; k < SV; ++k)
+                hv[i][k] = valid ? hrow[(int64_t)p * (pr.S / 4) + 32 * k + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const int p = warp + 8 * (r0 + i);
+            const bool valid = r0 + i < rows_per_warp && p < pr.H;
+            const float u = dtv * xp[i];
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < SV; ++k) {
+                float4 v = hv[i][k];
+                v.x = fmaf(alpha, v.x, u * bv[4 * k + 0]);
+                v.y = fmaf(alpha, v.y, u * bv[4 * k + 1]);
+                v.z = fmaf(alpha, v.z, u * bv[4 * k + 2]);
+                v.w = fmaf(alpha, v.w, u * bv[4 * k + 3]);
+                if (valid) hrow[(int64_t)p * (pr.S / 4) + 32 * k + lane] = v;
+                acc = fmaf(cv[4 * k + 0], v.x, acc);
+                acc = fmaf(cv[4 * k + 1], v.y, acc);
+                acc = fmaf(cv[4 * k + 2], v.z, acc);
+                acc = fmaf(cv[4 * k + 3], v.w, acc);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (valid && lane == 0) y[bh * pr.H + p] = from_f32<Tout>(fmaf(dh, xp[i], acc));
+        }
+    }
+}
+
+// Any S: one warp per state row (b, h, p), lanes striding over s.
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(256)
+k_ssd_step_any(const Tin *__restrict__ x, const Tin *__restrict__ dt, const float *__restrict__ A,
+               const Tin *__restrict__ Bm, const Tin *__restrict__ Cm, const float *__restrict__ D,
+               float *__restrict__ hst, Tout *__restrict__ y, Problem pr)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t p = (int64_t)blockIdx.x * 8 + warp;
@@ -484,9 +554,21 @@ static cudaError_t step_launch(const Problem &pr, const void *x, const void *dt,
                                const void *Bm, const void *Cm, const float *D, float *h, void *y,
                                cudaStream_t st)
 {
+    // S a multiple of 128 (and h 16-byte aligned): the vectorised kernel; any other S: one warp per row
+    if (pr.S % 128 == 0 && pr.S <= 512 && (reinterpret_cast<uintptr_t>(h) & 15) == 0 && pr.nh <= 65535 && pr.B <= 65535) {
+        dim3 grid((unsigned)pr.nh, (unsigned)pr.B);
+        const Tin *xi = (const Tin *)x, *di = (const Tin *)dt, *bi = (const Tin *)Bm, *ci = (const Tin *)Cm;
+        switch (pr.S / 128) {
+            case 1: k_ssd_step<Tin, Tout, 1><<<grid, 256, 0, st>>>(xi, di, A, bi, ci, D, h, (Tout *)y, pr); break;
+            case 2: k_ssd_step<Tin, Tout, 2><<<grid, 256, 0, st>>>(xi, di, A, bi, ci, D, h, (Tout *)y, pr); break;
+            case 3: k_ssd_step<Tin, Tout, 3><<<grid, 256, 0, st>>>(xi, di, A, bi, ci, D, h, (Tout *)y, pr); break;
+            default: k_ssd_step<Tin, Tout, 4><<<grid, 256, 0, st>>>(xi, di, A, bi, ci, D, h, (Tout *)y, pr); break;
+        }
+        return cudaGetLastError();
+    }
     dim3 grid((unsigned)((pr.H + 7) / 8), (unsigned)pr.nh, (unsigned)pr.B);
-    k_ssd_step<Tin, Tout><<<grid, 256, 0, st>>>((const Tin *)x, (const Tin *)dt, A, (const Tin *)Bm,
-                                                (const Tin *)Cm, D, h, (Tout *)y, pr);
+    k_ssd_step_any<Tin, Tout><<<grid, 256, 0, st>>>((const Tin *)x, (const Tin *)dt, A, (const Tin *)Bm,
+                                                    (const Tin *)Cm, D, h, (Tout *)y, pr);
     return cudaGetLastError();
 }
 
