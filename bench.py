@@ -62,7 +62,9 @@ def stage_bytes(s: workloads.Shape, plan: dict):
     ssd_fwd_plan): its own compulsory inputs read once and outputs written once, with
     the intermediates (G, the super-chunk states, the super-chunk-start states, all
     float32) counted as that stage's inputs/outputs; 0 for a stage that does not launch.
-    Also the whole-step compulsory I/O ("step")."""
+    A plan cuts the sequences ((batch, head) pairs) in two parts; chunk_state and
+    state_passing run per part and their bytes are summed.  Also the whole-step
+    compulsory I/O ("step")."""
     e = esize(s.dtype)
     Bsz, L, nh, H, S, G, T, nc = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups, s.chunk, s.nchunks
     x = Bsz * L * nh * H * e
@@ -70,24 +72,42 @@ def stage_bytes(s: workloads.Shape, plan: dict):
     bc = Bsz * L * G * S * e
     g = Bsz * nh * L * 4
     state = Bsz * nh * H * S * 4                       # one float32 state per (batch, head)
+    hs = H * S * 4                                     # one float32 state of one sequence
     h0 = state if s.h0_recipe != "none" else 0
     y = Bsz * L * nh * H * e
     ad = 2 * nh * 4
-    R, nsup = plan["chunks_per_super"], plan["n_super"]
-    # super-chunks whose state chunk_state produces: all but the last on the tensor-core
-    # path (the scan carries the last one itself), every chunk on the CUDA-core path
-    nm = nsup - 1 if plan["tensor_cores"] else nc
-    frac = min(nm * R * T, L) / L if L else 0.0       # share of the sequence chunk_state reads
+    nseq, hpg = Bsz * nh, nh // G
+    if plan["tensor_cores"]:
+        split = plan["split_sequences"]
+        parts = [(0, split, plan["chunks_per_super"], plan["n_super"]),
+                 (split, nseq - split, plan["tail_chunks_per_super"], plan["tail_n_super"])]
+    else:
+        parts = [(0, nseq, 1, nc)]
+    cs = sp = carried = 0.0
+    for lo, n, R, nsup in parts:
+        if n == 0:
+            continue
+        # super-chunks whose state chunk_state produces: all but the last on the tensor-core
+        # path (the scan carries the last one itself), every chunk on the CUDA-core path
+        nm = nsup - 1 if plan["tensor_cores"] else nc
+        carried += n * (nsup - 1) * hs if plan["tensor_cores"] else 0
+        if nm == 0:
+            continue
+        frac = min(nm * R * T, L) / L                  # share of each sequence chunk_state reads
+        pairs = len({(bh // nh, (bh % nh) // hpg) for bh in range(lo, lo + n)})   # (batch, group) pairs read
+        per_seq = L * (H * e + e + 4)                  # x, dt and G of one sequence
+        cs += frac * (n * per_seq + pairs * L * S * e) + n * nm * hs
+        sp += 2 * n * nm * hs + n * nc * 4 + (n * hs if h0 else 0)
     out = {
         "chunk_cumsum": dt + nh * 4 + g + (g if plan["tensor_cores"] else 0),   # + the float32 copy of dt
-        "chunk_state": (frac * (x + dt + bc + g) + nm * state) if nm else 0,
-        "state_passing": (nm * state + Bsz * nh * nc * 4 + h0 + nm * state) if nm else 0,
-        "chunk_scan": x + dt + 2 * bc + g + h0 + (nsup - 1) * state + nh * 4 + y + state,
+        "chunk_state": cs,
+        "state_passing": sp,
+        "chunk_scan": x + dt + 2 * bc + g + h0 + carried + nh * 4 + y + state,
         "step": x + dt + 2 * bc + ad + h0 + y + state,
     }
     if not plan["tensor_cores"]:
         out["state_passing"] += state                  # the CUDA-core path writes h_final there
-        out["chunk_scan"] -= state
+        out["chunk_scan"] += nc * state - state - h0   # reads every chunk-start state, not h0 or h_final
     return out
 
 

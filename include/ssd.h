@@ -100,19 +100,24 @@ ssd_status ssd_fwd_workspace_size(const ssd_desc *desc, size_t *bytes);
 ssd_status ssd_fwd_path(const ssd_desc *desc, int32_t *uses_tensor_cores);
 
 /* How ssd_fwd runs `desc` on the current device (written to *plan): which path,
- * how the sequence is cut into super-chunks of chunks_per_super chunks (the
- * tensor-core scan walks one super-chunk per CTA with the state on chip; the
- * CUDA-core path uses one chunk), and how many kernels and cudaMemsetAsync
- * calls one ssd_fwd call issues on its stream.  Host-side query: it reads the
- * device's SM count and launches nothing.
+ * how each sequence ((batch, head) pair, in b * nh + h order) is cut into
+ * super-chunks (the tensor-core scan walks one super-chunk per CTA with the
+ * state on chip; the CUDA-core path uses one chunk), and how many kernels and
+ * cudaMemsetAsync calls one ssd_fwd call issues on its stream.  The first
+ * split_sequences sequences are cut into super-chunks of chunks_per_super
+ * chunks, the remaining ones into super-chunks of tail_chunks_per_super chunks
+ * (so that the last wave of scan CTAs still covers the SMs).  Host-side query:
+ * it reads the device's SM count and launches nothing.
  * Errors: SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED, as for ssd_fwd. */
 typedef struct {
-    int32_t tensor_cores;      /* 1: tcgen05 kernels for chunk_state and chunk_scan      */
-    int32_t chunks_per_super;  /* R                                                      */
-    int32_t n_super;           /* super-chunks per sequence (ceil(nc / R))               */
-    int32_t kernel_launches;   /* kernels per ssd_fwd call (0 for an empty problem)      */
-    int32_t memsets;           /* cudaMemsetAsync calls per ssd_fwd call                 */
-    int32_t reserved[3];
+    int32_t tensor_cores;          /* 1: tcgen05 kernels for chunk_state and chunk_scan   */
+    int32_t chunks_per_super;      /* R of the first split_sequences sequences            */
+    int32_t n_super;               /* their super-chunks per sequence (ceil(nc / R))      */
+    int32_t kernel_launches;       /* kernels per ssd_fwd call (0 for an empty problem)   */
+    int32_t memsets;               /* cudaMemsetAsync calls per ssd_fwd call              */
+    int32_t split_sequences;       /* sequences cut with chunks_per_super (<= B * nh)     */
+    int32_t tail_chunks_per_super; /* R of the remaining sequences                        */
+    int32_t tail_n_super;          /* their super-chunks per sequence                     */
 } ssd_plan;
 
 ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan);

@@ -30,7 +30,9 @@ class Desc(ctypes.Structure):
 
 class Plan(ctypes.Structure):
     _fields_ = [("tensor_cores", ctypes.c_int32), ("chunks_per_super", ctypes.c_int32), ("n_super", ctypes.c_int32),
-                ("kernel_launches", ctypes.c_int32), ("memsets", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("kernel_launches", ctypes.c_int32), ("memsets", ctypes.c_int32),
+                ("split_sequences", ctypes.c_int32), ("tail_chunks_per_super", ctypes.c_int32),
+                ("tail_n_super", ctypes.c_int32)]
 
 
 class SSDError(RuntimeError):

@@ -3,6 +3,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <math.h>
+
 #include <mutex>
 
 #include "ssd_common.cuh"
@@ -110,12 +112,12 @@ int device_sms()
 }
 
 // Chunks per super-chunk for the tensor-core path.  Each scan CTA walks one
-// super-chunk of one (batch, head, 64-column block); more super-chunks give more
-// CTAs but cost an extra read of x and B (the chunk_state pass) and state traffic.
-// Pick the count that minimises estimated bytes / wave efficiency (one CTA per SM).
-int choose_chunks_per_super(const Problem &pr)
+// super-chunk of one (batch, head, 64-column block) with the state on chip, one CTA per
+// SM; more super-chunks give more CTAs but cost an extra read of x and B (the
+// chunk_state pass) and state traffic.  Pick the count that minimises estimated bytes /
+// wave efficiency.
+int choose_chunks_per_super(const Problem &pr, double sms)
 {
-    const double sms = (double)device_sms();
     const double es = (double)esize(pr.in_dt);
     const double units1 = (double)(pr.B * pr.nh * (pr.H / 64));
     const double x_bytes = (double)(pr.B * pr.L * pr.nh * pr.H) * es;
@@ -137,6 +139,54 @@ int choose_chunks_per_super(const Problem &pr)
         if (cost < best * 0.999) { best = cost; best_R = R; }
     }
     return best_R;
+}
+
+// How the tensor-core path cuts the sequences into super-chunks (ssd::ScanSplit).
+// Every sequence is first cut into super-chunks of R chunks (choose_chunks_per_super).
+// When that leaves the last wave of scan CTAs less than a third full, its few CTAs
+// would run alone for a whole super-chunk while the other SMs idle; instead, the
+// sequences of that last wave (rounded up to whole chunk_state head groups) are cut
+// again into super-chunks short enough that their CTAs spread over all SMs.  The short
+// super-chunks need their entering states (a chunk_state and a state_passing pass over
+// those sequences only), which costs far less than the idle wave.
+ssd::ScanSplit choose_tc_plan(const Problem &pr)
+{
+    const int64_t sms = device_sms();
+    const int64_t nseq = pr.B * pr.nh, npb = pr.H / 64;
+    const int R = choose_chunks_per_super(pr, (double)sms);
+    const int nsup = (int)((pr.nc + R - 1) / R);
+    ssd::ScanSplit sp{nseq, R, nsup, R, nsup, 1, nseq * nsup};
+    const int64_t per_seq = (int64_t)nsup * npb;             // scan CTAs per sequence
+    const int64_t ctas = nseq * per_seq;
+    const int64_t last = ctas % sms;                          // CTAs in the last, partial wave
+    if (ctas <= sms || last == 0 || 3 * last >= sms) return sp;
+    const int64_t align = ssd::state_heads_per_cta(pr);
+    int64_t tail = (last + per_seq - 1) / per_seq;            // sequences of the last wave
+    tail = (tail + align - 1) / align * align;
+    if (tail >= nseq) return sp;
+    // the tail's chunks over all SMs, at least one chunk per super-chunk
+    const int64_t tail_chunks = tail * (int64_t)pr.nc * npb;
+    int R1 = (int)((tail_chunks + sms - 1) / sms);
+    if (R1 < 1) R1 = 1;
+    if (R1 >= R) return sp;
+    sp.split = nseq - tail;
+    sp.R1 = R1;
+    sp.nsup1 = (int)((pr.nc + R1 - 1) / R1);
+    sp.base1 = sp.split * nsup;
+    return sp;
+}
+
+// The two parts of a plan as sequence runs with their cuts and state-array offsets.
+struct PlanPart {
+    ssd::SeqRange seqs;
+    int R, nsup;
+    int64_t base;        // first state index of the part in s_local / h_start
+};
+
+void plan_parts(const Problem &pr, const ssd::ScanSplit &sp, PlanPart out[2])
+{
+    out[0] = PlanPart{ssd::SeqRange{0, sp.split}, sp.R0, sp.nsup0, 0};
+    out[1] = PlanPart{ssd::SeqRange{sp.split, pr.B * pr.nh - sp.split}, sp.R1, sp.nsup1, sp.base1};
 }
 
 ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const float *A,
@@ -181,19 +231,25 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
         return SSD_ERR_CUDA;
 
     if (tc) {
-        const int R = choose_chunks_per_super(pr);
-        const int nsup = (int)((pr.nc + R - 1) / R);
-        // states of super-chunks 0 .. nsup-2 (the last one's state is produced by the scan)
+        const ssd::ScanSplit sp = choose_tc_plan(pr);
+        PlanPart parts[2];
+        plan_parts(pr, sp, parts);
+        const int64_t HS = pr.H * pr.S;
+        // per part: states of super-chunks 0 .. nsup-2 (the last one's state is produced by the scan)
         if (!rec(2)) return SSD_ERR_CUDA;
-        if (nsup > 1 && ssd::launch_chunk_state_tc(pr, x, dt, w.dtT, Bm, w.G, w.s_local, R, nsup, nsup - 1, w.err, st) !=
-                            cudaSuccess)
-            return SSD_ERR_CUDA;
+        for (const PlanPart &p : parts)
+            if (p.seqs.n > 0 && p.nsup > 1 &&
+                ssd::launch_chunk_state_tc(pr, p.seqs, x, dt, w.dtT, Bm, w.G, w.s_local + p.base * HS, p.R, p.nsup,
+                                           p.nsup - 1, w.err, st) != cudaSuccess)
+                return SSD_ERR_CUDA;
         if (!rec(3) || !rec(4)) return SSD_ERR_CUDA;
-        if (nsup > 1 &&
-            ssd::launch_state_passing(pr, w.G, w.s_local, h0, w.h_start, nullptr, R, nsup, nsup - 1, st) != cudaSuccess)
-            return SSD_ERR_CUDA;
+        for (const PlanPart &p : parts)
+            if (p.seqs.n > 0 && p.nsup > 1 &&
+                ssd::launch_state_passing(pr, p.seqs, w.G, w.s_local + p.base * HS, h0, w.h_start + p.base * HS,
+                                          nullptr, p.R, p.nsup, p.nsup - 1, st) != cudaSuccess)
+                return SSD_ERR_CUDA;
         if (!rec(5) || !rec(6)) return SSD_ERR_CUDA;
-        if (ssd::launch_chunk_scan_tc(pr, x, dt, Bm, Cm, D, w.G, h0, w.h_start, h_final, y, R, nsup, 1, w.err, st) !=
+        if (ssd::launch_chunk_scan_tc(pr, x, dt, Bm, Cm, D, w.G, h0, w.h_start, h_final, y, sp, w.err, st) !=
             cudaSuccess)
             return SSD_ERR_CUDA;
         if (!rec(7)) return SSD_ERR_CUDA;
@@ -202,7 +258,9 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
     const int nc = (int)pr.nc;
     if (!rec(2) || ssd::launch_chunk_state_simt(pr, x, dt, Bm, w.G, w.s_local, st) != cudaSuccess || !rec(3))
         return SSD_ERR_CUDA;
-    if (!rec(4) || ssd::launch_state_passing(pr, w.G, w.s_local, h0, w.h_start, h_final, 1, nc, nc, st) != cudaSuccess ||
+    if (!rec(4) ||
+        ssd::launch_state_passing(pr, ssd::SeqRange{0, pr.B * pr.nh}, w.G, w.s_local, h0, w.h_start, h_final, 1, nc,
+                                  nc, st) != cudaSuccess ||
         !rec(5))
         return SSD_ERR_CUDA;
     if (!rec(6) || ssd::launch_chunk_scan_simt(pr, x, dt, Bm, Cm, D, w.G, w.h_start, y, st) != cudaSuccess || !rec(7))
@@ -265,15 +323,27 @@ ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan)
         return SSD_OK;
     }
     if (p.tensor_cores) {
-        const int R = choose_chunks_per_super(pr);
-        const int nsup = (int)((pr.nc + R - 1) / R);
-        p.chunks_per_super = R;
-        p.n_super = nsup;
-        p.kernel_launches = nsup > 1 ? 4 : 2;
-        p.memsets = 1 + ((nsup > 1 && ssd::chunk_state_tc_memsets(pr, R, nsup - 1)) ? 1 : 0);
+        const ssd::ScanSplit sp = choose_tc_plan(pr);
+        PlanPart parts[2];
+        plan_parts(pr, sp, parts);
+        p.chunks_per_super = sp.R0;
+        p.n_super = sp.nsup0;
+        p.split_sequences = (int32_t)sp.split;
+        p.tail_chunks_per_super = sp.R1;
+        p.tail_n_super = sp.nsup1;
+        p.kernel_launches = 2;                 // cumsum and scan
+        p.memsets = 1;                         // the error word
+        for (const PlanPart &q : parts) {
+            if (q.seqs.n == 0 || q.nsup <= 1) continue;
+            p.kernel_launches += 2;            // chunk_state and state_passing of the part
+            if (ssd::chunk_state_tc_memsets(pr, q.seqs, q.R, q.nsup - 1)) p.memsets += 1;
+        }
     } else {
         p.chunks_per_super = 1;
         p.n_super = (int32_t)pr.nc;
+        p.split_sequences = (int32_t)(pr.B * pr.nh);
+        p.tail_chunks_per_super = 1;
+        p.tail_n_super = (int32_t)pr.nc;
         p.kernel_launches = 4;
         p.memsets = 1;
     }
@@ -349,7 +419,8 @@ ssd_status ssd_chunk_state(const ssd_desc *desc, const void *x, const void *dt, 
         return SSD_ERR_INVALID_ARG;
     const int nc = (int)pr.nc;
     cudaError_t e = use_tensor_cores(desc, pr)
-                        ? ssd::launch_chunk_state_tc(pr, x, dt, nullptr, Bm, G, s_local, 1, nc, nc, nullptr, (cudaStream_t)stream)
+                        ? ssd::launch_chunk_state_tc(pr, ssd::SeqRange{0, pr.B * pr.nh}, x, dt, nullptr, Bm, G, s_local,
+                                                     1, nc, nc, nullptr, (cudaStream_t)stream)
                         : ssd::launch_chunk_state_simt(pr, x, dt, Bm, G, s_local, (cudaStream_t)stream);
     return cuda_status(e);
 }
@@ -368,7 +439,8 @@ ssd_status ssd_state_passing(const ssd_desc *desc, const float *G, const float *
     const size_t states = (size_t)(pr.B * pr.nh * pr.nc * pr.H * pr.S);
     if (overlaps(s_local, states * 4, h_start, states * 4)) return SSD_ERR_INVALID_ARG;
     const int nc = (int)pr.nc;
-    return cuda_status(ssd::launch_state_passing(pr, G, s_local, h0, h_start, h_final, 1, nc, nc, (cudaStream_t)stream));
+    return cuda_status(ssd::launch_state_passing(pr, ssd::SeqRange{0, pr.B * pr.nh}, G, s_local, h0, h_start, h_final,
+                                                 1, nc, nc, (cudaStream_t)stream));
 }
 
 ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, const void *Bm,
@@ -387,7 +459,8 @@ ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, c
     const int nc = (int)pr.nc;
     cudaError_t e;
     if (use_tensor_cores(desc, pr)) {
-        e = ssd::launch_chunk_scan_tc(pr, x, dt, Bm, Cm, D, G, nullptr, h_start, nullptr, y, 1, nc, 0, nullptr,
+        const ssd::ScanSplit sp{pr.B * pr.nh, 1, nc, 1, nc, 0, 0};
+        e = ssd::launch_chunk_scan_tc(pr, x, dt, Bm, Cm, D, G, nullptr, h_start, nullptr, y, sp, nullptr,
                                       (cudaStream_t)stream);
     } else {
         e = ssd::launch_chunk_scan_simt(pr, x, dt, Bm, Cm, D, G, h_start, y, (cudaStream_t)stream);

@@ -28,6 +28,14 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(v);
 }
 
+// A run of sequences, i.e. (batch, head) pairs in b * nh + h order: [lo, lo + n).
+// The chunk_state and state_passing stages work on one run at a time; their
+// per-super-chunk states for sequence bh and super-chunk m sit at index
+// (bh - lo) * nsup + m of the state arrays they are given.
+struct SeqRange {
+    int64_t lo, n;
+};
+
 // Host-side launchers (one per stage).  Each returns the launch status.
 // dtT (nullable): also write dt as float32 in the [b][h][L] layout of G.
 cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *A, float *G,
@@ -35,10 +43,12 @@ cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *
 cudaError_t launch_chunk_state_simt(const Problem &pr, const void *x, const void *dt,
                                     const void *Bm, const float *G, float *s_local,
                                     cudaStream_t st);
-// Super-chunk state passing: h_start[m] for m < nsup (R chunks per super-chunk);
-// s_local is read for m < nm; h_final (nullable) is written when nm == nsup.
-cudaError_t launch_state_passing(const Problem &pr, const float *G, const float *s_local, const float *h0,
-                                 float *h_start, float *h_final, int R, int nsup, int nm, cudaStream_t st);
+// Super-chunk state passing over the sequences of `seqs`: h_start[m] for m < nsup
+// (R chunks per super-chunk); s_local is read for m < nm; h_final (nullable, indexed
+// by the absolute sequence) is written when nm == nsup.
+cudaError_t launch_state_passing(const Problem &pr, SeqRange seqs, const float *G, const float *s_local,
+                                 const float *h0, float *h_start, float *h_final, int R, int nsup, int nm,
+                                 cudaStream_t st);
 cudaError_t launch_chunk_scan_simt(const Problem &pr, const void *x, const void *dt,
                                    const void *Bm, const void *Cm, const float *D, const float *G,
                                    const float *h_start, void *y, cudaStream_t st);

@@ -177,7 +177,7 @@ template <int VEC>
 __global__ void __launch_bounds__(256)
 k_state_passing(const float *__restrict__ G, const float *__restrict__ s_local,
                 const float *__restrict__ h0, float *__restrict__ h_start,
-                float *__restrict__ h_final, Problem pr, int R, int nsup, int nm)
+                float *__restrict__ h_final, Problem pr, SeqRange seqs, int R, int nsup, int nm)
 {
     using V = typename std::conditional<VEC == 4, float4, float>::type;
     constexpr int kBatch = 8;                     // states loaded together (independent loads)
@@ -186,54 +186,55 @@ k_state_passing(const float *__restrict__ G, const float *__restrict__ s_local,
     const int64_t HS = pr.H * pr.S;
     const int64_t e = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * VEC;
     const bool active = e < HS;
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int64_t bh = (int64_t)b * pr.nh + h;
-    const float *Gh = G + bh * pr.L;
-    float st[VEC];
+    // one sequence at a time (a grid row may serve several when there are more than 65535)
+    for (int64_t rel = blockIdx.y; rel < seqs.n; rel += gridDim.y) {
+        const int64_t bh = seqs.lo + rel;
+        const float *Gh = G + bh * pr.L;
+        float st[VEC];
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) st[i] = 0.f;
-    if (active && h0) {
-        const V v = *reinterpret_cast<const V *>(h0 + bh * HS + e);
-        memcpy(st, &v, sizeof(V));
-    }
-    const int64_t base = bh * nsup * HS + e;
-    for (int w0 = 0; w0 < nsup; w0 += kWin) {
-        const int w1 = min(nsup, w0 + kWin);
-        __syncthreads();                          // the previous window's decays are no longer read
-        for (int m = w0 + threadIdx.x; m < min(w1, nm); m += blockDim.x) {
-            float dec = 0.f;
-            const int k1 = min((int)pr.nc, (m + 1) * R);
-            for (int k = m * R; k < k1; ++k) dec += Gh[min(pr.L, (int64_t)(k + 1) * pr.T) - 1];
-            sdec[m - w0] = exp2f(dec);
+        for (int i = 0; i < VEC; ++i) st[i] = 0.f;
+        if (active && h0) {
+            const V v = *reinterpret_cast<const V *>(h0 + bh * HS + e);
+            memcpy(st, &v, sizeof(V));
         }
-        __syncthreads();
-        if (!active) continue;
-        for (int m0 = w0; m0 < w1; m0 += kBatch) {
-            V sv[kBatch];
+        const int64_t base = rel * nsup * HS + e;
+        for (int w0 = 0; w0 < nsup; w0 += kWin) {
+            const int w1 = min(nsup, w0 + kWin);
+            __syncthreads();                          // the previous window's decays are no longer read
+            for (int m = w0 + threadIdx.x; m < min(w1, nm); m += blockDim.x) {
+                float dec = 0.f;
+                const int k1 = min((int)pr.nc, (m + 1) * R);
+                for (int k = m * R; k < k1; ++k) dec += Gh[min(pr.L, (int64_t)(k + 1) * pr.T) - 1];
+                sdec[m - w0] = exp2f(dec);
+            }
+            __syncthreads();
+            if (!active) continue;
+            for (int m0 = w0; m0 < w1; m0 += kBatch) {
+                V sv[kBatch];
 #pragma unroll
-            for (int i = 0; i < kBatch; ++i)
-                if (m0 + i < min(w1, nm)) sv[i] = *reinterpret_cast<const V *>(s_local + base + (int64_t)(m0 + i) * HS);
+                for (int i = 0; i < kBatch; ++i)
+                    if (m0 + i < min(w1, nm)) sv[i] = *reinterpret_cast<const V *>(s_local + base + (int64_t)(m0 + i) * HS);
 #pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-                const int m = m0 + i;
-                if (m >= w1) break;
-                V out;
-                memcpy(&out, st, sizeof(V));
-                *reinterpret_cast<V *>(h_start + base + (int64_t)m * HS) = out;
-                if (m >= nm) continue;
-                const float a = sdec[m - w0];
-                float sa[VEC];
-                memcpy(sa, &sv[i], sizeof(V));
+                for (int i = 0; i < kBatch; ++i) {
+                    const int m = m0 + i;
+                    if (m >= w1) break;
+                    V out;
+                    memcpy(&out, st, sizeof(V));
+                    *reinterpret_cast<V *>(h_start + base + (int64_t)m * HS) = out;
+                    if (m >= nm) continue;
+                    const float a = sdec[m - w0];
+                    float sa[VEC];
+                    memcpy(sa, &sv[i], sizeof(V));
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) st[j] = fmaf(a, st[j], sa[j]);
+                    for (int j = 0; j < VEC; ++j) st[j] = fmaf(a, st[j], sa[j]);
+                }
             }
         }
-    }
-    if (!active) return;
-    if (h_final && nm == nsup) {
-        V out;
-        memcpy(&out, st, sizeof(V));
-        *reinterpret_cast<V *>(h_final + bh * HS + e) = out;
+        if (active && h_final && nm == nsup) {
+            V out;
+            memcpy(&out, st, sizeof(V));
+            *reinterpret_cast<V *>(h_final + bh * HS + e) = out;
+        }
     }
 }
 
@@ -506,18 +507,20 @@ cudaError_t launch_chunk_state_simt(const Problem &pr, const void *x, const void
     return cudaGetLastError();
 }
 
-cudaError_t launch_state_passing(const Problem &pr, const float *G, const float *s_local, const float *h0,
-                                 float *h_start, float *h_final, int R, int nsup, int nm, cudaStream_t st)
+cudaError_t launch_state_passing(const Problem &pr, SeqRange seqs, const float *G, const float *s_local,
+                                 const float *h0, float *h_start, float *h_final, int R, int nsup, int nm,
+                                 cudaStream_t st)
 {
+    if (seqs.n <= 0) return cudaSuccess;
     const int64_t HS = pr.H * pr.S;
     const bool v4 = (HS % 4 == 0) && ((uintptr_t)s_local % 16 == 0) && ((uintptr_t)h_start % 16 == 0) &&
                     (!h0 || (uintptr_t)h0 % 16 == 0) && (!h_final || (uintptr_t)h_final % 16 == 0);
     const int vec = v4 ? 4 : 1;
-    dim3 grid((unsigned)((HS / vec + 255) / 256), (unsigned)pr.nh, (unsigned)pr.B);
+    dim3 grid((unsigned)((HS / vec + 255) / 256), (unsigned)(seqs.n < 65535 ? seqs.n : 65535));
     if (v4)
-        k_state_passing<4><<<grid, 256, 0, st>>>(G, s_local, h0, h_start, h_final, pr, R, nsup, nm);
+        k_state_passing<4><<<grid, 256, 0, st>>>(G, s_local, h0, h_start, h_final, pr, seqs, R, nsup, nm);
     else
-        k_state_passing<1><<<grid, 256, 0, st>>>(G, s_local, h0, h_start, h_final, pr, R, nsup, nm);
+        k_state_passing<1><<<grid, 256, 0, st>>>(G, s_local, h0, h_start, h_final, pr, seqs, R, nsup, nm);
     return cudaGetLastError();
 }
 

@@ -92,8 +92,10 @@ struct StateCfg {
     static constexpr int kN = HG * H;                      // MMA N: all heads' p columns
     static constexpr uint32_t kBBytes = (S / 64) * kAtomT;
     static constexpr uint32_t kXBytes = (kN / 64) * kAtomT;
-    // G and dt rows of the stage, [2][HG][kTok] f32, padded to keep stages 1024-byte aligned
-    static constexpr uint32_t kSideBytes = (2 * HG * kTok * 4 + 1023) / 1024 * 1024;
+    // G and dt rows of the stage, [2][HG][kTok] f32 (kSideLoad bytes), in a region padded to
+    // keep stages 1024-byte aligned
+    static constexpr uint32_t kSideLoad = 2 * HG * kTok * 4;
+    static constexpr uint32_t kSideBytes = (kSideLoad + 1023) / 1024 * 1024;
     static constexpr uint32_t kStage = kBBytes + kXBytes + kSideBytes;   // a multiple of 1024
     static constexpr int kStages = (204 * 1024) / kStage < 8 ? (204 * 1024) / kStage : 8;
     static constexpr int kMaxR = 256;
@@ -111,18 +113,22 @@ struct StateCfg {
     static_assert(kStage % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 };
 
-// (batch, super-chunk, first head) of a chunk_state unit; head groups vary fastest.
+// (batch, super-chunk, first head) of a chunk_state unit, and the unit's first sequence
+// relative to the run being processed.  A unit is HG heads of one group over one
+// super-chunk; the run's head groups vary fastest.
 struct StateUnit {
     int b, m, h0;
+    int64_t rel;         // (b * nh + h0) - first sequence of the run
 };
 
-__device__ __forceinline__ StateUnit state_unit(int64_t u, int nhq, int nm, int HG)
+__device__ __forceinline__ StateUnit state_unit(int64_t u, int64_t bhg_lo, int64_t nbhg, int nhq, int HG)
 {
     StateUnit r;
-    r.h0 = (int)(u % nhq) * HG;
-    u /= nhq;
-    r.m = (int)(u % nm);
-    r.b = (int)(u / nm);
+    const int64_t rel_g = u % nbhg, bhg = bhg_lo + rel_g;
+    r.m = (int)(u / nbhg);
+    r.b = (int)(bhg / nhq);
+    r.h0 = (int)(bhg % nhq) * HG;
+    r.rel = rel_g * HG;
     return r;
 }
 
@@ -130,7 +136,8 @@ template <int S, int H, int HG>
 __global__ void __launch_bounds__(192, 1)
 k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmX,
                  const float *__restrict__ G, const __nv_bfloat16 *__restrict__ dt, const float *__restrict__ dtT,
-                 float *__restrict__ s_out, Problem pr, int R, int nsup, int nm, int *err)
+                 float *__restrict__ s_out, Problem pr, int64_t bhg_lo, int64_t nbhg, int R, int nsup, int nm,
+                 int *err)
 {
     using Cfg = StateCfg<S, H, HG>;
     constexpr int kN = Cfg::kN, kS = Cfg::kStages, kTok = Cfg::kTok;
@@ -146,7 +153,7 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
     const int nhq = (int)(pr.nh / HG);
     const int qpc = (int)(pr.T / kTok);                      // stages per chunk
     const int64_t nq_u = (int64_t)R * qpc;                   // stages per unit (every unit holds R chunks)
-    const int64_t total = (int64_t)pr.B * nm * nhq * nq_u;
+    const int64_t total = nbhg * nm * nq_u;
     const int64_t q_lo = total * blockIdx.x / gridDim.x;
     const int64_t q_hi = total * (blockIdx.x + 1) / gridDim.x;
     // staged: the TMA thread also copies each stage's G and dt rows (dt from the float32
@@ -174,12 +181,12 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
                 if (i >= kS && !mbar_wait(smem_u32(&bars[kFreeB + st]), ((i / kS) - 1) & 1, kWaitNs)) {
                     ok = false; set_error(err, 1); break;
                 }
-                const StateUnit un = state_unit(gq / nq_u, nhq, nm, HG);
+                const StateUnit un = state_unit(gq / nq_u, bhg_lo, nbhg, nhq, HG);
                 const int g = (int)(un.h0 / pr.hpg);
                 const int t0 = (int)((int64_t)un.m * R * pr.T + (gq % nq_u) * kTok);
                 uint8_t *base = smem + st * Cfg::kStage;
                 const uint32_t full = smem_u32(&bars[kFullB + st]);
-                mbar_arrive_expect_tx(full, Cfg::kBBytes + Cfg::kXBytes + (staged ? Cfg::kSideBytes : 0u));
+                mbar_arrive_expect_tx(full, Cfg::kBBytes + Cfg::kXBytes + (staged ? Cfg::kSideLoad : 0u));
                 if (staged) {
                     uint8_t *side = base + Cfg::kBBytes + Cfg::kXBytes;
                     for (int hh = 0; hh < HG; ++hh) {
@@ -237,7 +244,7 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
         // this row's dt and G for every head, loaded one stage ahead
         float n_dt[HG], n_g[HG];
         auto load_row = [&](int64_t gq) {
-            const StateUnit un = state_unit(gq / nq_u, nhq, nm, HG);
+            const StateUnit un = state_unit(gq / nq_u, bhg_lo, nbhg, nhq, HG);
             const int64_t t = (int64_t)un.m * R * pr.T + (gq % nq_u) * kTok + xr;
 #pragma unroll
             for (int hh = 0; hh < HG; ++hh) {
@@ -250,7 +257,7 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
         for (int64_t gq = q_lo; gq < q_hi; ++piece) {
             const int64_t u = gq / nq_u;
             const int64_t p_begin = gq, p_end = q_hi < (u + 1) * nq_u ? q_hi : (u + 1) * nq_u;
-            const StateUnit un = state_unit(u, nhq, nm, HG);
+            const StateUnit un = state_unit(u, bhg_lo, nbhg, nhq, HG);
             // log2 decay from the end of chunk k to the end of the super-chunk, plus chunk k's own
             // G_last: gl[hh][k] = sum_{k' >= k} G_last(k'), per head (double-buffered by piece)
             float *gl = sGl + (piece & 1) * (HG * Cfg::kMaxR);
@@ -321,7 +328,7 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
 #pragma unroll 4
                     for (int c0 = 0; c0 < kN; c0 += 16) {
                         const int hh = c0 / H, p0 = c0 % H;
-                        float *dst = s_out + (((int64_t)un.b * pr.nh + un.h0 + hh) * nsup + un.m) * (int64_t)(H * S) + s;
+                        float *dst = s_out + ((un.rel + hh) * nsup + un.m) * (int64_t)(H * S) + s;
                         uint32_t v[16];
                         tmem_ld16(tmem + lane_base + lb * kN + c0, v);
                         tmem_ld_wait();
@@ -409,7 +416,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 const float *__restrict__ G, const __nv_bfloat16 *__restrict__ dt, const float *__restrict__ Dp,
                 const float *__restrict__ h0,
                 const float *__restrict__ h_start, float *__restrict__ h_final,
-                __nv_bfloat16 *__restrict__ y, Problem pr, int R, int nsup, int hs_from, int *err)
+                __nv_bfloat16 *__restrict__ y, Problem pr, ScanSplit sp, int *err)
 {
     using Cfg = ScanCfg<S>;
     constexpr int kCBS = Cfg::kCBStages, kXS = Cfg::kXStages;
@@ -420,21 +427,31 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
     uint32_t *tmem_slot = (uint32_t *)(bars + kNumScanBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // CTA -> (part, super-chunk m, sequence bh, 64-column block pb), column blocks fastest,
+    // then the part's sequences, then m
+    // (32-bit: the launcher checks that the CTA count fits)
     const int npb = (int)(pr.H / kPB);
-    int u = blockIdx.x;
+    const int units0 = (int)sp.split * sp.nsup0 * npb;
+    const bool part1 = (int)blockIdx.x >= units0;
+    int u = part1 ? (int)blockIdx.x - units0 : (int)blockIdx.x;
+    const int seq_lo = part1 ? (int)sp.split : 0;
+    const int nseq = part1 ? (int)(pr.B * pr.nh - sp.split) : (int)sp.split;
+    const int R = part1 ? sp.R1 : sp.R0, nsup = part1 ? sp.nsup1 : sp.nsup0;
     const int pb = u % npb; u /= npb;
-    const int h = u % pr.nh; u /= pr.nh;
-    const int m = u % nsup;
-    const int b = u / nsup;
+    const int bhi = seq_lo + u % nseq;
+    const int m = u / nseq;
+    const int b = bhi / (int)pr.nh, h = bhi % (int)pr.nh;
     const int g = (int)(h / pr.hpg);
     const int k_begin = m * R;
     const int k_end = min((int)pr.nc, k_begin + R);
     const int qpc = (int)(pr.T / kQ);
     const int nq = (k_end - k_begin) * qpc;
     const int64_t t_begin = (int64_t)k_begin * pr.T;
-    const int64_t bh = (int64_t)b * pr.nh + h;
+    const int64_t bh = bhi;
     const float *Gh = G + bh * pr.L;
     const bool write_final = (m == nsup - 1) && h_final;
+    // h_start index of this super-chunk's entering state (used when m >= hs_from)
+    const int64_t hs_idx = (part1 ? sp.base1 : 0) + (int64_t)(bhi - seq_lo) * nsup + m;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumScanBars; ++i) {
@@ -597,9 +614,9 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                     const int s = lb * 128 + r;
                     uint32_t v[64];
                     if (q == 0) {
-                        // entering state: h0 (zeros if absent) for super-chunks m < hs_from, else h_start[m]
-                        const float *src = (m < hs_from) ? (h0 ? h0 + bh * (int64_t)(pr.H * S) : nullptr)
-                                                         : h_start + (bh * nsup + m) * (int64_t)(pr.H * S);
+                        // entering state: h0 (zeros if absent) for super-chunks m < hs_from, else h_start
+                        const float *src = (m < sp.hs_from) ? (h0 ? h0 + bh * (int64_t)(pr.H * S) : nullptr)
+                                                            : h_start + hs_idx * (int64_t)(pr.H * S);
                         if (src) {
                             src += (int64_t)(pb * kPB) * S + s;
 #pragma unroll
@@ -895,16 +912,30 @@ int current_sms()
     return sms > 0 ? sms : 1;
 }
 
+// chunk_state CTAs for `total` stages in units of nq_u.  With enough work, one CTA per
+// SM, each walking an equal slice (units cut between CTAs are added into a zeroed
+// output with atomics, whose cost the long slices amortise); with little work, one
+// whole unit per CTA, which needs no zeroing and no atomics.
+int64_t state_grid(int64_t total, int64_t nq_u)
+{
+    const int64_t sms = current_sms();
+    if (total < 16 * sms) return total / nq_u;
+    return sms;
+}
+
 template <int S, int H, int HG>
-cudaError_t state_launch(const Problem &pr, const void *x, const void *dt, const float *dtT, const void *Bm,
-                         const float *G, float *s_out, int R, int nsup, int nm, int *err, cudaStream_t st)
+cudaError_t state_launch(const Problem &pr, SeqRange seqs, const void *x, const void *dt, const float *dtT,
+                         const void *Bm, const float *G, float *s_out, int R, int nsup, int nm, int *err,
+                         cudaStream_t st)
 {
     using Cfg = StateCfg<S, H, HG>;
     if (R > Cfg::kMaxR) return cudaErrorInvalidValue;
     // every unit must hold R whole chunks (a short last super-chunk is left to the scan)
     if ((int64_t)nm * R > pr.nc) return cudaErrorInvalidValue;
+    // units are whole head groups of the run
+    if (seqs.lo % HG != 0 || seqs.n % HG != 0) return cudaErrorInvalidValue;
     const int64_t nq_u = (int64_t)R * (pr.T / Cfg::kTok);
-    const int64_t total = pr.B * (int64_t)nm * (pr.nh / HG) * nq_u;
+    const int64_t total = (seqs.n / HG) * (int64_t)nm * nq_u;
     if (total == 0) return cudaSuccess;
     CUtensorMap mB, mX;
     if (!make_map_4d(&mB, Bm, pr.S, pr.G, pr.L, pr.B, Cfg::kTok) || !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, Cfg::kTok))
@@ -912,22 +943,21 @@ cudaError_t state_launch(const Problem &pr, const void *x, const void *dt, const
     auto kern = k_chunk_state_tc<S, H, HG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    const int64_t sms = current_sms();
-    const int64_t grid = total < sms ? total : sms;
+    const int64_t grid = state_grid(total, nq_u);
     // a slice boundary inside a unit: both parts add into a zeroed s_out
     if (slices_split_units(total, grid, nq_u)) {
-        e = cudaMemsetAsync(s_out, 0, (size_t)(pr.B * pr.nh * nsup) * (size_t)(pr.H * pr.S) * sizeof(float), st);
+        e = cudaMemsetAsync(s_out, 0, (size_t)(seqs.n * nsup) * (size_t)(pr.H * pr.S) * sizeof(float), st);
         if (e != cudaSuccess) return e;
     }
-    kern<<<(unsigned)grid, 192, Cfg::kSmem, st>>>(mB, mX, G, (const __nv_bfloat16 *)dt, dtT, s_out, pr, R, nsup, nm,
-                                                   err);
+    kern<<<(unsigned)grid, 192, Cfg::kSmem, st>>>(mB, mX, G, (const __nv_bfloat16 *)dt, dtT, s_out, pr,
+                                                   seqs.lo / HG, seqs.n / HG, R, nsup, nm, err);
     return cudaGetLastError();
 }
 
 template <int S>
 cudaError_t scan_launch(const Problem &pr, const void *x, const void *dt, const void *Bm, const void *Cm, const float *D,
-                        const float *G, const float *h0, const float *h_start, float *h_final, void *y, int R, int nsup,
-                        int hs_from, int *err, cudaStream_t st)
+                        const float *G, const float *h0, const float *h_start, float *h_final, void *y,
+                        const ScanSplit &sp, int *err, cudaStream_t st)
 {
     CUtensorMap mC, mB, mX, mY;
     if (!make_map_4d(&mC, Cm, pr.S, pr.G, pr.L, pr.B, kQ) || !make_map_4d(&mB, Bm, pr.S, pr.G, pr.L, pr.B, kQ) ||
@@ -937,9 +967,11 @@ cudaError_t scan_launch(const Problem &pr, const void *x, const void *dt, const 
     auto kern = k_chunk_scan_tc<S>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(pr.B * nsup * pr.nh * (pr.H / kPB));
-    kern<<<grid, 448, Cfg::kSmem, st>>>(mC, mB, mX, mY, G, (const __nv_bfloat16 *)dt, D, h0,
-                                        h_start, h_final, (__nv_bfloat16 *)y, pr, R, nsup, hs_from, err);
+    const int64_t grid = (sp.split * sp.nsup0 + (pr.B * pr.nh - sp.split) * sp.nsup1) * (pr.H / kPB);
+    if (grid == 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    kern<<<(unsigned)grid, 448, Cfg::kSmem, st>>>(mC, mB, mX, mY, G, (const __nv_bfloat16 *)dt, D, h0,
+                                        h_start, h_final, (__nv_bfloat16 *)y, pr, sp, err);
     return cudaGetLastError();
 }
 
@@ -965,40 +997,56 @@ int state_heads_per_cta(const Problem &pr)
     return 1;
 }
 
-bool chunk_state_tc_memsets(const Problem &pr, int R, int nm)
+// Heads per chunk_state CTA for a launch over `seqs` with nm super-chunks of R chunks:
+// the most that share B tiles; for a small launch (one whole unit per CTA, see
+// state_grid) with fewer units than SMs, halved while that holds, since such a launch
+// is latency-bound and more, smaller units finish sooner.
+int state_launch_heads(const Problem &pr, SeqRange seqs, int R, int nm)
 {
-    const int64_t nq_u = (int64_t)R * (pr.T / 64);
-    const int64_t total = pr.B * (int64_t)nm * (pr.nh / state_heads_per_cta(pr)) * nq_u;
-    if (total == 0) return false;
-    const int64_t sms = current_sms();
-    return slices_split_units(total, total < sms ? total : sms, nq_u);
+    int hg = state_heads_per_cta(pr);
+    const int64_t sms = current_sms(), nq_u = (int64_t)R * (pr.T / 64);
+    while (hg > 1) {
+        const int64_t units = (seqs.n / hg) * nm;
+        if (units * nq_u >= 16 * sms || units >= sms) break;
+        hg /= 2;
+    }
+    return hg;
 }
 
-cudaError_t launch_chunk_state_tc(const Problem &pr, const void *x, const void *dt, const float *dtT, const void *Bm,
-                                  const float *G, float *s_out, int R, int nsup, int nm, int *err, cudaStream_t st)
+bool chunk_state_tc_memsets(const Problem &pr, SeqRange seqs, int R, int nm)
+{
+    const int64_t nq_u = (int64_t)R * (pr.T / 64);
+    const int64_t total = (seqs.n / state_launch_heads(pr, seqs, R, nm)) * (int64_t)nm * nq_u;
+    if (total == 0) return false;
+    return slices_split_units(total, state_grid(total, nq_u), nq_u);
+}
+
+cudaError_t launch_chunk_state_tc(const Problem &pr, SeqRange seqs, const void *x, const void *dt, const float *dtT,
+                                  const void *Bm, const float *G, float *s_out, int R, int nsup, int nm, int *err,
+                                  cudaStream_t st)
 {
     if (R < 1 || R > 256) return cudaErrorInvalidValue;
-    const int hg = state_heads_per_cta(pr);
+    const int hg = state_launch_heads(pr, seqs, R, nm);
     if (pr.S == 128 && pr.H == 64) {
-        if (hg == 4) return state_launch<128, 64, 4>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
-        if (hg == 2) return state_launch<128, 64, 2>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
-        return state_launch<128, 64, 1>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+        if (hg == 4) return state_launch<128, 64, 4>(pr, seqs, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+        if (hg == 2) return state_launch<128, 64, 2>(pr, seqs, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+        return state_launch<128, 64, 1>(pr, seqs, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
     }
     if (pr.S == 128 && pr.H == 128) {
-        if (hg == 2) return state_launch<128, 128, 2>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
-        return state_launch<128, 128, 1>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+        if (hg == 2) return state_launch<128, 128, 2>(pr, seqs, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+        return state_launch<128, 128, 1>(pr, seqs, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
     }
-    if (pr.S == 256 && pr.H == 64) return state_launch<256, 64, 1>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
-    if (pr.S == 256 && pr.H == 128) return state_launch<256, 128, 1>(pr, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+    if (pr.S == 256 && pr.H == 64) return state_launch<256, 64, 1>(pr, seqs, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
+    if (pr.S == 256 && pr.H == 128) return state_launch<256, 128, 1>(pr, seqs, x, dt, dtT, Bm, G, s_out, R, nsup, nm, err, st);
     return cudaErrorNotSupported;
 }
 
 cudaError_t launch_chunk_scan_tc(const Problem &pr, const void *x, const void *dt, const void *Bm, const void *Cm,
                                  const float *D, const float *G, const float *h0, const float *h_start, float *h_final,
-                                 void *y, int R, int nsup, int hs_from, int *err, cudaStream_t st)
+                                 void *y, const ScanSplit &sp, int *err, cudaStream_t st)
 {
-    if (pr.S == 128) return scan_launch<128>(pr, x, dt, Bm, Cm, D, G, h0, h_start, h_final, y, R, nsup, hs_from, err, st);
-    if (pr.S == 256) return scan_launch<256>(pr, x, dt, Bm, Cm, D, G, h0, h_start, h_final, y, R, nsup, hs_from, err, st);
+    if (pr.S == 128) return scan_launch<128>(pr, x, dt, Bm, Cm, D, G, h0, h_start, h_final, y, sp, err, st);
+    if (pr.S == 256) return scan_launch<256>(pr, x, dt, Bm, Cm, D, G, h0, h_start, h_final, y, sp, err, st);
     return cudaErrorNotSupported;
 }
 

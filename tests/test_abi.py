@@ -138,13 +138,23 @@ def test_fwd_plan_is_consistent(lib):
     p = P()
     assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0
     assert p.tensor_cores == 1
-    nc = 16
+    nc, nseq = 16, 4 * 80
     assert 1 <= p.chunks_per_super <= nc and p.n_super == -(-nc // p.chunks_per_super)
-    assert p.kernel_launches == (4 if p.n_super > 1 else 2) and p.memsets in (1, 2)
-    # forced CUDA-core path: one chunk per super-chunk, four stages
+    assert 1 <= p.tail_chunks_per_super <= nc and p.tail_n_super == -(-nc // p.tail_chunks_per_super)
+    assert 0 < p.split_sequences <= nseq
+    # the split falls on a whole chunk_state head group (4 heads of one group here)
+    assert p.split_sequences % 4 == 0
+    parts = [(p.split_sequences, p.n_super), (nseq - p.split_sequences, p.tail_n_super)]
+    assert p.kernel_launches == 2 + sum(2 for n, ns in parts if n > 0 and ns > 1)
+    assert 1 <= p.memsets <= 3
+    # the same shape asks for the same plan (plans are cached per shape)
+    q = P()
+    assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(q)) == 0 and bytes(q) == bytes(p)
+    # forced CUDA-core path: one chunk per super-chunk, four stages, no split
     d.flags = 1
     assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0
     assert (p.tensor_cores, p.chunks_per_super, p.n_super, p.kernel_launches, p.memsets) == (0, 1, nc, 4, 1)
+    assert (p.split_sequences, p.tail_chunks_per_super, p.tail_n_super) == (nseq, 1, nc)
     # empty sequence: nothing launched
     d = desc(seqlen=0)
     assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0 and p.kernel_launches == 0
