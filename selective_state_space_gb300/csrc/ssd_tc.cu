@@ -535,12 +535,9 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                     const uint32_t so = (uint32_t)cs * Cfg::kCBStage;
                     const uint32_t ys = Cfg::kTys + (uint32_t)(q % Cfg::kYsBufs) * kPB;
                     const uint32_t yi = Cfg::kTyi + (uint32_t)(q & 1) * kPB;
-                    // Ys = C h^T (K = s): needs the state copy and a drained Ys buffer
+                    // Ys = C h^T (K = s): needs the state copy and a drained Ys buffer; the state group
+                    // arrives kHReady after both (one wait here instead of two)
                     if (!mbar_wait(smem_u32(&bars[kHReady]), q & 1, kWaitNs)) { ok = false; break; }
-                    if (q >= Cfg::kYsBufs) {
-                        const int e = q - Cfg::kYsBufs;
-                        if (!mbar_wait(smem_u32(&bars[kEpi0 + (e & 1)]), (e >> 1) & 1, kWaitNs)) { ok = false; break; }
-                    }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < S / 16; ++kk) {
@@ -568,13 +565,9 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                     for (int kk = 0; kk < kQ / 16; ++kk)
                         mma_bf16_ts(tmem + yi, tmem + Cfg::kTp + 8 * kk, adv(dX0, xs * kAtom + kk * 2048), id_y, 1u);
                     mma_commit(smem_u32(&bars[kIntra]));
-                    // next CB (the output group has read this one: P is built)
-                    if (q + 1 < nq) {
-                        const int c1 = (q + 1) % kCBS;
-                        if (!mbar_wait(smem_u32(&bars[kFull0 + c1]), ((q + 1) / kCBS) & 1, kWaitNs)) { ok = false; break; }
-                        tc_fence_after();
-                        issue_cb(q + 1);
-                    }
+                    // next CB: the output group has read this one (P is built), and it arrived kPReady
+                    // only after the C and B tiles of the next sub-chunk had landed
+                    if (q + 1 < nq) issue_cb(q + 1);
                 }
             } while (0);
             if (!ok) set_error(err, 1);
@@ -652,6 +645,15 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 }
                 tmem_st_wait();
                 fence_proxy_async_smem();
+                // the Ys buffer this sub-chunk writes is drained once the epilogue of sub-chunk
+                // q - kYsBufs has read it (and, kYsBufs <= 2, so is the Yi buffer of sub-chunk q:
+                // the epilogues arrive in order)
+                if (q >= Cfg::kYsBufs) {
+                    const int e = q - Cfg::kYsBufs;
+                    if (!mbar_wait(smem_u32(&bars[kEpi0 + (e & 1)]), (e >> 1) & 1, kWaitNs)) {
+                        ok = false; set_error(err, 1); break;
+                    }
+                }
                 tc_fence_before();
                 mbar_arrive(smem_u32(&bars[kHReady]));
             }
@@ -659,10 +661,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             // and D x into this sub-chunk's Yi accumulator (the Yi MMAs accumulate on top of it)
             {
                 if (!mbar_wait(smem_u32(&bars[kXFull0 + xs]), (q / kXS) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
-                // the Yi buffer of this sub-chunk is free once the epilogue of sub-chunk q - 2 read it
-                if (q >= 2 && !mbar_wait(smem_u32(&bars[kEpi0 + (q & 1)]), ((q >> 1) - 1) & 1, kWaitNs)) {
-                    ok = false; set_error(err, 1); break;
-                }
+                // (the Yi buffer of this sub-chunk was drained before kHReady, above)
                 tc_fence_after();
                 uint8_t *xt = smem + Cfg::kX + xs * kAtom;
                 const float wr = dtr * exp2f(glast - gr);
@@ -755,35 +754,32 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             if (ok) {
                 tc_fence_after();
                 const int jh = 64 * half;
-                uint32_t pk[32];
-                if (jh > wrow_hi) {                     // whole half above the diagonal: zeros
+                const uint32_t ta = tmem + lane_base + Cfg::kTcb + jh;
+                const uint32_t tp = tmem + lane_base + Cfg::kTp + 32 * half;
+                // one 16-column block per iteration (a compact loop body: the four warp roles
+                // share each sub-partition's instruction cache)
+#pragma unroll 1
+                for (int blk = 0; blk < 4; ++blk) {
+                    const int j0 = jh + 16 * blk;
+                    uint32_t pk[8];
+                    if (j0 > wrow_hi) {                           // above the diagonal for the whole warp
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) pk[e] = 0u;
-                } else {
-                    uint32_t v[64];
-                    const uint32_t ta = tmem + lane_base + Cfg::kTcb + jh;
-                    tmem_ld16(ta + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                    tmem_ld16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-                    tmem_ld16(ta + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
-                    tmem_ld16(ta + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int blk = 0; blk < 4; ++blk) {
-                        const int j0 = jh + 16 * blk;
+                        for (int e = 0; e < 8; ++e) pk[e] = 0u;
+                    } else {
+                        uint32_t v[16];
+                        tmem_ld16(ta + 16 * blk, v);
+                        tmem_ld_wait();
                         float f[16];
-                        if (j0 > wrow_hi) {                       // above the diagonal for the whole warp
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) f[e] = 0.f;
-                        } else if (j0 + 15 < wrow_lo) {           // left of every row of the warp: factored
+                        if (j0 + 15 < wrow_lo) {                  // left of every row of the warp: factored
                             const float ei = ex2_approx(gr - cG[j0 + 15]);
                             const float4 *f4 = reinterpret_cast<const float4 *>(cF + j0);
 #pragma unroll
                             for (int e4 = 0; e4 < 4; ++e4) {
                                 const float4 fj = f4[e4];
-                                f[4 * e4 + 0] = __uint_as_float(v[16 * blk + 4 * e4 + 0]) * ei * fj.x;
-                                f[4 * e4 + 1] = __uint_as_float(v[16 * blk + 4 * e4 + 1]) * ei * fj.y;
-                                f[4 * e4 + 2] = __uint_as_float(v[16 * blk + 4 * e4 + 2]) * ei * fj.z;
-                                f[4 * e4 + 3] = __uint_as_float(v[16 * blk + 4 * e4 + 3]) * ei * fj.w;
+                                f[4 * e4 + 0] = __uint_as_float(v[4 * e4 + 0]) * ei * fj.x;
+                                f[4 * e4 + 1] = __uint_as_float(v[4 * e4 + 1]) * ei * fj.y;
+                                f[4 * e4 + 2] = __uint_as_float(v[4 * e4 + 2]) * ei * fj.z;
+                                f[4 * e4 + 3] = __uint_as_float(v[4 * e4 + 3]) * ei * fj.w;
                             }
                         } else {                                  // meets the diagonal: exact, selected
                             const float4 *g4 = reinterpret_cast<const float4 *>(cG + j0);
@@ -794,19 +790,23 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
 #pragma unroll
                                 for (int c = 0; c < 4; ++c) {
                                     const int e = 4 * e4 + c, j = j0 + e;
-                                    const float val = __uint_as_float(v[16 * blk + e]) * ex2_approx(gr - gjs[c]);
+                                    const float val = __uint_as_float(v[e]) * ex2_approx(gr - gjs[c]);
                                     f[e] = (j <= r) ? val : 0.f;
                                 }
                             }
                         }
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) pk[8 * blk + e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+                        for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
                     }
+                    tmem_st8(tp + 8 * blk, pk);
                 }
-                const uint32_t tp = tmem + lane_base + Cfg::kTp + 32 * half;
-                tmem_st16(tp, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                tmem_st16(tp + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
                 tmem_st_wait();
+                // the MMA warp issues the next CB right after kPReady: one thread checks that its
+                // C and B tiles have landed (the stage cannot be reloaded before this arrival)
+                if (storer && q + 1 < nq &&
+                    !mbar_wait(smem_u32(&bars[kFull0 + (q + 1) % kCBS]), ((q + 1) / kCBS) & 1, kWaitNs)) {
+                    ok = false; set_error(err, 1);
+                }
                 tc_fence_before();
                 mbar_arrive(smem_u32(&bars[kPReady]));
             }
@@ -818,28 +818,30 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             if (ok) {
                 tc_fence_after();
                 const float eg = ex2_approx(gr - gbase);
-                uint32_t vs[32], vi[32];
                 const uint32_t c0 = 32 * half;
                 const uint32_t ys = Cfg::kTys + (uint32_t)(q % Cfg::kYsBufs) * kPB + c0;
                 const uint32_t yi = Cfg::kTyi + (uint32_t)(q & 1) * kPB + c0;
-                tmem_ld16(tmem + lane_base + ys, *reinterpret_cast<uint32_t(*)[16]>(&vs[0]));
-                tmem_ld16(tmem + lane_base + ys + 16, *reinterpret_cast<uint32_t(*)[16]>(&vs[16]));
-                tmem_ld16(tmem + lane_base + yi, *reinterpret_cast<uint32_t(*)[16]>(&vi[0]));
-                tmem_ld16(tmem + lane_base + yi + 16, *reinterpret_cast<uint32_t(*)[16]>(&vi[16]));
-                tmem_ld_wait();
+                // 16 columns per iteration (compact loop body, as above)
+#pragma unroll 1
+                for (int c16 = 0; c16 < 32; c16 += 16) {
+                    uint32_t vs[16], vi[16];
+                    tmem_ld16(tmem + lane_base + ys + c16, vs);
+                    tmem_ld16(tmem + lane_base + yi + c16, vi);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int k = 8 * c + 2 * e;
+                            o[e] = pack_bf16x2(fmaf(eg, __uint_as_float(vs[k]), __uint_as_float(vi[k])),
+                                               fmaf(eg, __uint_as_float(vs[k + 1]), __uint_as_float(vi[k + 1])));
+                        }
+                        *(uint4 *)(ystage + sw128(r, 4 * half + (c16 >> 3) + c)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
                 tc_fence_before();
                 mbar_arrive(smem_u32(&bars[kEpi0 + (q & 1)]));
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t o[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k = 8 * c + 2 * e;
-                        o[e] = pack_bf16x2(fmaf(eg, __uint_as_float(vs[k]), __uint_as_float(vi[k])),
-                                           fmaf(eg, __uint_as_float(vs[k + 1]), __uint_as_float(vi[k + 1])));
-                    }
-                    *(uint4 *)(ystage + sw128(r, 4 * half + c)) = make_uint4(o[0], o[1], o[2], o[3]);
-                }
                 fence_proxy_async_smem();
             }
             // all rows staged (and the column arrays free for the next sub-chunk)
