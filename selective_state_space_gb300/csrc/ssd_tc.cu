@@ -38,7 +38,7 @@ using namespace ptx;
 constexpr int kQ = 128;                       // tokens per tensor-core sub-chunk (MMA M)
 constexpr int kPB = 64;                       // p-columns per scan unit (one swizzle atom)
 constexpr uint32_t kAtom = kQ * 128;          // bytes of one 128-row x 128-byte swizzled region
-constexpr uint64_t kWaitNs = 2000000000ull;   // bound on every wait: 2 s
+constexpr uint64_t kWaitNs = 250000000ull;    // bound on every wait: 250 ms (legitimate waits take microseconds)
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
@@ -402,10 +402,11 @@ struct ScanCfg {
     static_assert(kXStages <= 4, "x-slot barriers");
 };
 
-// kFull/kFree: the C and B tiles of a C/B stage; kXFull: an x tile; kYSt: the y staged
-// in an x slot has been read by its bulk store (the slot may be reloaded).
+// kFull/kFree: the C and B tiles of a C/B stage; kIntra0/1: the Yi MMAs into Yi buffer 0/1
+// are done; kXFull: an x tile; kYSt: the y staged in an x slot has been read by its bulk
+// store (the slot may be reloaded).
 enum ScanBar {
-    kFull0 = 0, kFree0 = 2, kCb = 4, kHReady, kXReady, kPReady, kIntra, kUpdate, kEpi0, kEpi1,
+    kFull0 = 0, kFree0 = 2, kCb = 4, kHReady, kXReady, kPReady, kIntra0, kIntra1, kUpdate, kEpi0, kEpi1,
     kXFull0, kYSt0 = kXFull0 + 4, kNumScanBars = kYSt0 + 4
 };
 
@@ -564,10 +565,18 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
 #pragma unroll
                     for (int kk = 0; kk < kQ / 16; ++kk)
                         mma_bf16_ts(tmem + yi, tmem + Cfg::kTp + 8 * kk, adv(dX0, xs * kAtom + kk * 2048), id_y, 1u);
-                    mma_commit(smem_u32(&bars[kIntra]));
-                    // next CB: the output group has read this one (P is built), and it arrived kPReady
-                    // only after the C and B tiles of the next sub-chunk had landed
-                    if (q + 1 < nq) issue_cb(q + 1);
+                    mma_commit(smem_u32(&bars[kIntra0 + (q & 1)]));
+                    // next CB: the output group has read this one (P is built); with two C/B stages it
+                    // arrived kPReady only after the next sub-chunk's C and B tiles had landed.  With
+                    // one stage those tiles load only after this sub-chunk's update, which waits on the
+                    // epilogue the output group runs after kPReady, so this thread waits for them.
+                    if (q + 1 < nq) {
+                        if (kCBS == 1) {
+                            if (!mbar_wait(smem_u32(&bars[kFull0]), (q + 1) & 1, kWaitNs)) { ok = false; break; }
+                            tc_fence_after();
+                        }
+                        issue_cb(q + 1);
+                    }
                 }
             } while (0);
             if (!ok) set_error(err, 1);
@@ -734,88 +743,102 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             n_gend = Gh[t0 + (r | 15)];                // G at the end of row r's 16-token block
             n_gbase = (q % qpc == 0) ? 0.f : Gh[t0 - 1];
         };
+        // Software-pipelined by one sub-chunk: iteration q builds P of sub-chunk q + 1, then
+        // writes y of sub-chunk q.  The MMAs of q + 1 wait on that P, while the y of q waits
+        // only on the Yi MMAs of q, which run meanwhile.
+        float gr_y = 0.f, gbase_y = 0.f;               // scalars of the sub-chunk whose y is next
         if (nq > 0) load_scalars(0);
-        for (int q = 0; q < nq; ++q) {
-            const int64_t t0 = t_begin + (int64_t)q * kQ;
-            const int xs = q % kXS;
-            const float gr = n_gr, gend = n_gend, gbase = n_gbase;
-            if (half == 0) {
-                cG[r] = gr;
-                cF[r] = ex2_approx(gend - gr);          // 2^(G_blockend - G_j) <= 1 for A dt >= 0
-            }
-            group_sync();
-            if (q + 1 < nq) load_scalars(q + 1);
+        for (int q = -1; q < nq; ++q) {
+            float gr_p = gr_y, gbase_p = gbase_y;
+            if (q + 1 < nq) {
+                const int qp = q + 1;                      // the sub-chunk whose P is built
+                const float gr = n_gr, gend = n_gend;
+                gr_p = n_gr;
+                gbase_p = n_gbase;
+                if (half == 0) {
+                    cG[r] = gr;
+                    cF[r] = ex2_approx(gend - gr);          // 2^(G_blockend - G_j) <= 1 for A dt >= 0
+                }
+                group_sync();
+                if (qp + 1 < nq) load_scalars(qp + 1);
 
-            // P[i][j] = CB[i][j] 2^(G_i - G_j) for j <= i, else 0, as bf16 pairs in TMEM (the
-            // A operand of Yi).  Blocks of 16 columns entirely left of this warp's rows use the
-            // factored form 2^(G_i - G_e) 2^(G_e - G_j) (G_e = G at the block's last column; both
-            // factors <= 1); blocks that meet the diagonal evaluate 2^(G_i - G_j) per element.
-            if (ok && !mbar_wait(smem_u32(&bars[kCb]), q & 1, kWaitNs)) { ok = false; set_error(err, 1); }
-            if (ok) {
-                tc_fence_after();
-                const int jh = 64 * half;
-                const uint32_t ta = tmem + lane_base + Cfg::kTcb + jh;
-                const uint32_t tp = tmem + lane_base + Cfg::kTp + 32 * half;
-                // one 16-column block per iteration (a compact loop body: the four warp roles
-                // share each sub-partition's instruction cache)
+                // P[i][j] = CB[i][j] 2^(G_i - G_j) for j <= i, else 0, as bf16 pairs in TMEM (the
+                // A operand of Yi).  Blocks of 16 columns entirely left of this warp's rows use the
+                // factored form 2^(G_i - G_e) 2^(G_e - G_j) (G_e = G at the block's last column; both
+                // factors <= 1); blocks that meet the diagonal evaluate 2^(G_i - G_j) per element.
+                // (the CB of qp is issued after the Yi of q, the last reader of the single P buffer)
+                if (ok && !mbar_wait(smem_u32(&bars[kCb]), qp & 1, kWaitNs)) { ok = false; set_error(err, 1); }
+                if (ok) {
+                    tc_fence_after();
+                    const int jh = 64 * half;
+                    const uint32_t ta = tmem + lane_base + Cfg::kTcb + jh;
+                    const uint32_t tp = tmem + lane_base + Cfg::kTp + 32 * half;
+                    // one 16-column block per iteration (a compact loop body: the four warp roles
+                    // share each sub-partition's instruction cache)
 #pragma unroll 1
-                for (int blk = 0; blk < 4; ++blk) {
-                    const int j0 = jh + 16 * blk;
-                    uint32_t pk[8];
-                    if (j0 > wrow_hi) {                           // above the diagonal for the whole warp
+                    for (int blk = 0; blk < 4; ++blk) {
+                        const int j0 = jh + 16 * blk;
+                        uint32_t pk[8];
+                        if (j0 > wrow_hi) {                           // above the diagonal for the whole warp
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) pk[e] = 0u;
-                    } else {
-                        uint32_t v[16];
-                        tmem_ld16(ta + 16 * blk, v);
-                        tmem_ld_wait();
-                        float f[16];
-                        if (j0 + 15 < wrow_lo) {                  // left of every row of the warp: factored
-                            const float ei = ex2_approx(gr - cG[j0 + 15]);
-                            const float4 *f4 = reinterpret_cast<const float4 *>(cF + j0);
+                            for (int e = 0; e < 8; ++e) pk[e] = 0u;
+                        } else {
+                            uint32_t v[16];
+                            tmem_ld16(ta + 16 * blk, v);
+                            tmem_ld_wait();
+                            float f[16];
+                            if (j0 + 15 < wrow_lo) {                  // left of every row of the warp: factored
+                                const float ei = ex2_approx(gr - cG[j0 + 15]);
+                                const float4 *f4 = reinterpret_cast<const float4 *>(cF + j0);
 #pragma unroll
-                            for (int e4 = 0; e4 < 4; ++e4) {
-                                const float4 fj = f4[e4];
-                                f[4 * e4 + 0] = __uint_as_float(v[4 * e4 + 0]) * ei * fj.x;
-                                f[4 * e4 + 1] = __uint_as_float(v[4 * e4 + 1]) * ei * fj.y;
-                                f[4 * e4 + 2] = __uint_as_float(v[4 * e4 + 2]) * ei * fj.z;
-                                f[4 * e4 + 3] = __uint_as_float(v[4 * e4 + 3]) * ei * fj.w;
-                            }
-                        } else {                                  // meets the diagonal: exact, selected
-                            const float4 *g4 = reinterpret_cast<const float4 *>(cG + j0);
+                                for (int e4 = 0; e4 < 4; ++e4) {
+                                    const float4 fj = f4[e4];
+                                    f[4 * e4 + 0] = __uint_as_float(v[4 * e4 + 0]) * ei * fj.x;
+                                    f[4 * e4 + 1] = __uint_as_float(v[4 * e4 + 1]) * ei * fj.y;
+                                    f[4 * e4 + 2] = __uint_as_float(v[4 * e4 + 2]) * ei * fj.z;
+                                    f[4 * e4 + 3] = __uint_as_float(v[4 * e4 + 3]) * ei * fj.w;
+                                }
+                            } else {                                  // meets the diagonal: exact, selected
+                                const float4 *g4 = reinterpret_cast<const float4 *>(cG + j0);
 #pragma unroll
-                            for (int e4 = 0; e4 < 4; ++e4) {
-                                const float4 gj = g4[e4];
-                                const float gjs[4] = {gj.x, gj.y, gj.z, gj.w};
+                                for (int e4 = 0; e4 < 4; ++e4) {
+                                    const float4 gj = g4[e4];
+                                    const float gjs[4] = {gj.x, gj.y, gj.z, gj.w};
 #pragma unroll
-                                for (int c = 0; c < 4; ++c) {
-                                    const int e = 4 * e4 + c, j = j0 + e;
-                                    const float val = __uint_as_float(v[e]) * ex2_approx(gr - gjs[c]);
-                                    f[e] = (j <= r) ? val : 0.f;
+                                    for (int c = 0; c < 4; ++c) {
+                                        const int e = 4 * e4 + c, j = j0 + e;
+                                        const float val = __uint_as_float(v[e]) * ex2_approx(gr - gjs[c]);
+                                        f[e] = (j <= r) ? val : 0.f;
+                                    }
                                 }
                             }
-                        }
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+                            for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+                        }
+                        tmem_st8(tp + 8 * blk, pk);
                     }
-                    tmem_st8(tp + 8 * blk, pk);
+                    tmem_st_wait();
+                    // the MMA warp issues the next CB right after kPReady: one thread checks that its
+                    // C and B tiles have landed (the stage cannot be reloaded before this arrival)
+                    if (kCBS > 1 && storer && qp + 1 < nq &&
+                        !mbar_wait(smem_u32(&bars[kFull0 + (qp + 1) % kCBS]), ((qp + 1) / kCBS) & 1, kWaitNs)) {
+                        ok = false; set_error(err, 1);
+                    }
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&bars[kPReady]));
                 }
-                tmem_st_wait();
-                // the MMA warp issues the next CB right after kPReady: one thread checks that its
-                // C and B tiles have landed (the stage cannot be reloaded before this arrival)
-                if (storer && q + 1 < nq &&
-                    !mbar_wait(smem_u32(&bars[kFull0 + (q + 1) % kCBS]), ((q + 1) / kCBS) & 1, kWaitNs)) {
-                    ok = false; set_error(err, 1);
-                }
-                tc_fence_before();
-                mbar_arrive(smem_u32(&bars[kPReady]));
             }
             // y = 2^(G_i - G_base) Ys + Yi   (Yi already holds D x; this thread: 32 columns).
             // y is staged in this sub-chunk's x slot (its last reader, the Yi MMA, has completed)
             // in the same swizzled [t][p] layout, then written by one bulk tensor store.
+            const int64_t t0 = t_begin + (int64_t)q * kQ;
+            const int xs = (q + kXS) % kXS;
+            const float gr = gr_y, gbase = gbase_y;
             uint8_t *ystage = smem + Cfg::kX + xs * kAtom;
-            if (ok && !mbar_wait(smem_u32(&bars[kIntra]), q & 1, kWaitNs)) { ok = false; set_error(err, 1); }
-            if (ok) {
+            if (q >= 0 && ok && !mbar_wait(smem_u32(&bars[kIntra0 + (q & 1)]), (q >> 1) & 1, kWaitNs)) {
+                ok = false; set_error(err, 1);
+            }
+            if (q >= 0 && ok) {
                 tc_fence_after();
                 const float eg = ex2_approx(gr - gbase);
                 const uint32_t c0 = 32 * half;
@@ -846,7 +869,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             }
             // all rows staged (and the column arrays free for the next sub-chunk)
             group_sync();
-            if (storer) {
+            if (storer && q >= 0) {
                 // the store of sub-chunk q stays in flight; the slot of sub-chunk q - 1 is
                 // released once its store has read it
                 if (ok) {
@@ -856,6 +879,8 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 bulk_wait_read_1();
                 if (q > 0) mbar_arrive(smem_u32(&bars[kYSt0 + (q - 1) % kXS]));
             }
+            gr_y = gr_p;
+            gbase_y = gbase_p;
         }
         if (storer) {
             bulk_wait_all();
