@@ -119,7 +119,8 @@ int device_sms()
 int choose_chunks_per_super(const Problem &pr, double sms)
 {
     const double es = (double)esize(pr.in_dt);
-    const double units1 = (double)(pr.B * pr.nh * (pr.H / 64));
+    // scan CTAs of one super-chunk over all sequences
+    const double units1 = (double)(pr.B * pr.nh * (pr.H / 64)) / ssd::scan_seqs_per_cta(pr);
     const double x_bytes = (double)(pr.B * pr.L * pr.nh * pr.H) * es;
     const double bc_bytes = (double)(pr.B * pr.L * pr.G * pr.S) * es;
     const double alg = 2.0 * x_bytes + 2.0 * bc_bytes;
@@ -152,20 +153,24 @@ int choose_chunks_per_super(const Problem &pr, double sms)
 ssd::ScanSplit choose_tc_plan(const Problem &pr)
 {
     const int64_t sms = device_sms();
-    const int64_t nseq = pr.B * pr.nh, npb = pr.H / 64;
+    // a scan "row" is the spc sequences one CTA walks together (two heads of a group, or one)
+    const int64_t spc = ssd::scan_seqs_per_cta(pr);
+    const int64_t nseq = pr.B * pr.nh, npb = spc == 2 ? 1 : pr.H / 64;   // CTAs per row and super-chunk
     const int R = choose_chunks_per_super(pr, (double)sms);
     const int nsup = (int)((pr.nc + R - 1) / R);
     ssd::ScanSplit sp{nseq, R, nsup, R, nsup, 1, nseq * nsup};
-    const int64_t per_seq = (int64_t)nsup * npb;             // scan CTAs per sequence
-    const int64_t ctas = nseq * per_seq;
+    const int64_t per_row = (int64_t)nsup * npb;             // scan CTAs per row
+    const int64_t ctas = nseq / spc * per_row;
     const int64_t last = ctas % sms;                          // CTAs in the last, partial wave
     if (ctas <= sms || last == 0 || 3 * last >= sms) return sp;
-    const int64_t align = ssd::state_heads_per_cta(pr);
-    int64_t tail = (last + per_seq - 1) / per_seq;            // sequences of the last wave
+    // the tail is whole chunk_state head groups and whole scan rows (both powers of two)
+    const int64_t sh = ssd::state_heads_per_cta(pr);
+    const int64_t align = sh > spc ? sh : spc;
+    int64_t tail = (last + per_row - 1) / per_row * spc;      // sequences of the last wave
     tail = (tail + align - 1) / align * align;
     if (tail >= nseq) return sp;
     // the tail's chunks over all SMs, at least one chunk per super-chunk
-    const int64_t tail_chunks = tail * (int64_t)pr.nc * npb;
+    const int64_t tail_chunks = tail / spc * (int64_t)pr.nc * npb;
     int R1 = (int)((tail_chunks + sms - 1) / sms);
     if (R1 < 1) R1 = 1;
     if (R1 >= R) return sp;

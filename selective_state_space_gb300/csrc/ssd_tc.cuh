@@ -37,6 +37,10 @@ struct ScanSplit {
     int64_t base1;
 };
 
+// Sequences per scan CTA: 2 (two heads of one B/C group) when S = 128, H = 64 and the
+// heads per group are even, else 1.  With 2, both parts of a ScanSplit hold whole pairs.
+int scan_seqs_per_cta(const Problem &pr);
+
 // Output y for every super-chunk of `sp`; the last super-chunk of each sequence also
 // writes h_final when it is not NULL.
 cudaError_t launch_chunk_scan_tc(const Problem &pr, const void *x, const void *dt, const void *Bm,

@@ -49,6 +49,8 @@ SMALL = [
     workloads.custom(1, 640, 4, 64, 128, 1, 128, "bf16", h0_recipe="normal", seed=14, name="blog-small"),
     workloads.custom(1, 256, 2, 128, 128, 1, 256, "bf16", seed=17, name="h128-s128"),
     workloads.custom(1, 256, 2, 64, 256, 1, 128, "bf16", seed=18, name="h64-s256"),
+    # three heads per group: the one-head-per-CTA scan kernel at S = 128, H = 64
+    workloads.custom(2, 512, 6, 64, 128, 2, 256, "bf16", h0_recipe="normal", seed=19, name="odd-hpg"),
     workloads.custom(2, 77, 6, 8, 16, 3, 16, "f32", h0_recipe="normal", seed=15, name="odd-f32"),
     workloads.custom(1, 33, 2, 1, 1, 1, 1, "f32", seed=16, name="scalar-T1"),
 ]
