@@ -28,6 +28,31 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(v);
 }
 
+// Programmatic dependent launch.  The kernels after the cumsum are launched with
+// programmatic stream serialisation (launch_pdl): each lets the next kernel of the
+// stream start its launch and prologue early (pdl_trigger) and waits for the previous
+// kernel's results, with their memory visible, before reading them (pdl_wait).  Both
+// instructions are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // A run of sequences, i.e. (batch, head) pairs in b * nh + h order: [lo, lo + n).
 // The chunk_state and state_passing stages work on one run at a time; their
 // per-super-chunk states for sequence bh and super-chunk m sit at index

@@ -35,6 +35,7 @@ k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *_
     extern __shared__ float tile[];   // [T][33] in-run cumsum, then (dtT only) [T][33] dt
     __shared__ float run_sum[32][33]; // [run][head] run totals (T <= 1024: at most 32 runs)
     __shared__ float run_off[32][33]; // [run][head] sum of the totals of the runs before
+    pdl_trigger();                    // the next kernel may launch; it waits for this one's G
     const int k = blockIdx.x, hbase = blockIdx.y * 32, b = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t0 = (int64_t)k * T;
@@ -183,6 +184,8 @@ k_state_passing(const float *__restrict__ G, const float *__restrict__ s_local,
     constexpr int kBatch = 8;                     // states loaded together (independent loads)
     constexpr int kWin = 1024;                    // super-chunks whose decays are staged at once
     __shared__ float sdec[kWin];                  // exp2 of each super-chunk's total log2 decay
+    pdl_trigger();
+    pdl_wait();                                   // G and s_local come from the kernels before
     const int64_t HS = pr.H * pr.S;
     const int64_t e = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * VEC;
     const bool active = e < HS;
@@ -518,10 +521,10 @@ cudaError_t launch_state_passing(const Problem &pr, SeqRange seqs, const float *
     const int vec = v4 ? 4 : 1;
     dim3 grid((unsigned)((HS / vec + 255) / 256), (unsigned)(seqs.n < 65535 ? seqs.n : 65535));
     if (v4)
-        k_state_passing<4><<<grid, 256, 0, st>>>(G, s_local, h0, h_start, h_final, pr, seqs, R, nsup, nm);
-    else
-        k_state_passing<1><<<grid, 256, 0, st>>>(G, s_local, h0, h_start, h_final, pr, seqs, R, nsup, nm);
-    return cudaGetLastError();
+        return launch_pdl(k_state_passing<4>, grid, dim3(256), 0, st, G, s_local, h0, h_start, h_final, pr, seqs, R,
+                          nsup, nm);
+    return launch_pdl(k_state_passing<1>, grid, dim3(256), 0, st, G, s_local, h0, h_start, h_final, pr, seqs, R, nsup,
+                      nm);
 }
 
 template <typename Tin, typename Tout>

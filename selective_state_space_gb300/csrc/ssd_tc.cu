@@ -178,6 +178,9 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    // the next kernel may launch now; this one reads G (and the states) of the kernels before
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -476,6 +479,9 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    // the next kernel may launch now; this one reads G (and the states) of the kernels before
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         // ---- TMA producer ---------------------------------------------------------------
@@ -1016,6 +1022,9 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    // the next kernel may launch now; this one reads G (and the states) of the kernels before
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         // ---- C and B tiles (one stage: free once CB, the update and C h^T have read it) -------
@@ -1569,9 +1578,8 @@ cudaError_t state_launch(const Problem &pr, SeqRange seqs, const void *x, const 
         e = cudaMemsetAsync(s_out, 0, (size_t)(seqs.n * nsup) * (size_t)(pr.H * pr.S) * sizeof(float), st);
         if (e != cudaSuccess) return e;
     }
-    kern<<<(unsigned)grid, 192, Cfg::kSmem, st>>>(mB, mX, G, (const __nv_bfloat16 *)dt, dtT, s_out, pr,
-                                                   seqs.lo / HG, seqs.n / HG, R, nsup, nm, err);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(192), Cfg::kSmem, st, mB, mX, G, (const __nv_bfloat16 *)dt,
+                      dtT, s_out, pr, (int64_t)(seqs.lo / HG), (int64_t)(seqs.n / HG), R, nsup, nm, err);
 }
 
 template <int S>
@@ -1590,9 +1598,8 @@ cudaError_t scan_launch(const Problem &pr, const void *x, const void *dt, const 
     const int64_t grid = (sp.split * sp.nsup0 + (pr.B * pr.nh - sp.split) * sp.nsup1) * (pr.H / kPB);
     if (grid == 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kern<<<(unsigned)grid, 448, Cfg::kSmem, st>>>(mC, mB, mX, mY, G, (const __nv_bfloat16 *)dt, D, h0,
-                                        h_start, h_final, (__nv_bfloat16 *)y, pr, sp, err);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(448), Cfg::kSmem, st, mC, mB, mX, mY, G,
+                      (const __nv_bfloat16 *)dt, D, h0, h_start, h_final, (__nv_bfloat16 *)y, pr, sp, err);
 }
 
 cudaError_t scan_pair_launch(const Problem &pr, const void *x, const void *dt, const void *Bm, const void *Cm,
@@ -1611,9 +1618,8 @@ cudaError_t scan_pair_launch(const Problem &pr, const void *x, const void *dt, c
     const int64_t grid = (sp.split / 2) * sp.nsup0 + ((pr.B * pr.nh - sp.split) / 2) * sp.nsup1;
     if (grid == 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-    k_chunk_scan_pair<<<(unsigned)grid, PairCfg::kThreads, PairCfg::kSmem, st>>>(
-        mC, mB, mX, mY, G, (const __nv_bfloat16 *)dt, D, h0, h_start, h_final, pr, sp, err);
-    return cudaGetLastError();
+    return launch_pdl(k_chunk_scan_pair, dim3((unsigned)grid), dim3(PairCfg::kThreads), PairCfg::kSmem, st, mC, mB,
+                      mX, mY, G, (const __nv_bfloat16 *)dt, D, h0, h_start, h_final, pr, sp, err);
 }
 
 }  // namespace
