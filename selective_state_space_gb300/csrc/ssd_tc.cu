@@ -924,8 +924,9 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
 // float32x2 elsewhere): it is the bulk of the issued instructions.  Scaling C h^T in place before P x
 // accumulates onto it lets one accumulator per sub-chunk hold y, so two of them fit in
 // TMEM and the next sub-chunk's C h^T never waits for this one's epilogue.
-// MMA issue order per sub-chunk: update, C h^T, P x, next CB.  The state chain (update ->
-// hand-off -> w o x -> update) waits on nothing else.
+// MMA issue order per sub-chunk: C h^T, update, P x, next CB.  The state chain (update ->
+// hand-off -> w o x -> update) waits on nothing else, and the C/B stage is free for the
+// next tiles once the update has read it.
 // TMEM (512 columns): CB / P 0..127, Y buffers 128..255 and 256..383 (sub-chunk q in
 // buffer q % 2; head A then head B), state 384..511 (h_A^T then h_B^T; lanes = s).
 // Shared memory: one C/B stage, x in a 3-slot ring (the slots also stage y for its bulk
@@ -1102,18 +1103,10 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
                 for (int q = 0; q < nq; ++q) {
                     const int xs = q % kXS;
                     const uint32_t ty = tmem + Cfg::kTy + (uint32_t)(q & 1) * 128;
-                    // update on the state the state warps decayed, with their w o x
+                    // C [h_A^T | h_B^T] into Y buffer q % 2 (drained by the epilogue of q - 2), from the
+                    // bf16 state copy of the hand-off
                     if (!mbar_wait(smem_u32(&bars[pHReady]), q & 1, kWaitNs) ||
-                        !mbar_wait(smem_u32(&bars[pXReady]), q & 1, kWaitNs)) { ok = false; break; }
-                    tc_fence_after();
-                    if (q + 1 < nq || write_final) {
-#pragma unroll
-                        for (int kk = 0; kk < kQ / 16; ++kk)
-                            mma_bf16(tmem + Cfg::kTst, adv(dBm, kk * 2048), adv(dWx, kk * 2048), id_up, 1u);
-                        mma_commit(smem_u32(&bars[pUpdate]));
-                    }
-                    // C [h_A^T | h_B^T] into Y buffer q % 2 (drained by the epilogue of q - 2)
-                    if (q >= 2 && !mbar_wait(smem_u32(&bars[pEpi0 + (q & 1)]), ((q - 2) >> 1) & 1, kWaitNs)) {
+                        (q >= 2 && !mbar_wait(smem_u32(&bars[pEpi0 + (q & 1)]), ((q - 2) >> 1) & 1, kWaitNs))) {
                         ok = false; break;
                     }
                     tc_fence_after();
@@ -1123,7 +1116,16 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
                         mma_bf16(ty, adv(dC, off), adv(dHc, kk * 2048), id_ys, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(smem_u32(&bars[pYs]));
-                    mma_commit(smem_u32(&bars[pFree]));      // CB, the update and C h^T have read C and B
+                    // update on the state the state warps decayed, with their w o x
+                    if (!mbar_wait(smem_u32(&bars[pXReady]), q & 1, kWaitNs)) { ok = false; break; }
+                    tc_fence_after();
+                    if (q + 1 < nq || write_final) {
+#pragma unroll
+                        for (int kk = 0; kk < kQ / 16; ++kk)
+                            mma_bf16(tmem + Cfg::kTst, adv(dBm, kk * 2048), adv(dWx, kk * 2048), id_up, 1u);
+                        mma_commit(smem_u32(&bars[pUpdate]));
+                    }
+                    mma_commit(smem_u32(&bars[pFree]));      // CB, C h^T and the update have read C and B
                     // Y_h += P_h x_h (P from TMEM) once P is built and C h^T scaled
                     if (!mbar_wait(smem_u32(&bars[pPReady]), q & 1, kWaitNs)) { ok = false; break; }
                     tc_fence_after();
@@ -1171,11 +1173,10 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
             const float g0 = n_g[0], g1 = n_g[1], gl0 = n_gl[0], gl1 = n_gl[1], gb0 = n_gb[0], gb1 = n_gb[1];
             const float2 dtp = unpack_bf16x2(n_dt);
             if (q + 1 < nq) load_scalars(q + 1);
-            // the update of q - 1 has produced the state and read w o x; C h^T of q - 1 has
-            // read the bf16 copy
+            // the update of q - 1 has produced the state and read w o x (and C h^T of q - 1,
+            // issued before it, has read the bf16 copy)
             if (q > 0) {
-                if (!mbar_wait(smem_u32(&bars[pUpdate]), (q - 1) & 1, kWaitNs) ||
-                    !mbar_wait(smem_u32(&bars[pYs]), (q - 1) & 1, kWaitNs)) {
+                if (!mbar_wait(smem_u32(&bars[pUpdate]), (q - 1) & 1, kWaitNs)) {
                     ok = false; set_error(err, 1); break;
                 }
                 tc_fence_after();
@@ -1283,7 +1284,6 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
         const int half = (warp - 6) >> 2;              // columns 64 half .. 64 half + 63; C h^T of head `half`
         const int r = 32 * (warp & 3) + lane;          // TMEM lane = token row i
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const int wrow_lo = 32 * (warp & 3), wrow_hi = wrow_lo + 31;
         float *arr = (float *)(smem + Cfg::kArr);
         float *myGd = arr + half * (Cfg::kArrHead / 4);  // the arrays this thread fills (head `half`)
         float *myF = myGd + kQ, *myGe = myF + kQ;
@@ -1323,6 +1323,7 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
                 // (above the diagonal, left of every row of the warp, or meeting the diagonal).
                 // Per pair: both blocks' C B^T loaded, one wait, then P_A of each block into its
                 // first 8 columns and P_B into its last 8.
+                const int wrow_lo = 32 * (warp & 3), wrow_hi = wrow_lo + 31;
 #pragma unroll 1
                 for (int bp = 0; bp < 2; ++bp) {
                     const int j0 = 64 * half + 32 * bp;
@@ -1651,15 +1652,16 @@ int state_heads_per_cta(const Problem &pr)
 
 // Heads per chunk_state CTA for a launch over `seqs` with nm super-chunks of R chunks:
 // the most that share B tiles; for a small launch (one whole unit per CTA, see
-// state_grid) with fewer units than SMs, halved while that holds, since such a launch
-// is latency-bound and more, smaller units finish sooner.
+// state_grid), halved while the units still fit in one wave of CTAs, since such a
+// launch is latency-bound and more, smaller units finish sooner -- but a second wave
+// costs a whole unit's latency again.
 int state_launch_heads(const Problem &pr, SeqRange seqs, int R, int nm)
 {
     int hg = state_heads_per_cta(pr);
     const int64_t sms = current_sms(), nq_u = (int64_t)R * (pr.T / 64);
     while (hg > 1) {
         const int64_t units = (seqs.n / hg) * nm;
-        if (units * nq_u >= 16 * sms || units >= sms) break;
+        if (units * nq_u >= 16 * sms || 2 * units > sms) break;
         hg /= 2;
     }
     return hg;
