@@ -84,6 +84,8 @@ def stage_bytes(s: workloads.Shape, plan: dict):
     else:
         parts = [(0, nseq, 1, nc)]
     cs = sp = carried = 0.0
+    # the cumsum writes the float32 copy of dt only for the sequences chunk_state reads
+    dtT_seqs = sum(n for lo, n, R, nsup in parts if n > 0 and nsup > 1) if plan["tensor_cores"] else 0
     for lo, n, R, nsup in parts:
         if n == 0:
             continue
@@ -99,7 +101,7 @@ def stage_bytes(s: workloads.Shape, plan: dict):
         cs += frac * (n * per_seq + pairs * L * S * e) + n * nm * hs
         sp += 2 * n * nm * hs + n * nc * 4 + (n * hs if h0 else 0)
     out = {
-        "chunk_cumsum": dt + nh * 4 + g + (g if plan["tensor_cores"] else 0),   # + the float32 copy of dt
+        "chunk_cumsum": dt + nh * 4 + g + dtT_seqs * L * 4,   # + the float32 copy of dt
         "chunk_state": cs,
         "state_passing": sp,
         "chunk_scan": x + dt + 2 * bc + g + h0 + carried + nh * 4 + y + state,

@@ -5,6 +5,7 @@
 
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "ssd_common.cuh"
@@ -231,14 +232,26 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
     auto rec = [&](int i) -> bool { return !events || cudaEventRecord((cudaEvent_t)events[i], st) == cudaSuccess; };
     const bool tc = use_tensor_cores(desc, pr);
     if (cudaMemsetAsync(w.err, 0, sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
-    if (!rec(0) || ssd::launch_chunk_cumsum(pr, dt, A, w.G, tc ? w.dtT : nullptr, st) != cudaSuccess ||
+    ssd::ScanSplit sp{};
+    PlanPart parts[2];
+    // the float32 copy of dt is read by chunk_state only: the sequences of the parts it runs for
+    int64_t dtT_lo = 0, dtT_hi = 0;
+    if (tc) {
+        sp = choose_tc_plan(pr);
+        plan_parts(pr, sp, parts);
+        for (const PlanPart &p : parts) {
+            if (p.seqs.n <= 0 || p.nsup <= 1) continue;
+            if (dtT_hi == dtT_lo) { dtT_lo = p.seqs.lo; dtT_hi = p.seqs.lo + p.seqs.n; }
+            else { dtT_lo = std::min(dtT_lo, p.seqs.lo); dtT_hi = std::max(dtT_hi, p.seqs.lo + p.seqs.n); }
+        }
+    }
+    if (!rec(0) ||
+        ssd::launch_chunk_cumsum(pr, dt, A, w.G, dtT_hi > dtT_lo ? w.dtT : nullptr, dtT_lo, dtT_hi, st) !=
+            cudaSuccess ||
         !rec(1))
         return SSD_ERR_CUDA;
 
     if (tc) {
-        const ssd::ScanSplit sp = choose_tc_plan(pr);
-        PlanPart parts[2];
-        plan_parts(pr, sp, parts);
         const int64_t HS = pr.H * pr.S;
         // per part: states of super-chunks 0 .. nsup-2 (the last one's state is produced by the scan)
         if (!rec(2)) return SSD_ERR_CUDA;
@@ -409,7 +422,7 @@ ssd_status ssd_chunk_cumsum(const ssd_desc *desc, const void *dt, const float *A
     if (s != SSD_OK) return s;
     if (!nonempty(pr)) return SSD_OK;
     if (!dt || !A || !G || !aligned(G, 4) || !aligned(A, 4)) return SSD_ERR_INVALID_ARG;
-    return cuda_status(ssd::launch_chunk_cumsum(pr, dt, A, G, nullptr, (cudaStream_t)stream));
+    return cuda_status(ssd::launch_chunk_cumsum(pr, dt, A, G, nullptr, 0, 0, (cudaStream_t)stream));
 }
 
 ssd_status ssd_chunk_state(const ssd_desc *desc, const void *x, const void *dt, const void *Bm,

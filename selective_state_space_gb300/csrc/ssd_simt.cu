@@ -30,7 +30,7 @@ namespace {
 template <typename Tin>
 __global__ void __launch_bounds__(256)
 k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *__restrict__ G,
-               float *__restrict__ dtT, int64_t L, int nh, int T)
+               float *__restrict__ dtT, int64_t dtT_lo, int64_t dtT_hi, int64_t L, int nh, int T)
 {
     extern __shared__ float tile[];   // [T][33] in-run cumsum, then (dtT only) [T][33] dt
     __shared__ float run_sum[32][33]; // [run][head] run totals (T <= 1024: at most 32 runs)
@@ -88,8 +88,9 @@ k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *_
         if (hh >= nh) continue;
         float *dst = G + ((int64_t)b * nh + hh) * L + t0;
         for (int t = lane; t < n; t += 32) dst[t] = (tile[t * 33 + j] + run_off[t >> 5][j]) * kLog2e;
-        if (dtT) {
-            float *dd = dtT + ((int64_t)b * nh + hh) * L + t0;
+        const int64_t bh = (int64_t)b * nh + hh;
+        if (dtT && bh >= dtT_lo && bh < dtT_hi) {
+            float *dd = dtT + bh * L + t0;
             for (int t = lane; t < n; t += 32) dd[t] = tile[(T + t) * 33 + j];
         }
     }
@@ -183,7 +184,10 @@ k_state_passing(const float *__restrict__ G, const float *__restrict__ s_local,
     using V = typename std::conditional<VEC == 4, float4, float>::type;
     constexpr int kBatch = 8;                     // states loaded together (independent loads)
     constexpr int kWin = 1024;                    // super-chunks whose decays are staged at once
+    constexpr int kTile = 256;                    // chunk-end G values loaded together (= block size)
     __shared__ float sdec[kWin];                  // exp2 of each super-chunk's total log2 decay
+    __shared__ float sdl[kWin];                   // the total log2 decays, summed tile by tile
+    __shared__ float sgl[kTile];                  // G at the end of each chunk of the tile
     pdl_trigger();
     pdl_wait();                                   // G and s_local come from the kernels before
     const int64_t HS = pr.H * pr.S;
@@ -203,13 +207,27 @@ k_state_passing(const float *__restrict__ G, const float *__restrict__ s_local,
         const int64_t base = rel * nsup * HS + e;
         for (int w0 = 0; w0 < nsup; w0 += kWin) {
             const int w1 = min(nsup, w0 + kWin);
+            // each super-chunk's log2 decay is the sum of its chunks' last G values, added in
+            // chunk order; the chunk values are loaded a tile at a time by the whole block
             __syncthreads();                          // the previous window's decays are no longer read
-            for (int m = w0 + threadIdx.x; m < min(w1, nm); m += blockDim.x) {
-                float dec = 0.f;
-                const int k1 = min((int)pr.nc, (m + 1) * R);
-                for (int k = m * R; k < k1; ++k) dec += Gh[min(pr.L, (int64_t)(k + 1) * pr.T) - 1];
-                sdec[m - w0] = exp2f(dec);
+            const int wm = min(w1, nm);
+            for (int m = w0 + threadIdx.x; m < wm; m += blockDim.x) sdl[m - w0] = 0.f;
+            const int64_t c_end = min((int64_t)pr.nc, (int64_t)wm * R);
+            for (int64_t c0 = (int64_t)w0 * R; c0 < c_end; c0 += kTile) {
+                __syncthreads();
+                const int64_t c = c0 + threadIdx.x;
+                sgl[threadIdx.x] = c < c_end ? Gh[min(pr.L, (c + 1) * pr.T) - 1] : 0.f;
+                __syncthreads();
+                for (int m = w0 + threadIdx.x; m < wm; m += blockDim.x) {
+                    const int64_t k_lo = max((int64_t)m * R, c0);
+                    const int64_t k_hi = min(min((int64_t)(m + 1) * R, c0 + kTile), c_end);
+                    float acc = sdl[m - w0];
+                    for (int64_t k = k_lo; k < k_hi; ++k) acc += sgl[k - c0];
+                    sdl[m - w0] = acc;
+                }
             }
+            __syncthreads();
+            for (int m = w0 + threadIdx.x; m < wm; m += blockDim.x) sdec[m - w0] = exp2f(sdl[m - w0]);
             __syncthreads();
             if (!active) continue;
             for (int m0 = w0; m0 < w1; m0 += kBatch) {
@@ -478,7 +496,7 @@ size_t scan_smem_bytes(const Problem &pr)
 }  // namespace
 
 cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *A, float *G,
-                                float *dtT, cudaStream_t st)
+                                float *dtT, int64_t dtT_lo, int64_t dtT_hi, cudaStream_t st)
 {
     dim3 grid((unsigned)pr.nc, (unsigned)((pr.nh + 31) / 32), (unsigned)pr.B);
     const size_t smem = sizeof(float) * 33 * (size_t)pr.T * (dtT ? 2 : 1);
@@ -486,11 +504,11 @@ cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *
     if (pr.in_dt == SSD_BF16) {
         auto kern = k_chunk_cumsum<__nv_bfloat16>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
-        kern<<<grid, 256, smem, st>>>((const __nv_bfloat16 *)dt, A, G, dtT, pr.L, (int)pr.nh, (int)pr.T);
+        kern<<<grid, 256, smem, st>>>((const __nv_bfloat16 *)dt, A, G, dtT, dtT_lo, dtT_hi, pr.L, (int)pr.nh, (int)pr.T);
     } else {
         auto kern = k_chunk_cumsum<float>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
-        kern<<<grid, 256, smem, st>>>((const float *)dt, A, G, dtT, pr.L, (int)pr.nh, (int)pr.T);
+        kern<<<grid, 256, smem, st>>>((const float *)dt, A, G, dtT, dtT_lo, dtT_hi, pr.L, (int)pr.nh, (int)pr.T);
     }
     return cudaGetLastError();
 }
