@@ -147,6 +147,13 @@ __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk
 // Wait until all committed bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Prefetch `bytes` (a multiple of 16) from global memory into L2, 16-byte aligned.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 // Prefetch a 4-D tensor box into L2 (no shared-memory destination, no completion).
 __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3)
 {

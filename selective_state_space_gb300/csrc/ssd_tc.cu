@@ -307,20 +307,22 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
 #pragma unroll
                     for (int hh = 0; hh < HG; ++hh) wr[hh] = dtr[hh] * exp2f(lw[hh] - gr[hh]);
                     uint8_t *xt = smem + st * Cfg::kStage + Cfg::kBBytes;
+                    // w rounded to bf16 and the products taken in bf16 pairs (they are MMA operands,
+                    // rounded to bf16 either way)
 #pragma unroll
                     for (int a = 0; a < kN / 64; ++a) {
-                        const float w = wr[a / (H / 64)];
+                        const __nv_bfloat162 w2 = __float2bfloat162_rn(wr[a / (H / 64)]);
+                        uint4 v[4];
 #pragma unroll
-                        for (int c = xc0; c < xc0 + 4; ++c) {
-                            uint4 *p = (uint4 *)(xt + a * Cfg::kAtomT + sw128(xr, c));
-                            uint4 v = *p;
-                            float2 f0 = unpack_bf16x2(v.x), f1 = unpack_bf16x2(v.y), f2 = unpack_bf16x2(v.z),
-                                   f3 = unpack_bf16x2(v.w);
-                            v.x = pack_bf16x2(f0.x * w, f0.y * w);
-                            v.y = pack_bf16x2(f1.x * w, f1.y * w);
-                            v.z = pack_bf16x2(f2.x * w, f2.y * w);
-                            v.w = pack_bf16x2(f3.x * w, f3.y * w);
-                            *p = v;
+                        for (int c = 0; c < 4; ++c) v[c] = *(const uint4 *)(xt + a * Cfg::kAtomT + sw128(xr, xc0 + c));
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint4 o;
+                            o.x = mul_bf16x2(v[c].x, w2);
+                            o.y = mul_bf16x2(v[c].y, w2);
+                            o.z = mul_bf16x2(v[c].z, w2);
+                            o.w = mul_bf16x2(v[c].w, w2);
+                            *(uint4 *)(xt + a * Cfg::kAtomT + sw128(xr, xc0 + c)) = o;
                         }
                     }
                     fence_proxy_async_smem();
@@ -1057,6 +1059,15 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
     } else if (warp == 14) {
         // ---- x tiles of both heads (slot of sub-chunk q: free once y of q - 3 is stored) ------
         if (lane == 0) {
+            // the entering states of both heads into L2 first: the first hand-off reads them
+            // with strided loads, one head after the other
+            for (int hh = 0; hh < 2; ++hh) {
+                const float *src = (m < sp.hs_from) ? (h0 ? h0 + (int64_t)(bhA + hh) * (pr.H * S) : nullptr)
+                                                    : h_start + (hs_idx + hh * nsup) * (int64_t)(pr.H * S);
+                // (h0 need only be 4-byte aligned; a bulk prefetch needs 16)
+                if (src && nq > 0 && ((uintptr_t)src & 15u) == 0)
+                    bulk_prefetch_l2(src, (uint32_t)(pr.H * S * sizeof(float)));
+            }
             prefetch_tmap(&tmX);
             for (int q = 0; q < nq; ++q) {
                 const int t0 = (int)(t_begin + (int64_t)q * kQ);
