@@ -1195,10 +1195,11 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
             // state (float32, TMEM) -> bf16 copy [s][p] for C h^T, and the state times
             // 2^(G_last - G_base) back to TMEM for the update to accumulate on
 #pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
+            for (int hc32 = 0; hc32 < 4; ++hc32) {             // head hc32 / 2, columns 32 (hc32 % 2) ..
+                const int hh = hc32 >> 1, c32 = 32 * (hc32 & 1);
                 const float dec = exp2f(hh ? gl1 - gb1 : gl0 - gb0);
-                const uint32_t ta = tmem + lane_base + Cfg::kTst + 64 * hh;
-                uint32_t v[64];
+                const uint32_t ta = tmem + lane_base + Cfg::kTst + 64 * hh + c32;
+                uint32_t v[32];
                 if (q == 0) {
                     // entering state: h0 (zeros if absent) for super-chunks m < hs_from, else h_start
                     const float *src = (m < sp.hs_from)
@@ -1206,30 +1207,28 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
                                            : h_start + (hs_idx + hh * nsup) * (int64_t)(pr.H * S);
                     if (src) {
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) v[j] = __float_as_uint(src[(int64_t)j * S + r]);
+                        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(src[(int64_t)(c32 + j) * S + r]);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) v[j] = 0u;
+                        for (int j = 0; j < 32; ++j) v[j] = 0u;
                     }
                 } else {
                     tmem_ld16(ta + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
                     tmem_ld16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-                    tmem_ld16(ta + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
-                    tmem_ld16(ta + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
                     tmem_ld_wait();
                 }
                 uint8_t *hrow = hc + hh * kAtom;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint4 o;
                     o.x = pack_bf16x2(__uint_as_float(v[8 * c + 0]), __uint_as_float(v[8 * c + 1]));
                     o.y = pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3]));
                     o.z = pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5]));
                     o.w = pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7]));
-                    *(uint4 *)(hrow + sw128(r, c)) = o;
+                    *(uint4 *)(hrow + sw128(r, (c32 >> 3) + c)) = o;
                 }
 #pragma unroll
-                for (int j = 0; j < 64; j += 2) {
+                for (int j = 0; j < 32; j += 2) {
                     const float2 d2 = __fmul2_rn(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
                                                  make_float2(dec, dec));
                     v[j] = __float_as_uint(d2.x);
@@ -1237,8 +1236,6 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
                 }
                 tmem_st16(ta + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
                 tmem_st16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-                tmem_st16(ta + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
-                tmem_st16(ta + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
             }
             tmem_st_wait();
             fence_proxy_async_smem();
@@ -1350,11 +1347,11 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
                     tmem_ld16(tcb + j0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
                     tmem_ld16(tcb + j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                     tmem_ld_wait();
-                    uint32_t pk[32];
                     if (j0 + 31 < wrow_lo) {                       // left of every row of the warp: factored
 #pragma unroll
                         for (int k2 = 0; k2 < 2; ++k2) {
                             const int jb = j0 + 16 * k2;
+                            uint32_t pk[16];
                             const float eA = ex2_approx(g0 - GeA[jb >> 4]);
                             const float eB = ex2_approx(g1 - GeB[jb >> 4]);
                             const float4 *fa = reinterpret_cast<const float4 *>(FA + jb);
@@ -1370,16 +1367,18 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
                                 const float2 pA23 = __fmul2_rn(__fmul2_rn(v23, make_float2(eA, eA)), make_float2(a.z, a.w));
                                 const float2 pB01 = __fmul2_rn(__fmul2_rn(v01, make_float2(eB, eB)), make_float2(c.x, c.y));
                                 const float2 pB23 = __fmul2_rn(__fmul2_rn(v23, make_float2(eB, eB)), make_float2(c.z, c.w));
-                                pk[16 * k2 + 2 * e4] = pack_bf16x2(pA01.x, pA01.y);
-                                pk[16 * k2 + 2 * e4 + 1] = pack_bf16x2(pA23.x, pA23.y);
-                                pk[16 * k2 + 8 + 2 * e4] = pack_bf16x2(pB01.x, pB01.y);
-                                pk[16 * k2 + 8 + 2 * e4 + 1] = pack_bf16x2(pB23.x, pB23.y);
+                                pk[2 * e4] = pack_bf16x2(pA01.x, pA01.y);
+                                pk[2 * e4 + 1] = pack_bf16x2(pA23.x, pA23.y);
+                                pk[8 + 2 * e4] = pack_bf16x2(pB01.x, pB01.y);
+                                pk[8 + 2 * e4 + 1] = pack_bf16x2(pB23.x, pB23.y);
                             }
+                            tmem_st16(tcb + jb, pk);
                         }
                     } else {                                       // meets the diagonal: exact, selected
 #pragma unroll
                         for (int k2 = 0; k2 < 2; ++k2) {
                             const int jb = j0 + 16 * k2;
+                            uint32_t pk[16];
                             const float4 *da = reinterpret_cast<const float4 *>(GdA + jb);
                             const float4 *db = reinterpret_cast<const float4 *>(GdB + jb);
 #pragma unroll
@@ -1396,15 +1395,14 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
                                     pa[e] = (j <= r) ? xa : 0.f;
                                     pb[e] = (j <= r) ? xb : 0.f;
                                 }
-                                pk[16 * k2 + 2 * e4] = pack_bf16x2(pa[0], pa[1]);
-                                pk[16 * k2 + 2 * e4 + 1] = pack_bf16x2(pa[2], pa[3]);
-                                pk[16 * k2 + 8 + 2 * e4] = pack_bf16x2(pb[0], pb[1]);
-                                pk[16 * k2 + 8 + 2 * e4 + 1] = pack_bf16x2(pb[2], pb[3]);
+                                pk[2 * e4] = pack_bf16x2(pa[0], pa[1]);
+                                pk[2 * e4 + 1] = pack_bf16x2(pa[2], pa[3]);
+                                pk[8 + 2 * e4] = pack_bf16x2(pb[0], pb[1]);
+                                pk[8 + 2 * e4 + 1] = pack_bf16x2(pb[2], pb[3]);
                             }
+                            tmem_st16(tcb + jb, pk);
                         }
                     }
-                    tmem_st16(tcb + j0, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                    tmem_st16(tcb + j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
                 }
                 // C h^T of head `half`, row r: Y <- 2^(G_i - G_base) Y before P x accumulates onto it
                 if (!mbar_wait(smem_u32(&bars[pYs]), q & 1, kWaitNs)) { ok = false; set_error(err, 1); }
