@@ -1483,21 +1483,19 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
             // all rows staged (every epilogue thread reaches this, errors or not)
             named_bar_sync(2, 128);
             if (storer) {
-                // the store of q stays in flight; the slot of q - 1 is released once its store has read it
+                // the slot goes back to the x loader as soon as the store has read it (the x load
+                // for three sub-chunks ahead then has a whole period to land)
                 if (ok) {
                     const int t0 = (int)(t_begin + (int64_t)q * kQ);
                     tma_store_4d(&tmY, smem_u32(ystage), 0, hA, t0, b);
                     tma_store_4d(&tmY, smem_u32(ystage + kAtom), 0, hA + 1, t0, b);
                     bulk_commit();
                 }
-                bulk_wait_read_1();
-                if (q >= 1) mbar_arrive(smem_u32(&bars[pYSt0 + (q - 1) % kXS]));
+                bulk_wait_read();
+                mbar_arrive(smem_u32(&bars[pYSt0 + xs]));
             }
         }
-        if (storer) {
-            bulk_wait_all();
-            if (nq > 0) mbar_arrive(smem_u32(&bars[pYSt0 + (nq - 1) % kXS]));
-        }
+        if (storer) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
