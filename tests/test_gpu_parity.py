@@ -214,3 +214,22 @@ def test_decode_step_f32_large_batch():
     y_or, h_or = oracle.ssd_step(inp.x[:, 0], inp.dt[:, 0], inp.A, inp.B[:, 0], inp.C[:, 0], inp.D, inp.h0)
     torch.cuda.synchronize()
     assert rel_max_err(y, y_or) <= 1e-5 and rel_max_err(h, h_or) <= 1e-5
+
+
+@pytest.mark.parametrize("dt_hot", [0.24, 1.0], ids=["decay-2^83-per-block", "decay-2^346-per-block"])
+def test_fast_decay_blocks(dt_hot):
+    """Runs of tokens whose 16-token blocks decay by 2^83 and 2^346 (dt = 0.24 and 1 with A
+    near -16): the scan's factored decays must stay finite (no factor above 1 may be formed
+    from a block's decay) and the masked entries must stay exactly zero."""
+    shape = workloads.custom(2, 768, 4, 64, 128, 1, 256, "bf16", a_range=(14.0, 16.0), h0_recipe="normal",
+                             seed=21, name="fast-decay")
+    inp = workloads.make_inputs(shape)
+    dt = inp.dt.float()
+    dt[:, 100:180, :] = dt_hot          # spans two sub-chunks and a chunk boundary's neighbourhood
+    dt[1, 300:310, 1] = dt_hot
+    inp.dt = dt.to(inp.dt.dtype).contiguous()
+    assert tc_path(shape)
+    y_ref, hf_ref = oracle_full(inp)
+    y, hf = run_fwd(inp)
+    assert rel_max_err(y, y_ref) <= TOL["bf16"]
+    assert rel_max_err(hf, hf_ref) <= TOL["bf16"]
