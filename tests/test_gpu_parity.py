@@ -233,3 +233,46 @@ def test_fast_decay_blocks(dt_hot):
     y, hf = run_fwd(inp)
     assert rel_max_err(y, y_ref) <= TOL["bf16"]
     assert rel_max_err(hf, hf_ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("shape", [
+    workloads.custom(2, 1024, 6, 64, 128, 1, 256, "bf16", h0_recipe="normal", seed=22, name="pair-h0"),
+    workloads.custom(1, 2048, 4, 64, 128, 2, 128, "bf16", seed=23, name="pair-g2"),
+    workloads.custom(2, 512, 6, 64, 128, 2, 256, "bf16", h0_recipe="normal", seed=24, name="single-hpg3"),
+], ids=lambda s: s.name)
+def test_without_final_state(shape):
+    """Without h_final the scan skips the state update of each sequence's last sub-chunk:
+    y must not change (bit for bit), on both tensor-core scan kernels."""
+    inp = workloads.make_inputs(shape)
+    d = to_dev(inp)
+    y1, hf = api.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], shape.chunk, d["h0"], check_errors=True)
+    y2, none = api.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], shape.chunk, d["h0"],
+                           want_h_final=False, check_errors=True)
+    torch.cuda.synchronize()
+    assert none is None
+    assert torch.equal(y1, y2)
+    y_ref, hf_ref = oracle_full(inp)
+    assert rel_max_err(y1, y_ref) <= TOL["bf16"]
+    assert rel_max_err(hf, hf_ref) <= TOL["bf16"]
+
+
+def test_plan_cuts_a_tail_for_the_pair_scan():
+    """A layer whose head pairs leave a nearly empty last wave of scan CTAs: the plan cuts the
+    last pairs into short super-chunks (chunk_state and state_passing for those sequences only),
+    and the result still matches the oracle on sampled (batch, head) pairs of both parts."""
+    shape = workloads.custom(4, 2048, 80, 64, 128, 1, 256, "bf16", h0_recipe="normal", seed=25, name="tail-cut")
+    inp = workloads.make_inputs(shape)
+    d = to_dev(inp)
+    plan = api.fwd_plan(api.desc_for(d["x"], d["B"], shape.chunk))
+    nseq = shape.batch * shape.nheads
+    if plan["split_sequences"] >= nseq:
+        pytest.skip("this GPU's SM count leaves no nearly empty last wave for this shape")
+    assert plan["split_sequences"] % 2 == 0
+    y, hf = run_fwd(inp)
+    split = plan["split_sequences"]
+    pairs = [(0, 0), ((split - 1) // shape.nheads, (split - 1) % shape.nheads),
+             (split // shape.nheads, split % shape.nheads), (shape.batch - 1, shape.nheads - 1)]
+    ref = oracle_pairs(inp, pairs)
+    for (b, h), (yr, hr) in ref.items():
+        assert rel_max_err(y[b, :, h], yr) <= TOL["bf16"], (b, h)
+        assert rel_max_err(hf[b, h], hr) <= TOL["bf16"], (b, h)
