@@ -131,7 +131,13 @@ ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan);
  *            bytes, 256-byte aligned, owned by the caller; its contents on
  *            entry are ignored and on exit are unspecified.
  * x, dt, Bm, Cm, y must be 16-byte aligned; A, D, h0, h_final 4-byte aligned.
- * y must not overlap any input.  Results are deterministic for a given input. */
+ * y must not overlap any input.  Results are deterministic for a given input,
+ * except when chunk_state splits a super-chunk between two CTAs (a plan with
+ * two memsets): the two partial states are added with float atomics, in either
+ * order, so results may differ between calls at the level of float rounding.
+ * The work is ordered on `stream` like any other stream work; inside the call
+ * the kernels after the first use programmatic dependent launch (each starts
+ * while the previous one finishes and waits for its results). */
 ssd_status ssd_fwd(const ssd_desc *desc, const void *x, const void *dt, const float *A,
                    const void *Bm, const void *Cm, const float *D, const float *h0, void *y,
                    float *h_final, void *workspace, size_t ws_bytes, ssd_stream_t stream);
