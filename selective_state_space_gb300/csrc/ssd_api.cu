@@ -234,12 +234,17 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
     if (cudaMemsetAsync(w.err, 0, sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
     ssd::ScanSplit sp{};
     PlanPart parts[2];
-    // the float32 copy of dt is read by chunk_state only: the sequences of the parts it runs for
+    // the float32 copy of dt is read by chunk_state only: the sequences of the parts it runs for.
+    // chunk_state fetches G and that copy by bulk copies of 64-token row pieces, which need
+    // 16-byte aligned starts: the rows of a sequence start at (b * nh + h) * L floats, so for L
+    // not a multiple of 4 chunk_state loads them per thread instead (no copy).
+    const bool staged = pr.L % 4 == 0;
     int64_t dtT_lo = 0, dtT_hi = 0;
     if (tc) {
         sp = choose_tc_plan(pr);
         plan_parts(pr, sp, parts);
         for (const PlanPart &p : parts) {
+            if (!staged) break;
             if (p.seqs.n <= 0 || p.nsup <= 1) continue;
             if (dtT_hi == dtT_lo) { dtT_lo = p.seqs.lo; dtT_hi = p.seqs.lo + p.seqs.n; }
             else { dtT_lo = std::min(dtT_lo, p.seqs.lo); dtT_hi = std::max(dtT_hi, p.seqs.lo + p.seqs.n); }
@@ -257,8 +262,8 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
         if (!rec(2)) return SSD_ERR_CUDA;
         for (const PlanPart &p : parts)
             if (p.seqs.n > 0 && p.nsup > 1 &&
-                ssd::launch_chunk_state_tc(pr, p.seqs, x, dt, w.dtT, Bm, w.G, w.s_local + p.base * HS, p.R, p.nsup,
-                                           p.nsup - 1, w.err, st) != cudaSuccess)
+                ssd::launch_chunk_state_tc(pr, p.seqs, x, dt, staged ? w.dtT : nullptr, Bm, w.G,
+                                           w.s_local + p.base * HS, p.R, p.nsup, p.nsup - 1, w.err, st) != cudaSuccess)
                 return SSD_ERR_CUDA;
         if (!rec(3) || !rec(4)) return SSD_ERR_CUDA;
         for (const PlanPart &p : parts)
@@ -436,7 +441,8 @@ ssd_status ssd_chunk_state(const ssd_desc *desc, const void *x, const void *dt, 
     if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(Bm, 16) || !aligned(G, 16) || !aligned(s_local, 16))
         return SSD_ERR_INVALID_ARG;
     const int nc = (int)pr.nc;
-    cudaError_t e = use_tensor_cores(desc, pr)
+    // every chunk's state, the last one included: the tensor-core kernel takes whole chunks only
+    cudaError_t e = use_tensor_cores(desc, pr) && pr.L % pr.T == 0
                         ? ssd::launch_chunk_state_tc(pr, ssd::SeqRange{0, pr.B * pr.nh}, x, dt, nullptr, Bm, G, s_local,
                                                      1, nc, nc, nullptr, (cudaStream_t)stream)
                         : ssd::launch_chunk_state_simt(pr, x, dt, Bm, G, s_local, (cudaStream_t)stream);

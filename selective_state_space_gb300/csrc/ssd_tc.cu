@@ -76,6 +76,14 @@ __device__ __forceinline__ void set_error(int *err, int bit)
     if (err) atomicOr(err, bit);
 }
 
+// Token index t clamped to the sequence, and whether t holds a token: only a kernel built for
+// a ragged last chunk (kRagged) pays for the checks; with whole chunks every t is inside.
+template <bool kRagged> __device__ __forceinline__ int64_t clamp_t(int64_t t, int64_t L)
+{
+    return kRagged ? (t < L ? t : L - 1) : t;
+}
+template <bool kRagged> __device__ __forceinline__ bool in_seq(int64_t t, int64_t L) { return !kRagged || t < L; }
+
 // ===========================================================================
 // chunk_state on tensor cores: the state one super-chunk produces from a zero start.
 //   s^T[s][p] = sum_{t in super-chunk m} w_t B_t[s] x_t[p],
@@ -422,7 +430,7 @@ enum ScanBar {
     kXFull0, kYSt0 = kXFull0 + 4, kNumScanBars = kYSt0 + 4
 };
 
-template <int S>
+template <int S, bool kRagged>
 __global__ void __launch_bounds__(448, 1)
 k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
@@ -458,7 +466,10 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
     const int k_begin = m * R;
     const int k_end = min((int)pr.nc, k_begin + R);
     const int qpc = (int)(pr.T / kQ);
-    const int nq = (k_end - k_begin) * qpc;
+    // sub-chunks of this super-chunk that hold tokens (the last chunk of a sequence may be short;
+    // its tokens past L are zero-filled by TMA, hold the state (dt = 0) and are not stored)
+    const int nq = kRagged ? (int)((min(pr.L, (int64_t)k_end * pr.T) - (int64_t)k_begin * pr.T + kQ - 1) / kQ)
+                           : (k_end - k_begin) * qpc;
     const int64_t t_begin = (int64_t)k_begin * pr.T;
     const int64_t bh = bhi;
     const float *Gh = G + bh * pr.L;
@@ -608,9 +619,10 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         float n_gr = 0.f, n_dt = 0.f, n_glast = 0.f, n_gbase = 0.f;
         auto load_scalars = [&](int q) {
             const int64_t t0 = t_begin + (int64_t)q * kQ;
-            n_gr = Gh[t0 + r];
-            n_dt = __bfloat162float(dt[((int64_t)b * pr.L + t0 + r) * pr.nh + h]);
-            n_glast = Gh[t0 + kQ - 1];
+            const int64_t tr = clamp_t<kRagged>(t0 + r, pr.L), tl = clamp_t<kRagged>(t0 + kQ - 1, pr.L);
+            n_gr = Gh[tr];
+            n_dt = in_seq<kRagged>(t0 + r, pr.L) ? __bfloat162float(dt[((int64_t)b * pr.L + t0 + r) * pr.nh + h]) : 0.f;
+            n_glast = Gh[tl];
             n_gbase = (q % qpc == 0) ? 0.f : Gh[t0 - 1];
         };
         if (nq > 0) load_scalars(0);
@@ -754,8 +766,8 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         float n_gr = 0.f, n_gend = 0.f, n_gbase = 0.f;
         auto load_scalars = [&](int q) {
             const int64_t t0 = t_begin + (int64_t)q * kQ;
-            n_gr = Gh[t0 + r];
-            n_gend = Gh[t0 + (r | 15)];                // G at the end of row r's 16-token block
+            n_gr = Gh[clamp_t<kRagged>(t0 + r, pr.L)];
+            n_gend = Gh[clamp_t<kRagged>(t0 + (r | 15), pr.L)];  // G at the end of row r's 16-token block
             n_gbase = (q % qpc == 0) ? 0.f : Gh[t0 - 1];
         };
         // Software-pipelined by one sub-chunk: iteration q builds P of sub-chunk q + 1, then
@@ -968,6 +980,7 @@ enum PairBar {
 };
 static_assert(pYSt0 + 3 == PairCfg::kNumBars, "pair barriers");
 
+template <bool kRagged>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
 k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
@@ -1003,7 +1016,10 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
     const int k_begin = m * R;
     const int k_end = min((int)pr.nc, k_begin + R);
     const int qpc = (int)(pr.T / kQ);
-    const int nq = (k_end - k_begin) * qpc;
+    // sub-chunks of this super-chunk that hold tokens (the last chunk of a sequence may be short;
+    // its tokens past L are zero-filled by TMA, hold the state (dt = 0) and are not stored)
+    const int nq = kRagged ? (int)((min(pr.L, (int64_t)k_end * pr.T) - (int64_t)k_begin * pr.T + kQ - 1) / kQ)
+                           : (k_end - k_begin) * qpc;
     const int64_t t_begin = (int64_t)k_begin * pr.T;
     const float *GA = G + (int64_t)bhA * pr.L, *GB = GA + pr.L;
     const bool write_final = (m == nsup - 1) && h_final;
@@ -1169,14 +1185,17 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
         uint32_t n_dt = 0;
         auto load_scalars = [&](int q) {
             const int64_t t0 = t_begin + (int64_t)q * kQ;
-            n_g[0] = GA[t0 + r];
-            n_g[1] = GB[t0 + r];
-            n_gl[0] = GA[t0 + kQ - 1];
-            n_gl[1] = GB[t0 + kQ - 1];
+            const int64_t tr = clamp_t<kRagged>(t0 + r, pr.L), tl = clamp_t<kRagged>(t0 + kQ - 1, pr.L);
+            n_g[0] = GA[tr];
+            n_g[1] = GB[tr];
+            n_gl[0] = GA[tl];
+            n_gl[1] = GB[tl];
             const bool cs = q % qpc == 0;
             n_gb[0] = cs ? 0.f : GA[t0 - 1];
             n_gb[1] = cs ? 0.f : GB[t0 - 1];
-            n_dt = *reinterpret_cast<const uint32_t *>(dt + ((int64_t)b * pr.L + t0 + r) * pr.nh + hA);
+            n_dt = in_seq<kRagged>(t0 + r, pr.L)
+                       ? *reinterpret_cast<const uint32_t *>(dt + ((int64_t)b * pr.L + t0 + r) * pr.nh + hA)
+                       : 0u;
         };
         if (nq > 0) load_scalars(0);
         for (int q = 0; q < nq && ok; ++q) {
@@ -1301,12 +1320,14 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
         float n_g[2] = {0.f, 0.f}, n_gb = 0.f, n_gend = 0.f, n_dt = 0.f;
         auto load_scalars = [&](int q) {
             const int64_t t0 = t_begin + (int64_t)q * kQ;
-            n_g[0] = GA[t0 + r];
-            n_g[1] = GB[t0 + r];
+            const int64_t tr = clamp_t<kRagged>(t0 + r, pr.L);
+            n_g[0] = GA[tr];
+            n_g[1] = GB[tr];
             const float *Gh = half ? GB : GA;
             n_gb = (q % qpc == 0) ? 0.f : Gh[t0 - 1];
-            n_gend = Gh[t0 + (r | 15)];
-            n_dt = __bfloat162float(dt[((int64_t)b * pr.L + t0 + r) * pr.nh + hA + half]);
+            n_gend = Gh[clamp_t<kRagged>(t0 + (r | 15), pr.L)];
+            n_dt = in_seq<kRagged>(t0 + r, pr.L) ? __bfloat162float(dt[((int64_t)b * pr.L + t0 + r) * pr.nh + hA + half])
+                                                 : 0.f;
         };
         if (nq > 0) load_scalars(0);
         for (int q = 0; q < nq; ++q) {
@@ -1567,13 +1588,16 @@ cudaError_t state_launch(const Problem &pr, SeqRange seqs, const void *x, const 
 {
     using Cfg = StateCfg<S, H, HG>;
     if (R > Cfg::kMaxR) return cudaErrorInvalidValue;
-    // every unit must hold R whole chunks (a short last super-chunk is left to the scan)
-    if ((int64_t)nm * R > pr.nc) return cudaErrorInvalidValue;
+    // every unit must hold R whole chunks (a short last super-chunk, and a short last chunk, are
+    // left to the scan)
+    if ((int64_t)nm * R * pr.T > pr.L) return cudaErrorInvalidValue;
     // units are whole head groups of the run
     if (seqs.lo % HG != 0 || seqs.n % HG != 0) return cudaErrorInvalidValue;
     const int64_t nq_u = (int64_t)R * (pr.T / Cfg::kTok);
     const int64_t total = (seqs.n / HG) * (int64_t)nm * nq_u;
     if (total == 0) return cudaSuccess;
+    // the staged path bulk-copies 64-token pieces of G and dtT rows: 16-byte aligned only when L % 4 == 0
+    if (dtT && (pr.L % 4 != 0 || ((uintptr_t)G % 16) || ((uintptr_t)dtT % 16))) return cudaErrorInvalidValue;
     CUtensorMap mB, mX;
     if (!make_map_4d(&mB, Bm, pr.S, pr.G, pr.L, pr.B, Cfg::kTok) || !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, Cfg::kTok))
         return cudaErrorInvalidValue;
@@ -1600,7 +1624,7 @@ cudaError_t scan_launch(const Problem &pr, const void *x, const void *dt, const 
         !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, kQ) || !make_map_4d(&mY, y, pr.H, pr.nh, pr.L, pr.B, kQ))
         return cudaErrorInvalidValue;
     using Cfg = ScanCfg<S>;
-    auto kern = k_chunk_scan_tc<S>;
+    auto kern = pr.L % pr.T == 0 ? k_chunk_scan_tc<S, false> : k_chunk_scan_tc<S, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t grid = (sp.split * sp.nsup0 + (pr.B * pr.nh - sp.split) * sp.nsup1) * (pr.H / kPB);
@@ -1620,13 +1644,14 @@ cudaError_t scan_pair_launch(const Problem &pr, const void *x, const void *dt, c
     if (!make_map_4d(&mC, Cm, pr.S, pr.G, pr.L, pr.B, kQ) || !make_map_4d(&mB, Bm, pr.S, pr.G, pr.L, pr.B, kQ) ||
         !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, kQ) || !make_map_4d(&mY, y, pr.H, pr.nh, pr.L, pr.B, kQ))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_chunk_scan_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = pr.L % pr.T == 0 ? k_chunk_scan_pair<false> : k_chunk_scan_pair<true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)PairCfg::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t grid = (sp.split / 2) * sp.nsup0 + ((pr.B * pr.nh - sp.split) / 2) * sp.nsup1;
     if (grid == 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-    return launch_pdl(k_chunk_scan_pair, dim3((unsigned)grid), dim3(PairCfg::kThreads), PairCfg::kSmem, st, mC, mB,
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(PairCfg::kThreads), PairCfg::kSmem, st, mC, mB,
                       mX, mY, G, (const __nv_bfloat16 *)dt, D, h0, h_start, h_final, pr, sp, err);
 }
 
@@ -1643,7 +1668,6 @@ bool tc_supported(const Problem &pr)
     if (pr.S != 128 && pr.S != 256) return false;
     if (pr.H != 64 && pr.H != 128) return false;
     if (pr.T % kQ != 0 || pr.T > 256) return false;
-    if (pr.L % pr.T != 0) return false;
     if (pr.L > 0x7fffffffLL || pr.B > 65535) return false;
     return true;
 }

@@ -51,6 +51,12 @@ SMALL = [
     workloads.custom(1, 256, 2, 64, 256, 1, 128, "bf16", seed=18, name="h64-s256"),
     # three heads per group: the one-head-per-CTA scan kernel at S = 128, H = 64
     workloads.custom(2, 512, 6, 64, 128, 2, 256, "bf16", h0_recipe="normal", seed=19, name="odd-hpg"),
+    # ragged lengths on the tensor-core path: a last chunk of 76 tokens (one short sub-chunk),
+    # and a long sequence cut into super-chunks whose last chunk holds 64 tokens
+    workloads.custom(2, 1100, 6, 64, 128, 1, 256, "bf16", h0_recipe="normal", seed=26, name="tc-ragged-76"),
+    workloads.custom(1, 8000, 8, 64, 128, 2, 256, "bf16", seed=27, name="tc-ragged-super"),
+    # L not a multiple of 4: chunk_state loads G and dt per thread (rows are not 16-byte aligned)
+    workloads.custom(1, 3001, 4, 64, 128, 1, 128, "bf16", h0_recipe="normal", seed=28, name="tc-ragged-odd"),
     workloads.custom(2, 77, 6, 8, 16, 3, 16, "f32", h0_recipe="normal", seed=15, name="odd-f32"),
     workloads.custom(1, 33, 2, 1, 1, 1, 1, "f32", seed=16, name="scalar-T1"),
 ]
@@ -61,6 +67,10 @@ def test_tensor_core_path_selected_for_bf16_layer_shapes():
         assert tc_path(shape), shape.name
         assert not tc_path(shape, SSD_FLAG_FORCE_SIMT)
     assert not tc_path(workloads.WORKLOADS[0])   # float32 inputs run on the CUDA cores
+    # lengths that are not a multiple of the chunk stay on the tensor cores
+    for shape in SMALL:
+        if shape.name in ("c3-ragged", "c4-ragged", "tc-ragged-76", "tc-ragged-super", "tc-ragged-odd"):
+            assert tc_path(shape), shape.name
 
 
 @pytest.mark.parametrize("path", sorted(PATHS))
