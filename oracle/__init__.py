@@ -1,4 +1,4 @@
-"""Double-precision CPU oracle for the Mamba-2 SSD forward pass and decode step.
+"""Double-precision CPU oracle for the Mamba-2 SSD forward pass, its gradients and the decode step.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The GPU library never
@@ -9,7 +9,9 @@ only builds it with gcc, loads it with ctypes and converts arrays to float64.
 Formulas follow the NVIDIA developer blog "Accelerating Mamba-2 with
 High-Performance Forward Pass Kernels in NVIDIA CUDA Tile", section
 "Mamba-2 architecture" (recurrence, output line, log-space chunk jump and
-chunk output).
+chunk output).  The gradients follow "Sasha Rush: Mamba: The Hard Way",
+Part 3 (the adjoint runs the same scan backwards), applied to that recurrence;
+``bwd_chunked`` restates them per chunk as a second, independent form.
 """
 from __future__ import annotations
 
@@ -56,6 +58,8 @@ def _load():
             lib.oracle_ssd_fwd_chunked.restype = ctypes.c_int
             lib.oracle_ssd_step.argtypes = [i64] * 5 + [D] * 8
             lib.oracle_ssd_step.restype = ctypes.c_int
+            lib.oracle_ssd_bwd_seq.argtypes = [i64] * 6 + [D] * 16 + [ctypes.c_int]
+            lib.oracle_ssd_bwd_seq.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -148,3 +152,25 @@ def ssd_step(x, dt, A, Bm, Cm, D, h):
     if rc != 0:
         raise ValueError(f"oracle_ssd_step failed ({rc})")
     return y, h
+
+
+def ssd_bwd_seq(x, dt, A, Bm, Cm, D, dy, h0=None, dh_final=None, nthreads=None):
+    """Gradients of sum(dy * y) + sum(dh_final * h_final) (reverse mode of the recurrence).
+
+    Returns a dict of float64 arrays: dx [B,L,nh,H], ddt [B,L,nh], dA [nh], dB, dC
+    [B,L,G,S], dD [nh], dh0 [B,nh,H,S] (the gradient of the initial state, zeros or not).
+    """
+    x, dt, A, Bm, Cm, D, h0, dy, dh_final = map(_f64, (x, dt, A, Bm, Cm, D, h0, dy, dh_final))
+    batch, seqlen, nheads, H, S, ngroups = _shapes(x, Bm)
+    out = dict(dx=np.zeros_like(x), ddt=np.zeros_like(dt), dA=np.zeros(nheads),
+               dB=np.zeros_like(Bm), dC=np.zeros_like(Cm), dD=np.zeros(nheads),
+               dh0=np.zeros((batch, nheads, H, S)))
+    rc = _load().oracle_ssd_bwd_seq(batch, seqlen, nheads, H, S, ngroups,
+                                    _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
+                                    _ptr(h0), _ptr(dy), _ptr(dh_final),
+                                    _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]),
+                                    _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+                                    _ptr(out["dh0"]), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_ssd_bwd_seq failed ({rc})")
+    return out

@@ -306,3 +306,217 @@ int oracle_ssd_step(int64_t batch, int64_t nheads, int64_t H, int64_t S, int64_t
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * Gradients of the forward pass (reverse mode of the plain recurrence).
+ *
+ * Source: "Sasha Rush: Mamba: The Hard Way" (Korean translation), Part 3,
+ * deriving the derivatives: for the scalar scan h_k = a_k h_{k-1} + b_k x_k, y_k = c_k h_k
+ * the adjoint runs the same scan backwards, dh_k = c_k dy_k + a_{k+1} dh_{k+1},
+ * and then dx_k = b_k dh_k, db_k = x_k dh_k, dc_k = h_k dy_k,
+ * da_k = dh_k h_{k-1}.  Here the same steps are taken for the matrix state of
+ * the blog's recurrence (a_t = exp(A dt_t), b_t = dt_t B_t, with c_t^T h_t
+ * contracting over the state index), and the chain rule carries da_t and db_t
+ * to dt_t, A and B:
+ *
+ *   lam_t  = dy_t c_t^T + exp(A dt_{t+1}) lam_{t+1},   lam_{L-1} = dy c^T + dh_final
+ *   dx_t[p]  = dt_t sum_s lam_t[p][s] B_t[s] + D dy_t[p]
+ *   dB_t[s] += dt_t sum_p lam_t[p][s] x_t[p]               (summed over the group's heads)
+ *   dC_t[s] += sum_p h_t[p][s] dy_t[p]                     (summed over the group's heads)
+ *   ddt_t   = <lam_t, x_t B_t^T> + A exp(A dt_t) <lam_t, h_{t-1}>
+ *   dA     += dt_t exp(A dt_t) <lam_t, h_{t-1}>
+ *   dD     += dy_t . x_t
+ *   dh0     = exp(A dt_0) lam_0
+ *
+ * The loss is sum(dy * y) + sum(dh_final * h_final); dh_final may be NULL
+ * (zeros).  The forward states h_t of the pair are kept in full (plain
+ * definition, no recomputation), so memory is (L + 1) H S doubles per thread.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int64_t batch, seqlen, nheads, H, S, ngroups;
+    const double *x, *dt, *A, *Bm, *Cm, *D, *h0, *dy, *dhf;
+    double *dx, *ddt, *dh0;
+    double *dB_head, *dC_head;   /* [batch][seqlen][nheads][S]: per-head parts of dB, dC */
+    double *dA_pair, *dD_pair;   /* [batch][nheads] */
+    int64_t next_unit;
+    pthread_mutex_t lock;
+} bwd_job_t;
+
+#define BIX_X(j, b, t, h, p) ((((b) * (j)->seqlen + (t)) * (j)->nheads + (h)) * (j)->H + (p))
+#define BIX_DT(j, b, t, h) (((b) * (j)->seqlen + (t)) * (j)->nheads + (h))
+#define BIX_BC(j, b, t, g, s) ((((b) * (j)->seqlen + (t)) * (j)->ngroups + (g)) * (j)->S + (s))
+#define BIX_HS(j, b, t, h, s) ((((b) * (j)->seqlen + (t)) * (j)->nheads + (h)) * (j)->S + (s))
+#define BIX_H(j, b, h, p, s) ((((b) * (j)->nheads + (h)) * (j)->H + (p)) * (j)->S + (s))
+
+/* hs: (seqlen + 1) * H * S doubles, hs[0] = h_{-1} = h0; lam: H * S doubles */
+static void bwd_unit(const bwd_job_t *j, int64_t b, int64_t h, double *hs, double *lam)
+{
+    const int64_t H = j->H, S = j->S, L = j->seqlen, HS = H * S;
+    const int64_t g = h / (j->nheads / j->ngroups);
+    const double Ah = j->A[h];
+    /* forward: every state h_t, t = -1 .. L-1 */
+    for (int64_t p = 0; p < H; ++p)
+        for (int64_t s = 0; s < S; ++s) hs[p * S + s] = j->h0 ? j->h0[BIX_H(j, b, h, p, s)] : 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+        const double dtv = j->dt[BIX_DT(j, b, t, h)];
+        const double alpha = exp(Ah * dtv);
+        const double *prev = hs + t * HS;
+        double *cur = hs + (t + 1) * HS;
+        for (int64_t p = 0; p < H; ++p) {
+            const double xp = j->x[BIX_X(j, b, t, h, p)];
+            for (int64_t s = 0; s < S; ++s)
+                cur[p * S + s] = alpha * prev[p * S + s] + dtv * j->Bm[BIX_BC(j, b, t, g, s)] * xp;
+        }
+    }
+    /* backward: lam = dh_final, then t = L-1 .. 0 */
+    for (int64_t p = 0; p < H; ++p)
+        for (int64_t s = 0; s < S; ++s) lam[p * S + s] = j->dhf ? j->dhf[BIX_H(j, b, h, p, s)] : 0.0;
+    double dA = 0.0, dD = 0.0;
+    for (int64_t t = L - 1; t >= 0; --t) {
+        const double dtv = j->dt[BIX_DT(j, b, t, h)];
+        const double alpha = exp(Ah * dtv);
+        const double *hprev = hs + t * HS;        /* h_{t-1} */
+        const double *hcur = hs + (t + 1) * HS;   /* h_t */
+        /* lam_t: add the output's contribution dy_t c_t^T */
+        for (int64_t p = 0; p < H; ++p) {
+            const double dyp = j->dy[BIX_X(j, b, t, h, p)];
+            for (int64_t s = 0; s < S; ++s) lam[p * S + s] += dyp * j->Cm[BIX_BC(j, b, t, g, s)];
+        }
+        /* dC_t (this head's part): h_t^T dy_t */
+        for (int64_t s = 0; s < S; ++s) {
+            double acc = 0.0;
+            for (int64_t p = 0; p < H; ++p) acc += hcur[p * S + s] * j->dy[BIX_X(j, b, t, h, p)];
+            j->dC_head[BIX_HS(j, b, t, h, s)] = acc;
+        }
+        /* dx_t = dt_t lam_t B_t + D dy_t */
+        for (int64_t p = 0; p < H; ++p) {
+            double acc = 0.0;
+            for (int64_t s = 0; s < S; ++s) acc += lam[p * S + s] * j->Bm[BIX_BC(j, b, t, g, s)];
+            const double dyp = j->dy[BIX_X(j, b, t, h, p)];
+            j->dx[BIX_X(j, b, t, h, p)] = dtv * acc + j->D[h] * dyp;
+            dD += dyp * j->x[BIX_X(j, b, t, h, p)];
+        }
+        /* dB_t (this head's part): dt_t lam_t^T x_t */
+        for (int64_t s = 0; s < S; ++s) {
+            double acc = 0.0;
+            for (int64_t p = 0; p < H; ++p) acc += lam[p * S + s] * j->x[BIX_X(j, b, t, h, p)];
+            j->dB_head[BIX_HS(j, b, t, h, s)] = dtv * acc;
+        }
+        /* d(dt_t): through b_t = dt_t B_t, and through a_t = exp(A dt_t) */
+        double via_b = 0.0, lam_hprev = 0.0;
+        for (int64_t p = 0; p < H; ++p) {
+            const double xp = j->x[BIX_X(j, b, t, h, p)];
+            for (int64_t s = 0; s < S; ++s) {
+                via_b += lam[p * S + s] * xp * j->Bm[BIX_BC(j, b, t, g, s)];
+                lam_hprev += lam[p * S + s] * hprev[p * S + s];
+            }
+        }
+        const double da = alpha * lam_hprev;      /* dL/da_t times a_t: d/d(A dt_t) */
+        j->ddt[BIX_DT(j, b, t, h)] = via_b + Ah * da;
+        dA += dtv * da;
+        /* lam_{t-1} gets exp(A dt_t) lam_t */
+        for (int64_t e = 0; e < HS; ++e) lam[e] *= alpha;
+    }
+    if (j->dh0)
+        for (int64_t p = 0; p < H; ++p)
+            for (int64_t s = 0; s < S; ++s) j->dh0[BIX_H(j, b, h, p, s)] = lam[p * S + s];
+    j->dA_pair[b * j->nheads + h] = dA;
+    j->dD_pair[b * j->nheads + h] = dD;
+}
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job_t *j = (bwd_job_t *)arg;
+    const int64_t units = j->batch * j->nheads;
+    const int64_t HS = j->H * j->S;
+    double *hs = (double *)malloc((size_t)((j->seqlen + 1) * HS) * sizeof(double));
+    double *lam = (double *)malloc((size_t)HS * sizeof(double));
+    if (!hs || !lam) { free(hs); free(lam); return (void *)1; }
+    for (;;) {
+        pthread_mutex_lock(&j->lock);
+        const int64_t u = j->next_unit++;
+        pthread_mutex_unlock(&j->lock);
+        if (u >= units) break;
+        bwd_unit(j, u / j->nheads, u % j->nheads, hs, lam);
+    }
+    free(hs);
+    free(lam);
+    return NULL;
+}
+
+/* Gradients of sum(dy * y) + sum(dh_final * h_final) with respect to every
+ * input of oracle_ssd_fwd_seq.  dh_final and h0 may be NULL (zeros); dh0 may be
+ * NULL (not written).  Output layouts match the inputs':
+ *   dx [batch][seqlen][nheads][H], ddt [batch][seqlen][nheads], dA, dD [nheads],
+ *   dB, dC [batch][seqlen][ngroups][S], dh0 [batch][nheads][H][S].
+ * The sums over heads (dB, dC) and over batch and time (dA, dD) are taken
+ * serially in index order after the parallel part.  Returns 0 on success. */
+int oracle_ssd_bwd_seq(int64_t batch, int64_t seqlen, int64_t nheads, int64_t H, int64_t S,
+                       int64_t ngroups, const double *x, const double *dt, const double *A,
+                       const double *Bm, const double *Cm, const double *D, const double *h0,
+                       const double *dy, const double *dh_final, double *dx, double *ddt,
+                       double *dA, double *dB, double *dC, double *dD, double *dh0, int nthreads)
+{
+    if (batch < 0 || seqlen < 0 || nheads < 0 || H <= 0 || S <= 0) return -1;
+    if (ngroups <= 0 || (nheads % ngroups) != 0) return -1;
+    const int64_t units = batch * nheads, hpg = ngroups ? nheads / ngroups : 1;
+    const int64_t HS = H * S;
+    for (int64_t h = 0; h < nheads; ++h) { dA[h] = 0.0; dD[h] = 0.0; }
+    memset(dB, 0, (size_t)(batch * seqlen * ngroups * S) * sizeof(double));
+    memset(dC, 0, (size_t)(batch * seqlen * ngroups * S) * sizeof(double));
+    if (units == 0) return 0;
+    if (seqlen == 0) {   /* no tokens: h_final = h0, so dh0 = dh_final */
+        if (dh0) {
+            if (dh_final) memcpy(dh0, dh_final, (size_t)(units * HS) * sizeof(double));
+            else memset(dh0, 0, (size_t)(units * HS) * sizeof(double));
+        }
+        return 0;
+    }
+    bwd_job_t j;
+    memset(&j, 0, sizeof j);
+    j.batch = batch; j.seqlen = seqlen; j.nheads = nheads; j.H = H; j.S = S; j.ngroups = ngroups;
+    j.x = x; j.dt = dt; j.A = A; j.Bm = Bm; j.Cm = Cm; j.D = D; j.h0 = h0; j.dy = dy; j.dhf = dh_final;
+    j.dx = dx; j.ddt = ddt; j.dh0 = dh0;
+    const size_t nhs = (size_t)(batch * seqlen * nheads * S);
+    j.dB_head = (double *)malloc(nhs * sizeof(double));
+    j.dC_head = (double *)malloc(nhs * sizeof(double));
+    j.dA_pair = (double *)malloc((size_t)units * sizeof(double));
+    j.dD_pair = (double *)malloc((size_t)units * sizeof(double));
+    int rc = 0;
+    if (!j.dB_head || !j.dC_head || !j.dA_pair || !j.dD_pair) rc = -2;
+    if (rc == 0) {
+        if (nthreads < 1) nthreads = 1;
+        if (nthreads > units) nthreads = (int)units;
+        pthread_mutex_init(&j.lock, NULL);
+        pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+        for (int i = 0; i < nthreads; ++i) pthread_create(&tid[i], NULL, bwd_worker, &j);
+        for (int i = 0; i < nthreads; ++i) {
+            void *ret = NULL;
+            pthread_join(tid[i], &ret);
+            if (ret) rc = -2;
+        }
+        free(tid);
+        pthread_mutex_destroy(&j.lock);
+    }
+    if (rc == 0) {
+        for (int64_t b = 0; b < batch; ++b)
+            for (int64_t t = 0; t < seqlen; ++t)
+                for (int64_t h = 0; h < nheads; ++h) {
+                    const int64_t g = h / hpg;
+                    for (int64_t s = 0; s < S; ++s) {
+                        dB[BIX_BC(&j, b, t, g, s)] += j.dB_head[BIX_HS(&j, b, t, h, s)];
+                        dC[BIX_BC(&j, b, t, g, s)] += j.dC_head[BIX_HS(&j, b, t, h, s)];
+                    }
+                }
+        for (int64_t b = 0; b < batch; ++b)
+            for (int64_t h = 0; h < nheads; ++h) {
+                dA[h] += j.dA_pair[b * nheads + h];
+                dD[h] += j.dD_pair[b * nheads + h];
+            }
+    }
+    free(j.dB_head);
+    free(j.dC_head);
+    free(j.dA_pair);
+    free(j.dD_pair);
+    return rc;
+}

@@ -3,7 +3,8 @@
 Each case copies ssd_oracle.c, plants one plausible mistake by text
 substitution (a dropped term, a wrong sign, a wrong index or mask, a swapped
 operand), builds the copy with gcc into a temporary directory, swaps it in as
-the oracle library and runs the pin suite of test_oracle_pins.py.  At least
+the oracle library and runs the pin suites of test_oracle_pins.py and
+test_oracle_bwd_pins.py.  At least
 one pin must fail for every mutant.  All of this runs on the CPU.
 """
 import ctypes
@@ -13,6 +14,7 @@ import subprocess
 import pytest
 
 import oracle
+from tests import test_oracle_bwd_pins as bwd_pins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ssd_oracle.c")
@@ -54,15 +56,46 @@ MUTANTS = {
     "step-decay-missing": (
         "row[s] = alpha * row[s] + dtv * Bv[s] * xp;",
         "row[s] = row[s] + dtv * Bv[s] * xp;"),
+    # gradients (oracle_ssd_bwd_seq)
+    "bwd-adjoint-undecayed": (
+        "for (int64_t e = 0; e < HS; ++e) lam[e] *= alpha;",
+        "for (int64_t e = 0; e < HS; ++e) lam[e] *= 1.0;"),
+    "bwd-dx-missing-dt": (
+        "j->dx[BIX_X(j, b, t, h, p)] = dtv * acc + j->D[h] * dyp;",
+        "j->dx[BIX_X(j, b, t, h, p)] = acc + j->D[h] * dyp;"),
+    "bwd-dC-uses-previous-state": (
+        "for (int64_t p = 0; p < H; ++p) acc += hcur[p * S + s] * j->dy[BIX_X(j, b, t, h, p)];",
+        "for (int64_t p = 0; p < H; ++p) acc += hprev[p * S + s] * j->dy[BIX_X(j, b, t, h, p)];"),
+    "bwd-ddt-drops-decay-path": (
+        "j->ddt[BIX_DT(j, b, t, h)] = via_b + Ah * da;",
+        "j->ddt[BIX_DT(j, b, t, h)] = via_b;"),
+    "bwd-dA-missing-dt": (
+        "dA += dtv * da;",
+        "dA += da;"),
+    "bwd-decay-path-uses-current-state": (
+        "lam_hprev += lam[p * S + s] * hprev[p * S + s];",
+        "lam_hprev += lam[p * S + s] * hcur[p * S + s];"),
+    "bwd-dB-wrong-group": (
+        "const int64_t g = h / hpg;\n                    for (int64_t s = 0; s < S; ++s) {",
+        "const int64_t g = h % ngroups;\n                    for (int64_t s = 0; s < S; ++s) {"),
+    "bwd-dB-transposed-operand": (
+        "for (int64_t p = 0; p < H; ++p) acc += lam[p * S + s] * j->x[BIX_X(j, b, t, h, p)];",
+        "for (int64_t p = 0; p < H; ++p) acc += lam[p * S + s] * j->dy[BIX_X(j, b, t, h, p)];"),
+    "bwd-dD-drops-x": (
+        "dD += dyp * j->x[BIX_X(j, b, t, h, p)];",
+        "dD += dyp;"),
+    "bwd-dh-final-ignored": (
+        "lam[p * S + s] = j->dhf ? j->dhf[BIX_H(j, b, h, p, s)] : 0.0;",
+        "lam[p * S + s] = 0.0;"),
 }
 
 
 def _pin_functions():
     out = []
-    for name in dir(pins):
+    for mod, name in [(m, n) for m in (pins, bwd_pins) for n in dir(m)]:
         if not name.startswith("test_"):
             continue
-        fn = getattr(pins, name)
+        fn = getattr(mod, name)
         marks = getattr(fn, "pytestmark", [])
         params = [m for m in marks if m.name == "parametrize"]
         if params:
@@ -86,7 +119,7 @@ def test_planted_mistake_is_caught(mutant, tmp_path, monkeypatch):
                     "-lpthread", "-lm"], check=True)
     real = oracle._load()
     lib = ctypes.CDLL(str(so))
-    for fname in ("oracle_ssd_fwd_seq", "oracle_ssd_fwd_chunked", "oracle_ssd_step"):
+    for fname in ("oracle_ssd_fwd_seq", "oracle_ssd_fwd_chunked", "oracle_ssd_step", "oracle_ssd_bwd_seq"):
         getattr(lib, fname).argtypes = getattr(real, fname).argtypes
         getattr(lib, fname).restype = getattr(real, fname).restype
     monkeypatch.setattr(oracle, "_lib", lib)
