@@ -365,6 +365,77 @@ def run_decode(args, shape):
     print(json.dumps(line), flush=True)
 
 
+BWD_METRIC = "ssd_bwd_tokens_per_s"
+# float32 CUDA-core peak of one GB300: 152 SMs x 128 FP32 lanes x 2 flop (FMA) x 2070 MHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def bwd_alg_flops(s: workloads.Shape) -> float:
+    """Algorithmic flops of the chunked gradient pass, per (batch, chunk): per head
+    10TSH (five contractions of 2TSH each: the forward chunk state, the entering-state
+    gradient, Lam B, Lam^T x and h_in^T dy) + T(T+1)(2H + 2S) (dy.x and the contractions of
+    v, dB and dC, lower triangles) + 6SH (both state passes and <Lam, h_in>), plus per
+    group T(T+1) S (C B^T, lower triangle)."""
+    T, S, H = s.chunk, s.dstate, s.headdim
+    per_head = 10 * T * S * H + T * (T + 1) * (2 * H + 2 * S) + 6 * S * H
+    return float(s.batch * s.nchunks * (s.nheads * per_head + s.ngroups * T * (T + 1) * S))
+
+
+def run_bwd(args, shape):
+    """ssd_bwd throughput on one layer: the whole gradient pass (forward recompute included)
+    per step, inputs and upstream gradients resident on the device."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from selective_state_space_gb300 import api
+    from selective_state_space_gb300.build import build
+    build()
+    inp = workloads.make_inputs(shape)
+    gin = workloads.make_grad_inputs(shape)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.tensors().items()}
+    dy, dhf = gin.dy.to(dev), gin.dh_final.to(dev)
+    desc = api.desc_for(d["x"], d["B"], shape.chunk)
+    ws = torch.empty(max(api.bwd_workspace_size(desc), 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return api.ssd_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], dy, shape.chunk, d["h0"], dhf,
+                           workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    ms_per_step = start.elapsed_time(end) / args.steps
+    e = esize(shape.dtype)
+    io = 2 * step_io_bytes(shape) + shape.batch * shape.seqlen * shape.nheads * shape.headdim * e   # + dy
+    flops = bwd_alg_flops(shape)
+    peaks, peak_kind = load_peaks()
+    line = {
+        "metric": BWD_METRIC, "value": shape.tokens / (ms_per_step * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (CUDA cores), " + shape.dtype + " (inputs, gradients)",
+        "data": "synthetic", "config": dict(config_of(shape), l2="no flush: inputs, gradients and workspace per step "
+                                            "exceed twice the 129 MB L2"),
+        "roofline": {"kernel": "ssd_bwd (whole pass)", "bound": "alu", "achieved": flops / (ms_per_step * 1e-3) / 1e12,
+                     "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": flops / (ms_per_step * 1e-3) / 1e12 / FP32_ALU_TFLOPS,
+                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2070 MHz", "alg_flops_per_step": flops,
+                     "traffic": None},
+        "hbm_roofline": {"alg_bytes_per_step": io, "achieved_gbs": io / (ms_per_step * 1e-3) / 1e9,
+                         "peak_gbs": float(peaks["hbm_gbs"]),
+                         "frac": io / (ms_per_step * 1e-3) / 1e9 / float(peaks["hbm_gbs"])},
+        "e2e": None,
+        "gpu_launches": 11 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -376,6 +447,8 @@ def main():
     ap.add_argument("--ref-step-s", type=float, default=2.0)
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
+                    help="bwd: time the gradient pass (ssd_bwd) of the workload instead of the forward pass")
     args = ap.parse_args()
     dshape = parse_decode(args.workload)
     if dshape is not None:
@@ -385,6 +458,12 @@ def main():
         run_decode(args, dshape)
         return
     shape = workloads.by_name(args.workload)
+    if args.which == "bwd":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the forward pass only"}))
+            return
+        run_bwd(args, shape)
+        return
     if args.impl == "reference":
         run_reference(args, shape)
         return

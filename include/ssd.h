@@ -198,6 +198,33 @@ ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, c
                           const void *Cm, const float *D, const float *G, const float *h_start,
                           void *y, ssd_stream_t stream);
 
+/* ---- Gradients of the forward pass --------------------------------------
+ * Reverse mode of the recurrence above, taken chunk by chunk ("Sasha Rush:
+ * Mamba: The Hard Way", Part 3: the adjoint state runs the same scan
+ * backwards; each coefficient's gradient pairs a forward and a backward
+ * quantity).  For upstream gradients dy (of y) and dh_final (of h_final),
+ * ssd_bwd writes the gradient of  sum(dy * y) + sum(dh_final * h_final)
+ * with respect to every input of ssd_fwd:
+ *   dx   [B][L][nh][H]  in      ddt [B][L][nh] in      dA, dD [nh] float32
+ *   dB   [B][L][G][S]   in      dC  [B][L][G][S] in    dh0 [B][nh][H][S] float32
+ * dy has the layout of y and the in dtype: the gradient pass requires
+ * desc.in_dtype == desc.out_dtype.  dh_final, h0 and dh0 are nullable (zeros;
+ * not written).  dB, dC sum over the heads of each group; dA, dD over batch
+ * and tokens.
+ * Limits: H <= 128, S <= 256, chunk <= 256, in_dtype == out_dtype; other
+ * well-formed problems return SSD_ERR_UNSUPPORTED.  desc.flags is ignored.
+ * All pointers aligned to their element size (2 bytes for bf16, 4 otherwise);
+ * outputs must not overlap inputs or each other.  The forward states are
+ * recomputed inside the call (nothing from an earlier ssd_fwd is reused).
+ * Every sum is taken in a fixed order: results are deterministic.
+ * workspace: at least ssd_bwd_workspace_size() bytes, 256-byte aligned. */
+ssd_status ssd_bwd_workspace_size(const ssd_desc *desc, size_t *bytes);
+ssd_status ssd_bwd(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                   const void *Bm, const void *Cm, const float *D, const float *h0,
+                   const void *dy, const float *dh_final, void *dx, void *ddt, float *dA,
+                   void *dB, void *dC, float *dD, float *dh0, void *workspace, size_t ws_bytes,
+                   ssd_stream_t stream);
+
 /* ---- Forward pass for callers that cannot allocate device memory ---------
  * (The pages have no counterpart to this entry point: it is a deployment aid.)
  *

@@ -18,7 +18,8 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
 EXPORTS = ("ssd_status_string", "ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd_plan", "ssd_fwd", "ssd_fwd_timed",
            "ssd_fwd_check",
            "ssd_step",
-           "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_fwd_noalloc")
+           "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_bwd_workspace_size",
+           "ssd_bwd", "ssd_fwd_noalloc")
 
 
 class Desc(ctypes.Structure):
@@ -82,6 +83,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ssd_fwd_check.restype = st
         lib.ssd_fwd_noalloc.argtypes = [DP] + [P] * 9 + [P]
         lib.ssd_fwd_noalloc.restype = st
+        lib.ssd_bwd_workspace_size.argtypes = [DP, ctypes.POINTER(ctypes.c_size_t)]
+        lib.ssd_bwd_workspace_size.restype = st
+        lib.ssd_bwd.argtypes = [DP] + [P] * 17 + [ctypes.c_size_t, P]
+        lib.ssd_bwd.restype = st
         _lib = lib
         return lib
 

@@ -134,6 +134,37 @@ def ssd_step(x, dt, A, B, C, D, h, *, y=None, out_dtype=None, stream=None):
     return y
 
 
+def bwd_workspace_size(desc: Desc) -> int:
+    n = ctypes.c_size_t(0)
+    check("ssd_bwd_workspace_size", _native.load().ssd_bwd_workspace_size(ctypes.byref(desc), ctypes.byref(n)))
+    return int(n.value)
+
+
+def ssd_bwd(x, dt, A, B, C, D, dy, chunk: int, h0=None, dh_final=None, *, want_dh0=True, workspace=None,
+            stream=None):
+    """Gradients of sum(dy * y) + sum(dh_final * h_final) for the forward pass of ``ssd_fwd``.
+
+    Same input layouts as ``ssd_fwd``; dy has the layout and dtype of x (the gradient
+    pass needs the output dtype equal to the input dtype).  Returns a dict with dx, ddt,
+    dB, dC (the input dtype), dA, dD [nh] float32 and dh0 [B,nh,H,S] float32 (or None).
+    """
+    desc = desc_for(x, B, chunk, None, 0)
+    batch, seqlen, nheads, headdim = x.shape
+    dstate = B.shape[3]
+    out = {"dx": torch.empty_like(x), "ddt": torch.empty_like(dt), "dB": torch.empty_like(B),
+           "dC": torch.empty_like(C), "dA": torch.empty(nheads, dtype=torch.float32, device=x.device),
+           "dD": torch.empty(nheads, dtype=torch.float32, device=x.device),
+           "dh0": torch.empty((batch, nheads, headdim, dstate), dtype=torch.float32, device=x.device)
+           if want_dh0 else None}
+    if workspace is None:
+        workspace = torch.empty(max(bwd_workspace_size(desc), 256), dtype=torch.uint8, device=x.device)
+    check("ssd_bwd", _native.load().ssd_bwd(
+        ctypes.byref(desc), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(h0), _ptr(dy),
+        _ptr(dh_final), _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]),
+        _ptr(out["dD"]), _ptr(out["dh0"]), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
 # ---- the four stages, one call each (intermediate layouts in include/ssd.h) ----
 
 def ssd_chunk_cumsum(dt, A, chunk: int, desc: Desc = None, *, G=None, stream=None):

@@ -492,6 +492,72 @@ ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, c
     return cuda_status(e);
 }
 
+ssd_status ssd_bwd_workspace_size(const ssd_desc *desc, size_t *bytes)
+{
+    Problem pr;
+    if (!bytes) return SSD_ERR_INVALID_ARG;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    if (!ssd::bwd_supported(pr)) return SSD_ERR_UNSUPPORTED;
+    *bytes = nonempty(pr) ? ssd::bwd_workspace(pr, nullptr, nullptr) : 0;
+    return SSD_OK;
+}
+
+ssd_status ssd_bwd(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                   const void *Bm, const void *Cm, const float *D, const float *h0,
+                   const void *dy, const float *dh_final, void *dx, void *ddt, float *dA,
+                   void *dB, void *dC, float *dD, float *dh0, void *workspace, size_t ws_bytes,
+                   ssd_stream_t stream)
+{
+    Problem pr;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    if (!ssd::bwd_supported(pr)) return SSD_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t es = esize(pr.in_dt);
+    const size_t nstate = (size_t)(pr.B * pr.nh * pr.H * pr.S);
+    if ((dA && !aligned(dA, 4)) || (dD && !aligned(dD, 4)) || (h0 && !aligned(h0, 4)) ||
+        (dh_final && !aligned(dh_final, 4)) || (dh0 && !aligned(dh0, 4)))
+        return SSD_ERR_INVALID_ARG;
+    if (pr.nh > 0 && (!dA || !dD)) return SSD_ERR_INVALID_ARG;
+    if (!nonempty(pr)) {
+        // no tokens: h_final = h0, so dh0 = dh_final; dA and dD are empty sums
+        if (pr.nh > 0 && (cudaMemsetAsync(dA, 0, pr.nh * sizeof(float), st) != cudaSuccess ||
+                          cudaMemsetAsync(dD, 0, pr.nh * sizeof(float), st) != cudaSuccess))
+            return SSD_ERR_CUDA;
+        if (dh0 && nstate) {
+            cudaError_t e = dh_final ? cudaMemcpyAsync(dh0, dh_final, nstate * sizeof(float), cudaMemcpyDeviceToDevice, st)
+                                     : cudaMemsetAsync(dh0, 0, nstate * sizeof(float), st);
+            return cuda_status(e);
+        }
+        return SSD_OK;
+    }
+    if (!x || !dt || !A || !Bm || !Cm || !D || !dy || !dx || !ddt || !dB || !dC) return SSD_ERR_INVALID_ARG;
+    if (!aligned(x, es) || !aligned(dt, es) || !aligned(Bm, es) || !aligned(Cm, es) || !aligned(dy, es) ||
+        !aligned(dx, es) || !aligned(ddt, es) || !aligned(dB, es) || !aligned(dC, es) || !aligned(A, 4) ||
+        !aligned(D, 4))
+        return SSD_ERR_INVALID_ARG;
+    const size_t nx = (size_t)(pr.B * pr.L * pr.nh * pr.H) * es;
+    const size_t ndt = (size_t)(pr.B * pr.L * pr.nh) * es;
+    const size_t nbc = (size_t)(pr.B * pr.L * pr.G * pr.S) * es;
+    const void *ins[] = {x, dt, Bm, Cm, dy, h0, dh_final, A, D};
+    const size_t in_sz[] = {nx, ndt, nbc, nbc, nx, h0 ? nstate * 4 : 0, dh_final ? nstate * 4 : 0,
+                            (size_t)pr.nh * 4, (size_t)pr.nh * 4};
+    const void *outs[] = {dx, ddt, dB, dC, dA, dD, dh0};
+    const size_t out_sz[] = {nx, ndt, nbc, nbc, (size_t)pr.nh * 4, (size_t)pr.nh * 4, dh0 ? nstate * 4 : 0};
+    for (int o = 0; o < 7; ++o) {
+        for (int i = 0; i < 9; ++i)
+            if (overlaps(outs[o], out_sz[o], ins[i], in_sz[i])) return SSD_ERR_INVALID_ARG;
+        for (int o2 = o + 1; o2 < 7; ++o2)
+            if (overlaps(outs[o], out_sz[o], outs[o2], out_sz[o2])) return SSD_ERR_INVALID_ARG;
+    }
+    ssd::BwdWork w;
+    const size_t need = ssd::bwd_workspace(pr, workspace, &w);
+    if (!workspace || !aligned(workspace, kWsAlign) || ws_bytes < need) return SSD_ERR_WORKSPACE;
+    const ssd::BwdArgs a{x, dt, Bm, Cm, dy, A, D, h0, dh_final, dx, ddt, dB, dC, dA, dD, dh0};
+    return cuda_status(ssd::launch_bwd(pr, a, w, st));
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

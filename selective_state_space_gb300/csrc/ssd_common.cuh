@@ -78,6 +78,25 @@ cudaError_t launch_state_passing(const Problem &pr, SeqRange seqs, const float *
 cudaError_t launch_chunk_scan_simt(const Problem &pr, const void *x, const void *dt,
                                    const void *Bm, const void *Cm, const float *D, const float *G,
                                    const float *h_start, void *y, cudaStream_t st);
+// Gradients of the forward pass (ssd_bwd.cu).  Pointers as in ssd_bwd of include/ssd.h.
+struct BwdArgs {
+    const void *x, *dt, *Bm, *Cm, *dy;
+    const float *A, *D, *h0, *dh_final;
+    void *dx, *ddt, *dB, *dC;
+    float *dA, *dD, *dh0;
+};
+// Workspace of the gradient pass, carved by bwd_workspace: G, the states entering each
+// chunk, the gradients of the states leaving them, six per-token float arrays and the
+// per-slice partial sums of dB and dC.  nslice slices of hps heads split each group.
+struct BwdWork {
+    float *G, *h_start, *lam, *Qd, *Nd, *Cmd, *Dd, *Rw, *Ad, *dBp, *dCp;
+    int nslice, hps;
+};
+bool bwd_supported(const Problem &pr);
+// Carves `base` (nullptr: sizes only) and returns the bytes needed.
+size_t bwd_workspace(const Problem &pr, void *base, BwdWork *w);
+cudaError_t launch_bwd(const Problem &pr, const BwdArgs &a, const BwdWork &w, cudaStream_t st);
+
 cudaError_t launch_ssd_step(const Problem &pr, const void *x, const void *dt, const float *A,
                             const void *Bm, const void *Cm, const float *D, float *h, void *y,
                             cudaStream_t st);

@@ -133,3 +133,20 @@ def make_inputs(shape: Shape, seed: Optional[int] = None) -> Inputs:
     dt = dt.to(dt_)
     return Inputs(shape, x.contiguous(), dt.contiguous(), A.contiguous(), Bm.contiguous(),
                   Cm.contiguous(), D.contiguous(), None if h0 is None else h0.contiguous())
+
+
+@dataclasses.dataclass
+class GradInputs:
+    dy: torch.Tensor                  # [B, L, nh, H]   input dtype (the gradient of y)
+    dh_final: Optional[torch.Tensor]  # [B, nh, H, S]   float32 (the gradient of h_final) or None
+
+
+def make_grad_inputs(shape: Shape, with_dh_final: bool = True, seed: Optional[int] = None) -> GradInputs:
+    """Upstream gradients for the gradient pass, from their own generator (seed + 1000 by
+    default): dy ~ N(0, 1) in the input dtype, then dh_final ~ N(0, 0.1) float32."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed((shape.seed + 1000) if seed is None else seed)
+    Bsz, L, nh, H, S = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate
+    dy = torch.randn((Bsz, L, nh, H), generator=g, dtype=torch.float32).to(torch_dtype(shape.dtype))
+    dhf = 0.1 * torch.randn((Bsz, nh, H, S), generator=g, dtype=torch.float32) if with_dh_final else None
+    return GradInputs(dy.contiguous(), None if dhf is None else dhf.contiguous())
