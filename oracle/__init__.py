@@ -12,6 +12,8 @@ High-Performance Forward Pass Kernels in NVIDIA CUDA Tile", section
 chunk output).  The gradients follow "Sasha Rush: Mamba: The Hard Way",
 Part 3 (the adjoint runs the same scan backwards), applied to that recurrence;
 ``bwd_chunked`` restates them per chunk as a second, independent form.
+``s6_fwd_seq`` is the Mamba-1 selective scan of the same page, Part 5
+(discretize, then the per-channel vector recurrence).
 """
 from __future__ import annotations
 
@@ -60,6 +62,8 @@ def _load():
             lib.oracle_ssd_step.restype = ctypes.c_int
             lib.oracle_ssd_bwd_seq.argtypes = [i64] * 6 + [D] * 16 + [ctypes.c_int]
             lib.oracle_ssd_bwd_seq.restype = ctypes.c_int
+            lib.oracle_s6_fwd_seq.argtypes = [i64] * 5 + [D] * 9
+            lib.oracle_s6_fwd_seq.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -174,3 +178,18 @@ def ssd_bwd_seq(x, dt, A, Bm, Cm, D, dy, h0=None, dh_final=None, nthreads=None):
     if rc != 0:
         raise ValueError(f"oracle_ssd_bwd_seq failed ({rc})")
     return out
+
+
+def s6_fwd_seq(x, delta, A, Bm, Cm, D=None, h0=None):
+    """Mamba-1 selective scan (S6).  x, delta [B, dim, L]; A [dim, N]; Bm, Cm [B, G, N, L];
+    D [dim] or None; h0 [B, dim, N] or None.  Returns (y [B, dim, L], h_final [B, dim, N])."""
+    x, delta, A, Bm, Cm, D, h0 = map(_f64, (x, delta, A, Bm, Cm, D, h0))
+    batch, dim, seqlen = x.shape
+    ngroups, N = Bm.shape[1], Bm.shape[2]
+    y = np.zeros((batch, dim, seqlen))
+    hf = np.zeros((batch, dim, N))
+    rc = _load().oracle_s6_fwd_seq(batch, seqlen, dim, N, ngroups, _ptr(x), _ptr(delta), _ptr(A), _ptr(Bm),
+                                   _ptr(Cm), _ptr(D), _ptr(h0), _ptr(y), _ptr(hf))
+    if rc != 0:
+        raise ValueError(f"oracle_s6_fwd_seq failed ({rc})")
+    return y, hf

@@ -520,3 +520,55 @@ int oracle_ssd_bwd_seq(int64_t batch, int64_t seqlen, int64_t nheads, int64_t H,
     free(j.dD_pair);
     return rc;
 }
+
+/* ---------------------------------------------------------------------------
+ * Mamba-1 selective scan (S6), forward: "Sasha Rush: Mamba: The Hard Way"
+ * (Korean translation), Part 5.  Each channel d carries a vector state of N
+ * entries with its own continuous-time A[d][n]; the step size delta and the
+ * input-dependent B, C vary per token.  Per token the parameters are first
+ * discretised (the page's discretize):
+ *     abar = exp(delta_t A[d][n]),   bbar = delta_t B_t[n]
+ * and then the plain recurrence runs (the page's mamba_torch loop):
+ *     h[n] = abar h[n] + bbar x_t,   y_t = sum_n C_t[n] h[n]  (+ D[d] x_t)
+ * Channels map to B/C groups as group = d / (dim / ngroups).  The skip term
+ * D is an addition of this library's interface (NULL: none), as are h0 and
+ * h_final (NULL: zeros / not written).
+ *
+ * Layouts (time innermost, the page's (batch, ., channel, token) order):
+ *   x, delta, y  [batch][dim][seqlen]
+ *   A            [dim][dstate]
+ *   Bm, Cm       [batch][ngroups][dstate][seqlen]
+ *   D            [dim]
+ *   h0, hf       [batch][dim][dstate]
+ * ------------------------------------------------------------------------- */
+int oracle_s6_fwd_seq(int64_t batch, int64_t seqlen, int64_t dim, int64_t N, int64_t ngroups,
+                      const double *x, const double *delta, const double *A, const double *Bm,
+                      const double *Cm, const double *D, const double *h0, double *y, double *h_final)
+{
+    if (batch < 0 || seqlen < 0 || dim < 0 || N <= 0 || ngroups <= 0 || (dim % ngroups) != 0) return -1;
+    const int64_t cpg = ngroups ? dim / ngroups : 1;
+    double *h = (double *)malloc((size_t)N * sizeof(double));
+    if (!h) return -2;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t g = d / cpg;
+            for (int64_t n = 0; n < N; ++n) h[n] = h0 ? h0[(b * dim + d) * N + n] : 0.0;
+            for (int64_t t = 0; t < seqlen; ++t) {
+                const double xt = x[(b * dim + d) * seqlen + t];
+                const double dl = delta[(b * dim + d) * seqlen + t];
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    const double abar = exp(dl * A[d * N + n]);
+                    const double bbar = dl * Bm[((b * ngroups + g) * N + n) * seqlen + t];
+                    h[n] = abar * h[n] + bbar * xt;
+                    acc += Cm[((b * ngroups + g) * N + n) * seqlen + t] * h[n];
+                }
+                y[(b * dim + d) * seqlen + t] = acc + (D ? D[d] * xt : 0.0);
+            }
+            if (h_final)
+                for (int64_t n = 0; n < N; ++n) h_final[(b * dim + d) * N + n] = h[n];
+        }
+    }
+    free(h);
+    return 0;
+}

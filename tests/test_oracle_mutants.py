@@ -3,8 +3,8 @@
 Each case copies ssd_oracle.c, plants one plausible mistake by text
 substitution (a dropped term, a wrong sign, a wrong index or mask, a swapped
 operand), builds the copy with gcc into a temporary directory, swaps it in as
-the oracle library and runs the pin suites of test_oracle_pins.py and
-test_oracle_bwd_pins.py.  At least
+the oracle library and runs the pin suites of test_oracle_pins.py,
+test_oracle_bwd_pins.py and test_oracle_s6_pins.py.  At least
 one pin must fail for every mutant.  All of this runs on the CPU.
 """
 import ctypes
@@ -16,6 +16,7 @@ import pytest
 import oracle
 from tests import test_oracle_bwd_pins as bwd_pins
 from tests import test_oracle_pins as pins
+from tests import test_oracle_s6_pins as s6_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ssd_oracle.c")
 
@@ -84,6 +85,22 @@ MUTANTS = {
     "bwd-dD-drops-x": (
         "dD += dyp * j->x[BIX_X(j, b, t, h, p)];",
         "dD += dyp;"),
+    # Mamba-1 selective scan (oracle_s6_fwd_seq)
+    "s6-A-transposed": (
+        "const double abar = exp(dl * A[d * N + n]);",
+        "const double abar = exp(dl * A[(n * dim + d) % (dim * N)]);"),
+    "s6-bbar-missing-delta": (
+        "const double bbar = dl * Bm[((b * ngroups + g) * N + n) * seqlen + t];",
+        "const double bbar = Bm[((b * ngroups + g) * N + n) * seqlen + t];"),
+    "s6-output-uses-previous-state": (
+        "h[n] = abar * h[n] + bbar * xt;\n                    acc += Cm[((b * ngroups + g) * N + n) * seqlen + t] * h[n];",
+        "acc += Cm[((b * ngroups + g) * N + n) * seqlen + t] * h[n];\n                    h[n] = abar * h[n] + bbar * xt;"),
+    "s6-wrong-group": (
+        "const int64_t g = d / cpg;\n            for (int64_t n = 0; n < N; ++n) h[n] = h0",
+        "const int64_t g = d % ngroups;\n            for (int64_t n = 0; n < N; ++n) h[n] = h0"),
+    "s6-skip-dropped": (
+        "y[(b * dim + d) * seqlen + t] = acc + (D ? D[d] * xt : 0.0);",
+        "y[(b * dim + d) * seqlen + t] = acc;"),
     "bwd-dh-final-ignored": (
         "lam[p * S + s] = j->dhf ? j->dhf[BIX_H(j, b, h, p, s)] : 0.0;",
         "lam[p * S + s] = 0.0;"),
@@ -92,7 +109,7 @@ MUTANTS = {
 
 def _pin_functions():
     out = []
-    for mod, name in [(m, n) for m in (pins, bwd_pins) for n in dir(m)]:
+    for mod, name in [(m, n) for m in (pins, bwd_pins, s6_pins) for n in dir(m)]:
         if not name.startswith("test_"):
             continue
         fn = getattr(mod, name)
@@ -119,7 +136,8 @@ def test_planted_mistake_is_caught(mutant, tmp_path, monkeypatch):
                     "-lpthread", "-lm"], check=True)
     real = oracle._load()
     lib = ctypes.CDLL(str(so))
-    for fname in ("oracle_ssd_fwd_seq", "oracle_ssd_fwd_chunked", "oracle_ssd_step", "oracle_ssd_bwd_seq"):
+    for fname in ("oracle_ssd_fwd_seq", "oracle_ssd_fwd_chunked", "oracle_ssd_step", "oracle_ssd_bwd_seq",
+                  "oracle_s6_fwd_seq"):
         getattr(lib, fname).argtypes = getattr(real, fname).argtypes
         getattr(lib, fname).restype = getattr(real, fname).restype
     monkeypatch.setattr(oracle, "_lib", lib)
