@@ -436,6 +436,134 @@ def run_bwd(args, shape):
     print(json.dumps(line), flush=True)
 
 
+S6_METRIC = "s6_fwd_tokens_per_s"
+# exp2 rate of the special-function units: 152 SMs x 32 per clock (the doubled exponential rate of this
+# Blackwell part; 16 per clock on earlier parts) x 2070 MHz
+SFU_EX2_PER_S = 152 * 32 * 2.070e9
+
+
+def s6_cpu_baseline(inp, budget_s: float):
+    """The S6 oracle as it stands on sampled channels at full length, on every core: each oracle call
+    scans one channel (ctypes releases the interpreter lock), and a thread pool runs one call per core."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    s = inp.shape
+    cores = oracle.default_threads()
+    cpg = s.dim // s.ngroups
+    t = inp.tensors()
+
+    def one(i):
+        b, d = i % s.batch, (i * 7919) % s.dim
+        g = d // cpg
+        oracle.s6_fwd_seq(t["x"][b:b + 1, d:d + 1], t["delta"][b:b + 1, d:d + 1], t["A"][d:d + 1],
+                          t["B"][b:b + 1, g:g + 1], t["C"][b:b + 1, g:g + 1],
+                          None if t["D"] is None else t["D"][d:d + 1],
+                          None if t["h0"] is None else t["h0"][b:b + 1, d:d + 1])
+
+    done, t0 = 0, time.perf_counter()
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        while time.perf_counter() - t0 < budget_s:
+            list(ex.map(one, range(done, done + cores)))
+            done += cores
+    el = time.perf_counter() - t0
+    tok = done * s.seqlen / s.dim                             # channels -> whole-workload tokens (B L per B dim)
+    return {"value": tok / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} channels (workload has {s.batch * s.dim}) at full length L={s.seqlen}, sequential "
+                      f"float64 recurrence, {el:.1f} s; tokens/s scaled to the whole workload"}
+
+
+def run_s6(args, shape):
+    """ssd_s6_fwd throughput: inputs resident; one step = the scan of every channel of the batch."""
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        import oracle
+        oracle.build()
+        inp = workloads.make_s6_inputs(shape)
+        vals = [s6_cpu_baseline(inp, max(1.0, args.ref_step_s)) for _ in range(args.warmup + args.steps)][args.warmup:]
+        tok = statistics.median(v["value"] for v in vals)
+        print(json.dumps({"impl": "reference", "metric": S6_METRIC, "value": tok, "unit": "tokens/s", "n_gpus": 1,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": shape.tokens / tok * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": {"workload": shape.name},
+                          "cpu_baseline": dict(vals[0], value=tok),
+                          "e2e": {"value": tok, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                          "gpu_launches": 0}), flush=True)
+        return
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from selective_state_space_gb300 import api
+    from selective_state_space_gb300.build import build
+    build()
+    inp = workloads.make_s6_inputs(shape)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.tensors().items()}
+    y = torch.empty_like(d["x"])
+    stream = torch.cuda.current_stream(dev)
+    e = esize(shape.dtype)
+    nx = shape.batch * shape.dim * shape.seqlen
+    nbc = shape.batch * shape.ngroups * shape.dstate * shape.seqlen
+    state = shape.batch * shape.dim * shape.dstate * 4
+    alg = 3 * nx * e + 2 * nbc * e + shape.dim * shape.dstate * 4 + (shape.dim * 4 if shape.skip else 0) \
+        + (state if shape.h0 else 0) + state
+    exps = nx * shape.dstate
+    flush = alg < 2 * L2_BYTES
+    scrub = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev) if flush else None
+    hf = torch.empty((shape.batch, shape.dim, shape.dstate), dtype=torch.float32, device=dev)
+
+    def step():
+        api.s6_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["h0"], y=y, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        ms = 0.0
+        if not flush:
+            start.record(stream)
+            for _ in range(args.steps):
+                step()
+            end.record(stream)
+            torch.cuda.synchronize()
+            ms = start.elapsed_time(end)
+        else:
+            for i in range(args.steps):
+                scrub.fill_(i & 0xff)
+                start.record(stream)
+                step()
+                end.record(stream)
+                torch.cuda.synchronize()
+                ms += start.elapsed_time(end)
+    ms_per_step = ms / args.steps
+    sec = ms_per_step * 1e-3
+    peaks, peak_kind = load_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    t_hbm, t_sfu = alg / (hbm_peak * 1e9), exps / SFU_EX2_PER_S
+    if t_hbm >= t_sfu:
+        roof = {"bound": "hbm", "achieved": alg / sec / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                "frac": alg / sec / 1e9 / hbm_peak, "peak_source": f"{peak_kind} hbm_gbs"}
+    else:
+        roof = {"bound": "alu", "achieved": exps / sec / 1e12, "peak": SFU_EX2_PER_S / 1e12, "unit": "Tex2/s",
+                "frac": exps / sec / SFU_EX2_PER_S,
+                "peak_source": "derived: 152 SMs x 32 exp2 per clock x 2070 MHz (special-function units)"}
+    roof.update({"kernel": "k_s6_scan", "alg_bytes_per_launch": alg, "exp2_per_launch": exps, "traffic": None,
+                 "hbm_frac": alg / sec / 1e9 / hbm_peak, "sfu_frac": exps / sec / SFU_EX2_PER_S})
+    line = {
+        "metric": S6_METRIC, "value": shape.tokens / sec, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 (state and arithmetic), " + shape.dtype + " (x, delta, B, C, y)",
+        "data": "synthetic",
+        "config": {"workload": shape.name, "batch": shape.batch, "seqlen": shape.seqlen, "dim": shape.dim,
+                   "dstate": shape.dstate, "ngroups": shape.ngroups, "input_dtype": shape.dtype,
+                   "l2": ("flushed between steps: each step timed alone after writing a 512 MB buffer" if flush
+                          else "no flush: compulsory I/O per step exceeds twice the 129 MB L2")},
+        "roofline": roof, "e2e": None, "gpu_launches": args.steps, "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = s6_cpu_baseline(inp, args.cpu_budget_s)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,6 +584,9 @@ def main():
             print(json.dumps({"impl": "reference", "unavailable": "the decode workloads time ssd_step only"}))
             return
         run_decode(args, dshape)
+        return
+    if args.workload.startswith("s6-"):
+        run_s6(args, workloads.s6_by_name(args.workload))
         return
     shape = workloads.by_name(args.workload)
     if args.which == "bwd":

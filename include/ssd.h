@@ -225,6 +225,35 @@ ssd_status ssd_bwd(const ssd_desc *desc, const void *x, const void *dt, const fl
                    void *dB, void *dC, float *dD, float *dh0, void *workspace, size_t ws_bytes,
                    ssd_stream_t stream);
 
+/* ---- Mamba-1 selective scan (S6), forward --------------------------------
+ * "Sasha Rush: Mamba: The Hard Way", Part 5: each channel d has a vector
+ * state of N entries with its own A[d][n]; per token the step is discretised,
+ *     abar = exp(delta_t A[d][n]),   bbar = delta_t B_t[n],
+ * and the recurrence h[n] = abar h[n] + bbar x_t, y_t = sum_n C_t[n] h[n]
+ * (+ D[d] x_t) runs over the tokens.  Channel d reads B/C group d / (dim / G).
+ * Layouts (time innermost):
+ *   x, delta, y  [B][dim][L]   (in, in, out dtype)      A   [dim][N] float32
+ *   Bm, Cm       [B][G][N][L]  in dtype                 D   [dim] float32, nullable (no skip)
+ *   h0, h_final  [B][dim][N]   float32, nullable (zeros / not written)
+ * delta is the positive step (no softplus or bias applied inside).
+ * Limits: 1 <= N <= 32, G divides dim, B <= 65535.  Pointers aligned to their
+ * element size; y must not overlap an input.  Deterministic. */
+typedef struct {
+    int64_t batch;      /* B >= 0 */
+    int64_t seqlen;     /* L >= 0 */
+    int64_t dim;        /* channels >= 0, a multiple of ngroups */
+    int64_t dstate;     /* N in [1, 32] */
+    int64_t ngroups;    /* G >= 1 */
+    int32_t in_dtype;   /* ssd_dtype of x, delta, Bm, Cm */
+    int32_t out_dtype;  /* ssd_dtype of y */
+    int32_t flags;      /* must be 0 */
+    int32_t reserved;   /* must be 0 */
+} ssd_s6_desc;
+
+ssd_status ssd_s6_fwd(const ssd_s6_desc *desc, const void *x, const void *delta, const float *A, const void *Bm,
+                  const void *Cm, const float *D, const float *h0, void *y, float *h_final,
+                  ssd_stream_t stream);
+
 /* ---- Forward pass for callers that cannot allocate device memory ---------
  * (The pages have no counterpart to this entry point: it is a deployment aid.)
  *

@@ -19,7 +19,7 @@ EXPORTS = ("ssd_status_string", "ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_f
            "ssd_fwd_check",
            "ssd_step",
            "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_bwd_workspace_size",
-           "ssd_bwd", "ssd_fwd_noalloc")
+           "ssd_bwd", "ssd_s6_fwd", "ssd_fwd_noalloc")
 
 
 class Desc(ctypes.Structure):
@@ -27,6 +27,12 @@ class Desc(ctypes.Structure):
                 ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
                 ("chunk", ctypes.c_int64), ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
                 ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class S6Desc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("dim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64), ("in_dtype", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32), ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):
@@ -87,6 +93,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ssd_bwd_workspace_size.restype = st
         lib.ssd_bwd.argtypes = [DP] + [P] * 17 + [ctypes.c_size_t, P]
         lib.ssd_bwd.restype = st
+        lib.ssd_s6_fwd.argtypes = [ctypes.POINTER(S6Desc)] + [P] * 10
+        lib.ssd_s6_fwd.restype = st
         _lib = lib
         return lib
 

@@ -165,6 +165,25 @@ def ssd_bwd(x, dt, A, B, C, D, dy, chunk: int, h0=None, dh_final=None, *, want_d
     return out
 
 
+def s6_fwd(x, delta, A, B, C, D=None, h0=None, *, y=None, want_h_final=True, out_dtype=None, stream=None):
+    """Mamba-1 selective scan (S6).  x, delta [B, dim, L] (float32 or bfloat16, same dtype);
+    A [dim, N] float32; B, C [B, G, N, L] (input dtype); D [dim] float32 or None;
+    h0 [B, dim, N] float32 or None.  Returns (y [B, dim, L], h_final [B, dim, N] or None)."""
+    batch, dim, seqlen = x.shape
+    ngroups, dstate = B.shape[1], B.shape[2]
+    d = _native.S6Desc()
+    d.batch, d.seqlen, d.dim, d.dstate, d.ngroups = batch, seqlen, dim, dstate, ngroups
+    d.in_dtype = _dtype_code(x.dtype)
+    d.out_dtype = _dtype_code(out_dtype or x.dtype)
+    d.flags = d.reserved = 0
+    if y is None:
+        y = torch.empty((batch, dim, seqlen), dtype=out_dtype or x.dtype, device=x.device)
+    h_final = torch.empty((batch, dim, dstate), dtype=torch.float32, device=x.device) if want_h_final else None
+    check("ssd_s6_fwd", _native.load().ssd_s6_fwd(ctypes.byref(d), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                          _ptr(h0), _ptr(y), _ptr(h_final), _stream(stream)))
+    return y, h_final
+
+
 # ---- the four stages, one call each (intermediate layouts in include/ssd.h) ----
 
 def ssd_chunk_cumsum(dt, A, chunk: int, desc: Desc = None, *, G=None, stream=None):

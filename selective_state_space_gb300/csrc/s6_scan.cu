@@ -1,0 +1,177 @@
+// s6_scan.cu -- Mamba-1 selective scan (S6), forward, on the CUDA cores.
+//
+// "Sasha Rush: Mamba: The Hard Way", Part 5: per channel d and state n the step
+// is discretised, abar = exp(delta_t A[d][n]), bbar = delta_t B_t[n], and the
+// vector recurrence h[n] = abar h[n] + bbar x_t, y_t = sum_n C_t[n] h[n] runs
+// over the tokens (plus D[d] x_t when D is given).
+//
+// Each channel's N states are split over kSplit adjacent lanes (NS states each);
+// a block holds kCh = 128 / kSplit channels of one B/C group of one batch row.
+// Tiles of kTT tokens are staged through shared memory: rows of x and delta are
+// contiguous in time, so consecutive threads load consecutive tokens; B and C rows
+// of the group are shared by all channels of the block.  The next tile is loaded
+// into registers while the current one is scanned.  The scan is bound by the
+// special-function unit (one exp2 per channel, state and token) once N >= 8.
+#include "ssd_common.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kSplit = 4;              // lanes per channel
+constexpr int kThreads = 128;
+constexpr int kCh = kThreads / kSplit; // channels per block
+constexpr int kTT = 64;                // tokens per tile
+constexpr int kXP = kTT + 1;           // padded row of a channel tile
+constexpr int kLx = kCh * kTT / kThreads;   // x (and delta) elements per thread per tile
+
+template <typename Tin, typename Tout, int NS>
+__global__ void __launch_bounds__(kThreads)
+k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float *__restrict__ A,
+          const Tin *__restrict__ Bm, const Tin *__restrict__ Cm, const float *__restrict__ D,
+          const float *__restrict__ h0, Tout *__restrict__ y, float *__restrict__ h_final,
+          int64_t L, int dim, int N, int G, int blocks_per_group)
+{
+    constexpr int NP = NS * kSplit;                 // padded state count
+    constexpr int kLb = (NP * kTT + kThreads - 1) / kThreads;   // B (and C) elements per thread per tile
+    __shared__ float xs[kCh * kXP], ds[kCh * kXP], ys[kCh * kXP];
+    __shared__ float bs[NP * kXP], cs[NP * kXP];
+    const int tid = threadIdx.x;
+    const int g = blockIdx.x / blocks_per_group;
+    const int cpg = dim / G;
+    const int c0 = (blockIdx.x % blocks_per_group) * kCh;      // first channel of the block inside the group
+    const int b = blockIdx.y;
+    const int nch = min(kCh, cpg - c0);                        // channels of this block
+    const int64_t row0 = (int64_t)b * dim + (int64_t)g * cpg + c0;   // (b, d) row of the first channel
+    const Tin *Bg = Bm + ((int64_t)b * G + g) * N * L;
+    const Tin *Cg = Cm + ((int64_t)b * G + g) * N * L;
+
+    // this thread's channel and states
+    const int ch = tid / kSplit, slice = tid % kSplit;
+    const bool active = ch < nch;
+    const int d = g * cpg + c0 + (active ? ch : 0);
+    float h[NS], a2[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+        const int n = slice * NS + s;
+        const bool on = active && n < N;
+        a2[s] = on ? A[(int64_t)d * N + n] * kLog2e : 0.f;
+        h[s] = (on && h0) ? h0[((int64_t)b * dim + d) * N + n] : 0.f;
+    }
+    const float dskip = (active && D) ? D[d] : 0.f;
+
+    // global -> registers for the tile starting at t0
+    float rx[kLx], rd[kLx], rb[kLb], rc[kLb];
+    auto fetch = [&](int64_t t0) {
+#pragma unroll
+        for (int i = 0; i < kLx; ++i) {
+            const int e = i * kThreads + tid, r = e / kTT, t = e % kTT;
+            const bool on = r < nch && t0 + t < L;
+            const int64_t o = (row0 + r) * L + t0 + t;
+            rx[i] = on ? to_f32(x[o]) : 0.f;
+            rd[i] = on ? to_f32(delta[o]) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kLb; ++i) {
+            const int e = i * kThreads + tid, n = e / kTT, t = e % kTT;
+            const bool on = n < N && e < NP * kTT && t0 + t < L;
+            const int64_t o = (int64_t)n * L + t0 + t;
+            rb[i] = on ? to_f32(Bg[o]) : 0.f;
+            rc[i] = on ? to_f32(Cg[o]) : 0.f;
+        }
+    };
+    auto stage = [&]() {
+#pragma unroll
+        for (int i = 0; i < kLx; ++i) {
+            const int e = i * kThreads + tid, r = e / kTT, t = e % kTT;
+            xs[r * kXP + t] = rx[i];
+            ds[r * kXP + t] = rd[i];
+        }
+#pragma unroll
+        for (int i = 0; i < kLb; ++i) {
+            const int e = i * kThreads + tid, n = e / kTT, t = e % kTT;
+            if (e < NP * kTT) {
+                bs[n * kXP + t] = rb[i];
+                cs[n * kXP + t] = rc[i];
+            }
+        }
+    };
+
+    const int64_t ntiles = (L + kTT - 1) / kTT;
+    fetch(0);
+    stage();
+    __syncthreads();
+    for (int64_t k = 0; k < ntiles; ++k) {
+        const int64_t t0 = k * kTT;
+        if (k + 1 < ntiles) fetch(t0 + kTT);
+        const int tn = (int)min((int64_t)kTT, L - t0);
+        const float *xr = xs + ch * kXP, *dr = ds + ch * kXP;
+        for (int t = 0; t < tn; ++t) {
+            const float xv = xr[t], dv = dr[t];
+            const float dx = dv * xv;
+            float acc = 0.f;
+#pragma unroll
+            for (int s = 0; s < NS; ++s) {
+                const int n = slice * NS + s;
+                const float abar = exp2f(dv * a2[s]);
+                h[s] = fmaf(abar, h[s], dx * bs[n * kXP + t]);
+                acc = fmaf(cs[n * kXP + t], h[s], acc);
+            }
+#pragma unroll
+            for (int off = 1; off < kSplit; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (slice == 0) ys[ch * kXP + t] = fmaf(dskip, xv, acc);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kLx; ++i) {
+            const int e = i * kThreads + tid, r = e / kTT, t = e % kTT;
+            if (r < nch && t0 + t < L) y[(row0 + r) * L + t0 + t] = from_f32<Tout>(ys[r * kXP + t]);
+        }
+        if (k + 1 < ntiles) stage();
+        __syncthreads();
+    }
+    if (active && h_final) {
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+            const int n = slice * NS + s;
+            if (n < N) h_final[((int64_t)b * dim + d) * N + n] = h[s];
+        }
+    }
+}
+
+template <typename Tin, typename Tout, int NS>
+cudaError_t s6_launch_t(const S6Problem &p, const void *x, const void *delta, const float *A, const void *Bm,
+                        const void *Cm, const float *D, const float *h0, void *y, float *h_final, cudaStream_t st)
+{
+    const int cpg = (int)(p.dim / p.G);
+    const int bpg = (cpg + kCh - 1) / kCh;
+    dim3 grid((unsigned)(bpg * p.G), (unsigned)p.B);
+    k_s6_scan<Tin, Tout, NS><<<grid, kThreads, 0, st>>>((const Tin *)x, (const Tin *)delta, A, (const Tin *)Bm,
+                                                        (const Tin *)Cm, D, h0, (Tout *)y, h_final, p.L, (int)p.dim,
+                                                        (int)p.N, (int)p.G, bpg);
+    return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout>
+cudaError_t s6_launch_io(const S6Problem &p, const void *x, const void *delta, const float *A, const void *Bm,
+                         const void *Cm, const float *D, const float *h0, void *y, float *h_final, cudaStream_t st)
+{
+    const int64_t ns = (p.N + kSplit - 1) / kSplit;
+    if (ns <= 1) return s6_launch_t<Tin, Tout, 1>(p, x, delta, A, Bm, Cm, D, h0, y, h_final, st);
+    if (ns <= 2) return s6_launch_t<Tin, Tout, 2>(p, x, delta, A, Bm, Cm, D, h0, y, h_final, st);
+    if (ns <= 4) return s6_launch_t<Tin, Tout, 4>(p, x, delta, A, Bm, Cm, D, h0, y, h_final, st);
+    return s6_launch_t<Tin, Tout, 8>(p, x, delta, A, Bm, Cm, D, h0, y, h_final, st);   // N <= 32
+}
+
+}  // namespace
+
+cudaError_t launch_s6_scan(const S6Problem &p, const void *x, const void *delta, const float *A, const void *Bm,
+                           const void *Cm, const float *D, const float *h0, void *y, float *h_final, cudaStream_t st)
+{
+    const bool ib = p.in_dt == SSD_BF16, ob = p.out_dt == SSD_BF16;
+    if (ib && ob) return s6_launch_io<__nv_bfloat16, __nv_bfloat16>(p, x, delta, A, Bm, Cm, D, h0, y, h_final, st);
+    if (ib) return s6_launch_io<__nv_bfloat16, float>(p, x, delta, A, Bm, Cm, D, h0, y, h_final, st);
+    if (ob) return s6_launch_io<float, __nv_bfloat16>(p, x, delta, A, Bm, Cm, D, h0, y, h_final, st);
+    return s6_launch_io<float, float>(p, x, delta, A, Bm, Cm, D, h0, y, h_final, st);
+}
+
+}  // namespace ssd

@@ -558,6 +558,43 @@ ssd_status ssd_bwd(const ssd_desc *desc, const void *x, const void *dt, const fl
     return cuda_status(ssd::launch_bwd(pr, a, w, st));
 }
 
+ssd_status ssd_s6_fwd(const ssd_s6_desc *desc, const void *x, const void *delta, const float *A, const void *Bm,
+                  const void *Cm, const float *D, const float *h0, void *y, float *h_final, ssd_stream_t stream)
+{
+    if (!desc) return SSD_ERR_INVALID_ARG;
+    if (desc->batch < 0 || desc->seqlen < 0 || desc->dim < 0 || desc->dstate < 1 || desc->ngroups < 1 ||
+        desc->dim % desc->ngroups != 0 || desc->flags != 0 || desc->reserved != 0)
+        return SSD_ERR_INVALID_ARG;
+    if ((desc->in_dtype != SSD_F32 && desc->in_dtype != SSD_BF16) ||
+        (desc->out_dtype != SSD_F32 && desc->out_dtype != SSD_BF16))
+        return SSD_ERR_INVALID_ARG;
+    if (desc->dstate > 32 || desc->batch > 65535 || desc->dim > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
+    const ssd::S6Problem p{desc->batch, desc->seqlen, desc->dim, desc->dstate, desc->ngroups, desc->in_dtype,
+                           desc->out_dtype};
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t nstate = (size_t)(p.B * p.dim * p.N);
+    if ((h0 && !aligned(h0, 4)) || (h_final && !aligned(h_final, 4))) return SSD_ERR_INVALID_ARG;
+    if (p.B == 0 || p.dim == 0) return SSD_OK;
+    if (p.L == 0) {
+        if (h_final) {
+            cudaError_t e = h0 ? cudaMemcpyAsync(h_final, h0, nstate * sizeof(float), cudaMemcpyDeviceToDevice, st)
+                               : cudaMemsetAsync(h_final, 0, nstate * sizeof(float), st);
+            return cuda_status(e);
+        }
+        return SSD_OK;
+    }
+    if (!x || !delta || !A || !Bm || !Cm || !y) return SSD_ERR_INVALID_ARG;
+    const size_t ei = esize(p.in_dt), eo = esize(p.out_dt);
+    if (!aligned(x, ei) || !aligned(delta, ei) || !aligned(Bm, ei) || !aligned(Cm, ei) || !aligned(y, eo) ||
+        !aligned(A, 4) || (D && !aligned(D, 4)))
+        return SSD_ERR_INVALID_ARG;
+    const size_t nx = (size_t)(p.B * p.dim * p.L), nbc = (size_t)(p.B * p.G * p.N * p.L);
+    if (overlaps(y, nx * eo, x, nx * ei) || overlaps(y, nx * eo, delta, nx * ei) || overlaps(y, nx * eo, Bm, nbc * ei) ||
+        overlaps(y, nx * eo, Cm, nbc * ei) || (h_final && overlaps(h_final, nstate * 4, y, nx * eo)))
+        return SSD_ERR_INVALID_ARG;
+    return cuda_status(ssd::launch_s6_scan(p, x, delta, A, Bm, Cm, D, h0, y, h_final, st));
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

@@ -97,6 +97,14 @@ bool bwd_supported(const Problem &pr);
 size_t bwd_workspace(const Problem &pr, void *base, BwdWork *w);
 cudaError_t launch_bwd(const Problem &pr, const BwdArgs &a, const BwdWork &w, cudaStream_t st);
 
+// Mamba-1 selective scan (s6_scan.cu): validated sizes of an s6_desc.
+struct S6Problem {
+    int64_t B, L, dim, N, G;
+    int in_dt, out_dt;
+};
+cudaError_t launch_s6_scan(const S6Problem &p, const void *x, const void *delta, const float *A, const void *Bm,
+                           const void *Cm, const float *D, const float *h0, void *y, float *h_final, cudaStream_t st);
+
 cudaError_t launch_ssd_step(const Problem &pr, const void *x, const void *dt, const float *A,
                             const void *Bm, const void *Cm, const float *D, float *h, void *y,
                             cudaStream_t st);

@@ -150,3 +150,90 @@ def make_grad_inputs(shape: Shape, with_dh_final: bool = True, seed: Optional[in
     dy = torch.randn((Bsz, L, nh, H), generator=g, dtype=torch.float32).to(torch_dtype(shape.dtype))
     dhf = 0.1 * torch.randn((Bsz, nh, H, S), generator=g, dtype=torch.float32) if with_dh_final else None
     return GradInputs(dy.contiguous(), None if dhf is None else dhf.contiguous())
+
+
+# ---- Mamba-1 selective scan (S6) workloads ----
+
+@dataclasses.dataclass(frozen=True)
+class S6Shape:
+    name: str
+    batch: int
+    seqlen: int
+    dim: int           # channels (d_inner)
+    dstate: int        # N
+    ngroups: int
+    dtype: str         # "f32" or "bf16": x, delta, B, C and y
+    recipe: str        # "hardway" (the page's create()) or "mamba1" (see make_s6_inputs)
+    skip: bool         # D present
+    h0: bool
+    seed: int
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.seqlen
+
+
+S6_WORKLOADS = [
+    # the timing run of "Mamba: The Hard Way", Part 5: mamba(*create(S=2048, Ba=8, D=1024, N=4))
+    S6Shape("s6-hardway-run", 8, 2048, 1024, 4, 1, "f32", "hardway", False, False, 20),
+    # a Mamba-1 130M-shaped layer: d_inner 1536, N = 16
+    S6Shape("s6-mamba-130m-layer", 8, 2048, 1536, 16, 1, "bf16", "mamba1", True, False, 21),
+]
+
+
+def s6_by_name(name: str) -> S6Shape:
+    for s in S6_WORKLOADS:
+        if s.name == name:
+            return s
+    raise KeyError(name)
+
+
+def s6_custom(batch, seqlen, dim, dstate, ngroups=1, dtype="f32", recipe="mamba1", skip=True, h0=True, seed=0,
+              name="s6-custom") -> S6Shape:
+    return S6Shape(name, batch, seqlen, dim, dstate, ngroups, dtype, recipe, skip, h0, seed)
+
+
+@dataclasses.dataclass
+class S6Inputs:
+    shape: S6Shape
+    x: torch.Tensor               # [B, dim, L]      input dtype
+    delta: torch.Tensor           # [B, dim, L]      input dtype (positive)
+    A: torch.Tensor               # [dim, N]         float32 (negative)
+    B: torch.Tensor               # [B, G, N, L]     input dtype
+    C: torch.Tensor               # [B, G, N, L]     input dtype
+    D: Optional[torch.Tensor]     # [dim]            float32 or None
+    h0: Optional[torch.Tensor]    # [B, dim, N]      float32 or None
+
+    def tensors(self):
+        return dict(x=self.x, delta=self.delta, A=self.A, B=self.B, C=self.C, D=self.D, h0=self.h0)
+
+
+def make_s6_inputs(shape: S6Shape, seed: Optional[int] = None) -> S6Inputs:
+    """Draw one selective-scan workload on the CPU, in the order x, delta, A, B, C, D, h0.
+
+    "hardway": the page's create(): x ~ U(0, 1), A = -1, B = 0.1, C ~ 0.1 U(0, 1),
+    delta ~ 0.1 U(0, 1).  "mamba1": x ~ N(0, 1), delta = exp(U(log 1e-3, log 1e-1)),
+    A[d][n] = -(n + 1) U(0.5, 1.5), B, C ~ N(0, 1), D ~ N(1, 0.1), h0 ~ N(0, 0.1)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(shape.seed if seed is None else seed)
+    Bsz, L, dim, N, G = shape.batch, shape.seqlen, shape.dim, shape.dstate, shape.ngroups
+    f32, dt_ = torch.float32, torch_dtype(shape.dtype)
+    if shape.recipe == "hardway":
+        x = torch.rand((Bsz, dim, L), generator=g, dtype=f32)
+        delta = 0.1 * torch.rand((Bsz, dim, L), generator=g, dtype=f32)
+        A = -torch.ones((dim, N), dtype=f32)
+        Bm = torch.full((Bsz, G, N, L), 0.1, dtype=f32)
+        Cm = 0.1 * torch.rand((Bsz, G, N, L), generator=g, dtype=f32)
+    elif shape.recipe == "mamba1":
+        x = torch.randn((Bsz, dim, L), generator=g, dtype=f32)
+        lo, hi = math.log(1e-3), math.log(1e-1)
+        delta = torch.exp(lo + (hi - lo) * torch.rand((Bsz, dim, L), generator=g, dtype=f32))
+        A = -(torch.arange(1, N + 1, dtype=f32)[None, :] * (0.5 + torch.rand((dim, N), generator=g, dtype=f32)))
+        Bm = torch.randn((Bsz, G, N, L), generator=g, dtype=f32)
+        Cm = torch.randn((Bsz, G, N, L), generator=g, dtype=f32)
+    else:
+        raise ValueError(shape.recipe)
+    D = (1.0 + 0.1 * torch.randn((dim,), generator=g, dtype=f32)) if shape.skip else None
+    h0 = 0.1 * torch.randn((Bsz, dim, N), generator=g, dtype=f32) if shape.h0 else None
+    return S6Inputs(shape, x.to(dt_).contiguous(), delta.to(dt_).contiguous(), A.contiguous(),
+                    Bm.to(dt_).contiguous(), Cm.to(dt_).contiguous(), D, h0)
