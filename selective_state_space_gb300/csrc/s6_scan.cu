@@ -10,8 +10,11 @@
 // Tiles of kTT tokens are staged through shared memory: rows of x and delta are
 // contiguous in time, so consecutive threads load consecutive tokens; B and C rows
 // of the group are shared by all channels of the block.  The next tile is loaded
-// into registers while the current one is scanned.  The scan is bound by the
-// special-function unit (one exp2 per channel, state and token) once N >= 8.
+// into registers while the current one is scanned.  Each lane records its partial
+// sum of C h per token in shared memory; the output pass adds the kSplit partials
+// and D x and writes y coalesced, so the token loop carries no shuffle.  The scan
+// is bound by the special-function unit (one exp2 per channel, state and token)
+// once N >= 8.
 #include "ssd_common.cuh"
 
 namespace ssd {
@@ -24,6 +27,24 @@ constexpr int kTT = 64;                // tokens per tile
 constexpr int kXP = kTT + 1;           // padded row of a channel tile
 constexpr int kLx = kCh * kTT / kThreads;   // x (and delta) elements per thread per tile
 
+__device__ __forceinline__ float fast_exp2(float v)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Shared memory of one block (dynamic): the channel tile as (x, delta) pairs, the group's
+// (B, C) pairs per state, and each lane's partial sum of C h per channel and token.
+template <int NS>
+struct S6Smem {
+    static constexpr int NP = NS * kSplit;     // padded state count
+    static constexpr size_t xd = (size_t)kCh * kXP;            // float2
+    static constexpr size_t bc = (size_t)NP * kXP;             // float2
+    static constexpr size_t yp = (size_t)kSplit * kCh * kXP;   // float
+    static constexpr size_t bytes = 8 * (xd + bc) + 4 * yp;
+};
+
 template <typename Tin, typename Tout, int NS>
 __global__ void __launch_bounds__(kThreads)
 k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float *__restrict__ A,
@@ -31,10 +52,13 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
           const float *__restrict__ h0, Tout *__restrict__ y, float *__restrict__ h_final,
           int64_t L, int dim, int N, int G, int blocks_per_group)
 {
-    constexpr int NP = NS * kSplit;                 // padded state count
+    using Sm = S6Smem<NS>;
+    constexpr int NP = Sm::NP;
     constexpr int kLb = (NP * kTT + kThreads - 1) / kThreads;   // B (and C) elements per thread per tile
-    __shared__ float xs[kCh * kXP], ds[kCh * kXP], ys[kCh * kXP];
-    __shared__ float bs[NP * kXP], cs[NP * kXP];
+    extern __shared__ float4 s6_smem[];
+    float2 *xd = reinterpret_cast<float2 *>(s6_smem);          // [kCh][kXP]  (x, delta)
+    float2 *bc = xd + Sm::xd;                                   // [NP][kXP]   (B, C)
+    float *yp = reinterpret_cast<float *>(bc + Sm::bc);         // [kSplit][kCh][kXP]
     const int tid = threadIdx.x;
     const int g = blockIdx.x / blocks_per_group;
     const int cpg = dim / G;
@@ -57,7 +81,6 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
         a2[s] = on ? A[(int64_t)d * N + n] * kLog2e : 0.f;
         h[s] = (on && h0) ? h0[((int64_t)b * dim + d) * N + n] : 0.f;
     }
-    const float dskip = (active && D) ? D[d] : 0.f;
 
     // global -> registers for the tile starting at t0
     float rx[kLx], rd[kLx], rb[kLb], rc[kLb];
@@ -83,17 +106,30 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
 #pragma unroll
         for (int i = 0; i < kLx; ++i) {
             const int e = i * kThreads + tid, r = e / kTT, t = e % kTT;
-            xs[r * kXP + t] = rx[i];
-            ds[r * kXP + t] = rd[i];
+            xd[r * kXP + t] = make_float2(rx[i], rd[i]);
         }
 #pragma unroll
         for (int i = 0; i < kLb; ++i) {
             const int e = i * kThreads + tid, n = e / kTT, t = e % kTT;
-            if (e < NP * kTT) {
-                bs[n * kXP + t] = rb[i];
-                cs[n * kXP + t] = rc[i];
-            }
+            if (e < NP * kTT) bc[n * kXP + t] = make_float2(rb[i], rc[i]);
         }
+    };
+    // one token: update this lane's states, record its partial sum of C h
+    const float2 *xr = xd + ch * kXP;
+    const float2 *bcr = bc + (slice * NS) * kXP;
+    float *ypr = yp + (slice * kCh + ch) * kXP;
+    auto token = [&](int t) {
+        const float2 v = xr[t];
+        const float dx = v.y * v.x;
+        float acc = 0.f;
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+            const float2 q = bcr[s * kXP + t];
+            const float abar = fast_exp2(v.y * a2[s]);
+            h[s] = fmaf(abar, h[s], dx * q.x);
+            acc = fmaf(q.y, h[s], acc);
+        }
+        ypr[t] = acc;
     };
 
     const int64_t ntiles = (L + kTT - 1) / kTT;
@@ -104,30 +140,29 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
         const int64_t t0 = k * kTT;
         if (k + 1 < ntiles) fetch(t0 + kTT);
         const int tn = (int)min((int64_t)kTT, L - t0);
-        const float *xr = xs + ch * kXP, *dr = ds + ch * kXP;
-        for (int t = 0; t < tn; ++t) {
-            const float xv = xr[t], dv = dr[t];
-            const float dx = dv * xv;
-            float acc = 0.f;
-#pragma unroll
-            for (int s = 0; s < NS; ++s) {
-                const int n = slice * NS + s;
-                const float abar = exp2f(dv * a2[s]);
-                h[s] = fmaf(abar, h[s], dx * bs[n * kXP + t]);
-                acc = fmaf(cs[n * kXP + t], h[s], acc);
-            }
-#pragma unroll
-            for (int off = 1; off < kSplit; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (slice == 0) ys[ch * kXP + t] = fmaf(dskip, xv, acc);
+        if (tn == kTT) {
+#pragma unroll 8
+            for (int t = 0; t < kTT; ++t) token(t);
+        } else {
+            for (int t = 0; t < tn; ++t) token(t);
         }
         __syncthreads();
+        // y = D x + the kSplit partial sums, written back coalesced
 #pragma unroll
         for (int i = 0; i < kLx; ++i) {
             const int e = i * kThreads + tid, r = e / kTT, t = e % kTT;
-            if (r < nch && t0 + t < L) y[(row0 + r) * L + t0 + t] = from_f32<Tout>(ys[r * kXP + t]);
+            if (r < nch && t0 + t < L) {
+                float acc = D ? D[g * cpg + c0 + r] * xd[r * kXP + t].x : 0.f;
+#pragma unroll
+                for (int sl = 0; sl < kSplit; ++sl) acc += yp[(sl * kCh + r) * kXP + t];
+                y[(row0 + r) * L + t0 + t] = from_f32<Tout>(acc);
+            }
         }
-        if (k + 1 < ntiles) stage();
         __syncthreads();
+        if (k + 1 < ntiles) {
+            stage();
+            __syncthreads();
+        }
     }
     if (active && h_final) {
 #pragma unroll
@@ -145,7 +180,11 @@ cudaError_t s6_launch_t(const S6Problem &p, const void *x, const void *delta, co
     const int cpg = (int)(p.dim / p.G);
     const int bpg = (cpg + kCh - 1) / kCh;
     dim3 grid((unsigned)(bpg * p.G), (unsigned)p.B);
-    k_s6_scan<Tin, Tout, NS><<<grid, kThreads, 0, st>>>((const Tin *)x, (const Tin *)delta, A, (const Tin *)Bm,
+    auto kern = k_s6_scan<Tin, Tout, NS>;
+    const size_t smem = S6Smem<NS>::bytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, st>>>((const Tin *)x, (const Tin *)delta, A, (const Tin *)Bm,
                                                         (const Tin *)Cm, D, h0, (Tout *)y, h_final, p.L, (int)p.dim,
                                                         (int)p.N, (int)p.G, bpg);
     return cudaGetLastError();
