@@ -35,14 +35,15 @@ __device__ __forceinline__ float fast_exp2(float v)
 }
 
 // Shared memory of one block (dynamic): the channel tile as (x, delta) pairs, the group's
-// (B, C) pairs per state, and each lane's partial sum of C h per channel and token.
+// (B, C) pairs per state, each lane's partial sum of C h per channel and token (the four
+// lanes of a channel write four different banks), and D of the block's channels.
 template <int NS>
 struct S6Smem {
     static constexpr int NP = NS * kSplit;     // padded state count
     static constexpr size_t xd = (size_t)kCh * kXP;            // float2
     static constexpr size_t bc = (size_t)NP * kXP;             // float2
     static constexpr size_t yp = (size_t)kSplit * kCh * kXP;   // float
-    static constexpr size_t bytes = 8 * (xd + bc) + 4 * yp;
+    static constexpr size_t bytes = 8 * (xd + bc) + 4 * (yp + kCh);
 };
 
 template <typename Tin, typename Tout, int NS>
@@ -58,7 +59,8 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
     extern __shared__ float4 s6_smem[];
     float2 *xd = reinterpret_cast<float2 *>(s6_smem);          // [kCh][kXP]  (x, delta)
     float2 *bc = xd + Sm::xd;                                   // [NP][kXP]   (B, C)
-    float *yp = reinterpret_cast<float *>(bc + Sm::bc);         // [kSplit][kCh][kXP]
+    float *yp = reinterpret_cast<float *>(bc + Sm::bc);         // [kCh][kSplit][kXP]
+    float *dsk = yp + Sm::yp;                                   // [kCh]  D of the block's channels
     const int tid = threadIdx.x;
     const int g = blockIdx.x / blocks_per_group;
     const int cpg = dim / G;
@@ -82,42 +84,52 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
         h[s] = (on && h0) ? h0[((int64_t)b * dim + d) * N + n] : 0.f;
     }
 
-    // global -> registers for the tile starting at t0
-    float rx[kLx], rd[kLx], rb[kLb], rc[kLb];
+    // global -> registers for the tile starting at t0, kept in the input dtype: nothing consumes the
+    // loads until stage() converts them, after the current tile's scan
+    const Tin zero = from_f32<Tin>(0.f);
+    Tin rx[kLx], rd[kLx], rb[kLb], rc[kLb];
     auto fetch = [&](int64_t t0) {
 #pragma unroll
         for (int i = 0; i < kLx; ++i) {
             const int e = i * kThreads + tid, r = e / kTT, t = e % kTT;
             const bool on = r < nch && t0 + t < L;
             const int64_t o = (row0 + r) * L + t0 + t;
-            rx[i] = on ? to_f32(x[o]) : 0.f;
-            rd[i] = on ? to_f32(delta[o]) : 0.f;
+            rx[i] = zero;
+            rd[i] = zero;
+            if (on) {
+                rx[i] = x[o];
+                rd[i] = delta[o];
+            }
         }
 #pragma unroll
         for (int i = 0; i < kLb; ++i) {
             const int e = i * kThreads + tid, n = e / kTT, t = e % kTT;
             const bool on = n < N && e < NP * kTT && t0 + t < L;
             const int64_t o = (int64_t)n * L + t0 + t;
-            rb[i] = on ? to_f32(Bg[o]) : 0.f;
-            rc[i] = on ? to_f32(Cg[o]) : 0.f;
+            rb[i] = zero;
+            rc[i] = zero;
+            if (on) {
+                rb[i] = Bg[o];
+                rc[i] = Cg[o];
+            }
         }
     };
     auto stage = [&]() {
 #pragma unroll
         for (int i = 0; i < kLx; ++i) {
             const int e = i * kThreads + tid, r = e / kTT, t = e % kTT;
-            xd[r * kXP + t] = make_float2(rx[i], rd[i]);
+            xd[r * kXP + t] = make_float2(to_f32(rx[i]), to_f32(rd[i]));
         }
 #pragma unroll
         for (int i = 0; i < kLb; ++i) {
             const int e = i * kThreads + tid, n = e / kTT, t = e % kTT;
-            if (e < NP * kTT) bc[n * kXP + t] = make_float2(rb[i], rc[i]);
+            if (e < NP * kTT) bc[n * kXP + t] = make_float2(to_f32(rb[i]), to_f32(rc[i]));
         }
     };
     // one token: update this lane's states, record its partial sum of C h
     const float2 *xr = xd + ch * kXP;
     const float2 *bcr = bc + (slice * NS) * kXP;
-    float *ypr = yp + (slice * kCh + ch) * kXP;
+    float *ypr = yp + (ch * kSplit + slice) * kXP;
     auto token = [&](int t) {
         const float2 v = xr[t];
         const float dx = v.y * v.x;
@@ -133,6 +145,7 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
     };
 
     const int64_t ntiles = (L + kTT - 1) / kTT;
+    if (tid < kCh) dsk[tid] = (D && tid < nch) ? D[g * cpg + c0 + tid] : 0.f;
     fetch(0);
     stage();
     __syncthreads();
@@ -152,9 +165,9 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
         for (int i = 0; i < kLx; ++i) {
             const int e = i * kThreads + tid, r = e / kTT, t = e % kTT;
             if (r < nch && t0 + t < L) {
-                float acc = D ? D[g * cpg + c0 + r] * xd[r * kXP + t].x : 0.f;
+                float acc = dsk[r] * xd[r * kXP + t].x;
 #pragma unroll
-                for (int sl = 0; sl < kSplit; ++sl) acc += yp[(sl * kCh + r) * kXP + t];
+                for (int sl = 0; sl < kSplit; ++sl) acc += yp[(r * kSplit + sl) * kXP + t];
                 y[(row0 + r) * L + t0 + t] = from_f32<Tout>(acc);
             }
         }
