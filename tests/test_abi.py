@@ -166,3 +166,103 @@ def test_timed_variant_requires_events(lib):
     a = 1 << 20
     assert lib.ssd_fwd_timed(ctypes.byref(d), a, a, a, a, a, a, None, 1 << 30, None, 1 << 34, 1 << 40, None,
                              None) == 1
+
+
+# ---- gradient pass and selective scan: host-side validation (nothing is launched) ----
+
+def bwd_ws(lib, d):
+    n = ctypes.c_size_t(0)
+    rc = lib.ssd_bwd_workspace_size(ctypes.byref(d), ctypes.byref(n))
+    return rc, n.value
+
+
+def test_bwd_workspace_size(lib):
+    B, L, nh, H, S, G, T = 2, 512, 8, 64, 128, 2, 256
+    rc, n = bwd_ws(lib, desc())
+    assert rc == 0
+    nc = (L + T - 1) // T
+    al = lambda v: (v + 255) // 256 * 256
+    # G, the entering states and their gradients, six per-token arrays, two partial sums (>= 1 slice)
+    fixed = 7 * al(4 * B * nh * L) + 2 * al(4 * B * nh * nc * H * S)
+    part = al(4 * B * L * G * S)
+    assert n >= fixed + 2 * part and (n - fixed) % (2 * 256) == 0
+    slices = (n - fixed) // 2 // 4 // (B * L * G * S)
+    assert 1 <= slices <= nh // G
+    assert bwd_ws(lib, desc(seqlen=0)) == (0, 0)
+    assert bwd_ws(lib, desc(seqlen=513))[1] > n
+    for bad in (dict(chunk=512), dict(headdim=256), dict(out_dtype=_native.SSD_F32)):
+        assert bwd_ws(lib, desc(**bad))[0] == 2, bad
+    assert bwd_ws(lib, desc(ngroups=3))[0] == 1
+    assert lib.ssd_bwd_workspace_size(ctypes.byref(desc()), None) == 1
+
+
+def test_bwd_argument_validation(lib):
+    d = desc()
+    rc, need = bwd_ws(lib, d)
+    a = 1 << 20
+    ws = 1 << 40
+    # x, dt, A, B, C, D, h0, dy, dh_final, dx, ddt, dA, dB, dC, dD, dh0, workspace, bytes, stream
+    args = [a, a + (1 << 24), a + (2 << 24), a + (3 << 24), a + (4 << 24), a + (5 << 24), None, a + (6 << 24), None,
+            1 << 32, (1 << 32) + (1 << 28), (1 << 32) + (2 << 28), (1 << 32) + (3 << 28), (1 << 32) + (4 << 28),
+            (1 << 32) + (5 << 28), None, ws, need, None]
+    for i in (0, 1, 2, 3, 4, 5, 7, 9, 10, 11, 12, 13, 14):   # required pointers
+        bad = list(args)
+        bad[i] = None
+        assert lib.ssd_bwd(ctypes.byref(d), *bad) == 1, i
+    bad = list(args)
+    bad[0] = a + 1                                              # x misaligned for bf16
+    assert lib.ssd_bwd(ctypes.byref(d), *bad) == 1
+    bad = list(args)
+    bad[9] = args[7]                                            # dx aliases dy
+    assert lib.ssd_bwd(ctypes.byref(d), *bad) == 1
+    bad = list(args)
+    bad[13] = args[12]                                          # dC aliases dB
+    assert lib.ssd_bwd(ctypes.byref(d), *bad) == 1
+    bad = list(args)
+    bad[17] = need - 1                                          # workspace one byte short
+    assert lib.ssd_bwd(ctypes.byref(d), *bad) == 3
+    bad = list(args)
+    bad[16] = ws + 128                                          # workspace misaligned
+    assert lib.ssd_bwd(ctypes.byref(d), *bad) == 3
+    d = desc(chunk=512)
+    assert lib.ssd_bwd(ctypes.byref(d), *args) == 2
+
+
+def s6desc(**kw):
+    d = _native.S6Desc()
+    base = dict(batch=2, seqlen=256, dim=64, dstate=16, ngroups=1, in_dtype=_native.SSD_BF16,
+                out_dtype=_native.SSD_BF16, flags=0, reserved=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(dstate=0), 1), (dict(ngroups=3), 1), (dict(batch=-1), 1), (dict(in_dtype=5), 1), (dict(flags=1), 1),
+    (dict(reserved=2), 1), (dict(dstate=33), 2), (dict(batch=70000), 2),
+])
+def test_s6_bad_descriptors_rejected(lib, bad, code):
+    d = s6desc(**bad)
+    a = 1 << 20
+    assert lib.ssd_s6_fwd(ctypes.byref(d), a, a, a, a, a, None, None, 1 << 30, None, None) == code
+
+
+def test_s6_argument_validation(lib):
+    d = s6desc()
+    a = 1 << 20
+    args = [a, a + (1 << 24), a + (2 << 24), a + (3 << 24), a + (4 << 24), None, None, 1 << 30, None, None]
+    for i in (0, 1, 2, 3, 4, 7):
+        bad = list(args)
+        bad[i] = None
+        assert lib.ssd_s6_fwd(ctypes.byref(d), *bad) == 1, i
+    bad = list(args)
+    bad[7] = args[0]                                            # y aliases x
+    assert lib.ssd_s6_fwd(ctypes.byref(d), *bad) == 1
+    bad = list(args)
+    bad[1] = args[1] + 1                                        # delta misaligned
+    assert lib.ssd_s6_fwd(ctypes.byref(d), *bad) == 1
+    assert lib.ssd_s6_fwd(None, *args) == 1
+    # nothing to do: no batch rows, or no tokens and no final state requested
+    assert lib.ssd_s6_fwd(ctypes.byref(s6desc(batch=0)), *args) == 0
+    assert lib.ssd_s6_fwd(ctypes.byref(s6desc(seqlen=0)), *args) == 0
