@@ -264,6 +264,21 @@ def run_reference(args, shape):
 L2_BYTES = 129 * 10**6
 
 
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time: each rank contributes its own, every rank receives the maximum
+    (a no-op on one process)."""
+    if dist is None:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank: float, ms: float) -> float:
+    """Units per second of the whole job: every rank processes its own units in `ms` (the max over ranks)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def needs_l2_flush(shape) -> bool:
     """Steps whose compulsory I/O is under twice the L2 could run partly from L2 on
     back-to-back steps; those are timed one step at a time with an L2 flush between."""
@@ -668,10 +683,7 @@ def main():
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     ms_per_step = ms / args.steps
     stage_ms = {st: statistics.mean(ev[i][2 * j].elapsed_time(ev[i][2 * j + 1]) for i in range(args.steps))
                 for j, st in enumerate(STAGES)}
@@ -702,10 +714,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
     if rank != 0:
         if dist:
@@ -718,7 +727,7 @@ def main():
     achieved = sb[top] / (stage_ms[top] * 1e-3) / 1e9
     # a kernel timed inside a long step: burst copy bandwidth is the only HBM figure measured
     peak = float(peaks["hbm_gbs"])
-    tokens_per_s = world * shape.tokens / (ms_per_step * 1e-3)
+    tokens_per_s = whole_job_rate(world, shape.tokens, ms_per_step)
     flops = alg_flops(shape)
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -736,7 +745,7 @@ def main():
         "plan": plan,
         "stages_ms": {s_: (stage_ms[s_] if sb[s_] else None) for s_ in STAGES},
         "stages_gbs": {s_: (sb[s_] / (stage_ms[s_] * 1e-3) / 1e9 if sb[s_] else None) for s_ in STAGES},
-        "e2e": {"value": world * shape.tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rate(world, shape.tokens, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": plan["kernel_launches"] * args.steps,
         "clocks": clk.summary(),
