@@ -154,7 +154,7 @@ ssd_status ssd_fwd_timed(const ssd_desc *desc, const void *x, const void *dt, co
 /* Synchronises `stream` and reports whether the last ssd_fwd that used
  * `workspace` hit a bounded device-side wait that expired (SSD_ERR_TIMEOUT:
  * the outputs of that call are invalid) or completed normally (SSD_OK).  The
- * tensor-core kernels bound every wait on a barrier (2 s) and record expiry
+ * tensor-core kernels bound every wait on a barrier (250 ms) and record expiry
  * in the workspace's error word instead of hanging. */
 ssd_status ssd_fwd_check(const void *workspace, ssd_stream_t stream);
 
