@@ -396,6 +396,51 @@ def bwd_alg_flops(s: workloads.Shape) -> float:
     return float(s.batch * s.nchunks * (s.nheads * per_head + s.ngroups * T * (T + 1) * S))
 
 
+def bwd_cpu_baseline(inp, gin, budget_s: float):
+    """The gradient oracle as it stands, on (batch, head) pairs at full sequence length, one pair per
+    call with every core on the pairs of a window; tokens/s scaled to the whole workload."""
+    import oracle
+    s = inp.shape
+    cores = oracle.default_threads()
+    hpg = s.nheads // s.ngroups
+    windows = list(_head_windows(s, cores))
+    done, rounds, t0 = 0, 0, time.perf_counter()
+    while True:
+        b, lo, hi = windows[rounds % len(windows)]
+        glo, ghi = lo // hpg, (hi - 1) // hpg + 1
+        oracle.ssd_bwd_seq(inp.x[b:b + 1, :, lo:hi], inp.dt[b:b + 1, :, lo:hi], inp.A[lo:hi],
+                           inp.B[b:b + 1, :, glo:ghi], inp.C[b:b + 1, :, glo:ghi], inp.D[lo:hi],
+                           gin.dy[b:b + 1, :, lo:hi], h0=None if inp.h0 is None else inp.h0[b:b + 1, lo:hi],
+                           dh_final=None if gin.dh_final is None else gin.dh_final[b:b + 1, lo:hi], nthreads=cores)
+        done += hi - lo
+        rounds += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": done * s.seqlen / s.nheads / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} (batch, head) pairs (workload has {s.batch * s.nheads}) at full length L={s.seqlen}, "
+                      f"reverse-mode float64 recurrence, {el:.1f} s; tokens/s scaled to the whole workload"}
+
+
+def run_bwd_reference(args, shape):
+    """The reference arm of the gradient pass: the oracle on the host cores, rank 0 only."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = workloads.make_inputs(shape)
+    gin = workloads.make_grad_inputs(shape)
+    vals = [bwd_cpu_baseline(inp, gin, max(1.0, args.ref_step_s)) for _ in range(args.warmup + args.steps)]
+    vals = vals[args.warmup:]
+    tok = statistics.median(v["value"] for v in vals)
+    print(json.dumps({"impl": "reference", "metric": BWD_METRIC, "value": tok, "unit": UNIT, "n_gpus": 1,
+                      "steps": args.steps, "warmup": args.warmup, "ms_per_step": shape.tokens / tok * 1e3,
+                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                      "data": "synthetic", "config": config_of(shape), "cpu_baseline": dict(vals[0], value=tok),
+                      "e2e": {"value": tok, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                      "gpu_launches": 0}), flush=True)
+
+
 def run_bwd(args, shape):
     """ssd_bwd throughput on one layer: the whole gradient pass (forward recompute included)
     per step, inputs and upstream gradients resident on the device."""
@@ -448,6 +493,8 @@ def run_bwd(args, shape):
         "gpu_launches": 11 * args.steps,
         "clocks": clk.summary(),
     }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = bwd_cpu_baseline(inp, gin, args.cpu_budget_s)
     print(json.dumps(line), flush=True)
 
 
@@ -606,7 +653,7 @@ def main():
     shape = workloads.by_name(args.workload)
     if args.which == "bwd":
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the forward pass only"}))
+            run_bwd_reference(args, shape)
             return
         run_bwd(args, shape)
         return
