@@ -490,7 +490,7 @@ def run_bwd(args, shape):
                          "peak_gbs": float(peaks["hbm_gbs"]),
                          "frac": io / (ms_per_step * 1e-3) / 1e9 / float(peaks["hbm_gbs"])},
         "e2e": None,
-        "gpu_launches": 11 * args.steps,
+        "gpu_launches": 10 * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
