@@ -302,7 +302,7 @@ const char *ssd_status_string(ssd_status s)
     switch (s) {
     case SSD_OK: return "SSD_OK";
     case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG: invalid argument (null/misaligned pointer, bad size or dtype)";
-    case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: problem size outside what this build handles";
+    case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: problem size outside what this library handles";
     case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing, too small or not 256-byte aligned";
     case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA call or kernel launch failed";
     case SSD_ERR_TOO_LARGE: return "SSD_ERR_TOO_LARGE: problem needs more scratch than the built-in no-alloc array";
