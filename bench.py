@@ -37,10 +37,11 @@ METRIC = "ssd_fwd_tokens_per_s"
 UNIT = "tokens/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")
-KERNEL_SOURCES = {  # the file that holds each stage's kernels (for the traffic record's freshness check);
-    # the traffic records are of the tensor-core path, whose chunk_state / chunk_scan live in ssd_tc.cu
+KERNEL_SOURCES = {  # the files that hold each kernel (for the traffic record's freshness check)
     "chunk_cumsum": ["ssd_simt.cu"], "state_passing": ["ssd_simt.cu"],
-    "chunk_state": ["ssd_tc.cu", "sm100_ptx.cuh"], "chunk_scan": ["ssd_tc.cu", "sm100_ptx.cuh"],
+    "chunk_state": ["ssd_tc.cu", "sm100_ptx.cuh", "tc_common.cuh"],
+    "chunk_scan": ["ssd_tc.cu", "sm100_ptx.cuh", "tc_common.cuh"],
+    "k_ssd_fwd_fused": ["ssd_fused.cu", "fused_plan.cuh", "sm100_ptx.cuh", "tc_common.cuh"],
 }
 
 
@@ -58,13 +59,16 @@ def esize(dtype: str) -> int:
 
 
 def stage_bytes(s: workloads.Shape, plan: dict):
-    """Algorithmic bytes per launch of each stage as the library runs it (``plan`` is
-    ssd_fwd_plan): its own compulsory inputs read once and outputs written once, with
-    the intermediates (G, the super-chunk states, the super-chunk-start states, all
-    float32) counted as that stage's inputs/outputs; 0 for a stage that does not launch.
-    A plan cuts the sequences ((batch, head) pairs) in two parts; chunk_state and
-    state_passing run per part and their bytes are summed.  Also the whole-step
-    compulsory I/O ("step")."""
+    """Bytes per launch of each stage as the library runs it (``plan`` is ssd_fwd_plan), with
+    the intermediates it moves counted: G, the float32 dt copy, the super-chunk states and the
+    super-chunk-start states, all float32; 0 for a stage that does not launch.  A plan cuts the
+    sequences ((batch, head) pairs) in two parts; chunk_state and state_passing run per part and
+    their bytes are summed.  With the fused kernel (plan["fused"]) every stage is one launch,
+    reported under "chunk_scan": the compulsory I/O, plus the x and B of the super-chunks whose
+    state a STATE item computes (read a second time), plus each such state written once, read
+    once and written once more as the entering state by the PASS items, and read by its SCAN
+    item.  Also the whole-step compulsory I/O ("step": each input read once, each
+    output written once, intermediates excluded)."""
     e = esize(s.dtype)
     Bsz, L, nh, H, S, G, T, nc = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups, s.chunk, s.nchunks
     x = Bsz * L * nh * H * e
@@ -76,14 +80,25 @@ def stage_bytes(s: workloads.Shape, plan: dict):
     h0 = state if s.h0_recipe != "none" else 0
     y = Bsz * L * nh * H * e
     ad = 2 * nh * 4
+    step = x + dt + 2 * bc + ad + h0 + y + state
     nseq, hpg = Bsz * nh, nh // G
+    split = plan["split_sequences"]
+    parts = [(0, split, plan["super_tokens"], plan["n_super"]),
+             (split, nseq - split, plan["tail_super_tokens"], plan["tail_n_super"])]
+    if plan["fused"]:
+        extra = 0.0
+        for lo, n, tok, nsup in parts:
+            if n == 0 or nsup <= 1:
+                continue
+            frac = (nsup - 1) * tok / L                 # share of each cut sequence a STATE item reads
+            groups = len({(bh // nh, (bh % nh) // hpg) for bh in range(lo, lo + n)})
+            extra += frac * (n * L * (H * e + e) + groups * L * S * e) + 4 * n * (nsup - 1) * hs
+        return {"chunk_cumsum": 0, "chunk_state": 0, "state_passing": 0, "chunk_scan": step + extra, "step": step}
+    cs = sp = carried = 0.0
     if plan["tensor_cores"]:
-        split = plan["split_sequences"]
-        parts = [(0, split, plan["chunks_per_super"], plan["n_super"]),
-                 (split, nseq - split, plan["tail_chunks_per_super"], plan["tail_n_super"])]
+        parts = [(lo, n, tok // T, nsup) for lo, n, tok, nsup in parts]
     else:
         parts = [(0, nseq, 1, nc)]
-    cs = sp = carried = 0.0
     # the cumsum writes the float32 copy of dt only for the sequences chunk_state reads
     dtT_seqs = sum(n for lo, n, R, nsup in parts if n > 0 and nsup > 1) if plan["tensor_cores"] else 0
     for lo, n, R, nsup in parts:
@@ -105,7 +120,7 @@ def stage_bytes(s: workloads.Shape, plan: dict):
         "chunk_state": cs,
         "state_passing": sp,
         "chunk_scan": x + dt + 2 * bc + g + h0 + carried + nh * 4 + y + state,
-        "step": x + dt + 2 * bc + ad + h0 + y + state,
+        "step": step,
     }
     if not plan["tensor_cores"]:
         out["state_passing"] += state                  # the CUDA-core path writes h_final there
@@ -771,7 +786,12 @@ def main():
     peaks, peak_kind = load_peaks()
     sb = stage_bytes(shape, plan)
     top = max(STAGES, key=lambda s_: stage_ms[s_] if sb[s_] else -1.0)
-    achieved = sb[top] / (stage_ms[top] * 1e-3) / 1e9
+    kname = "k_ssd_fwd_fused" if plan["fused"] else top
+    # the dominant kernel's algorithmic bytes are the compulsory I/O it owns -- every
+    # input read once and every output written once (intermediates excluded); the fused kernel and
+    # the scan of the four-stage path both read every input and write every output of the step
+    alg_top = sb["step"]
+    achieved = alg_top / (stage_ms[top] * 1e-3) / 1e9
     # a kernel timed inside a long step: burst copy bandwidth is the only HBM figure measured
     peak = float(peaks["hbm_gbs"])
     tokens_per_s = whole_job_rate(world, shape.tokens, ms_per_step)
@@ -783,15 +803,17 @@ def main():
         "data": "synthetic", "config": dict(config_of(shape), parallelism=f"replicas{world}",
                                             tensor_cores=tc),
         "tflops": flops / (ms_per_step * 1e-3) / 1e12,
-        "roofline": {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                     "alg_bytes_per_launch": sb[top], "traffic": traffic_record(top, shape.name)},
+                     "alg_bytes_per_launch": alg_top, "traffic": traffic_record(kname, shape.name),
+                     "plan_bytes_per_launch": sb[top],
+                     "plan_frac": sb[top] / (stage_ms[top] * 1e-3) / 1e9 / peak},
         "step_roofline": {"alg_bytes": sb["step"], "alg_flops": flops,
                           "roofline_ms": max(sb["step"] / (peak * 1e9), flops / (float(peaks["bf16_tflops"]) * 1e12)) * 1e3,
                           "frac": max(sb["step"] / (peak * 1e9), flops / (float(peaks["bf16_tflops"]) * 1e12)) * 1e3 / ms_per_step},
         "plan": plan,
         "stages_ms": {s_: (stage_ms[s_] if sb[s_] else None) for s_ in STAGES},
-        "stages_gbs": {s_: (sb[s_] / (stage_ms[s_] * 1e-3) / 1e9 if sb[s_] else None) for s_ in STAGES},
+        "stages_plan_gbs": {s_: (sb[s_] / (stage_ms[s_] * 1e-3) / 1e9 if sb[s_] else None) for s_ in STAGES},
         "e2e": {"value": whole_job_rate(world, shape.tokens, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": plan["kernel_launches"] * args.steps,

@@ -83,6 +83,13 @@ typedef struct {
  * exist for the shape (both are GPU code; this exists for cross-checking). */
 #define SSD_FLAG_FORCE_SIMT 1
 
+/* Test hook of the failure path: every bounded wait inside the tensor-core kernels that is
+ * not satisfied at once expires (a bound of zero instead of 250 ms).  The call then winds
+ * down without hanging -- each kernel still retires the copies and MMAs it has issued --
+ * and ssd_fwd_check reports SSD_ERR_TIMEOUT; its outputs are invalid.  Never set it in
+ * production code. */
+#define SSD_FLAG_EXPIRE_WAITS 2
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *ssd_status_string(ssd_status s);
 
@@ -101,23 +108,26 @@ ssd_status ssd_fwd_path(const ssd_desc *desc, int32_t *uses_tensor_cores);
 
 /* How ssd_fwd runs `desc` on the current device (written to *plan): which path,
  * how each sequence ((batch, head) pair, in b * nh + h order) is cut into
- * super-chunks (the tensor-core scan walks one super-chunk per CTA with the
- * state on chip; the CUDA-core path uses one chunk), and how many kernels and
+ * super-chunks (a tensor-core CTA walks one super-chunk of one sequence, or of two,
+ * with the state on chip; the CUDA-core path uses one chunk), and how many kernels and
  * cudaMemsetAsync calls one ssd_fwd call issues on its stream.  The first
- * split_sequences sequences are cut into super-chunks of chunks_per_super
- * chunks, the remaining ones into super-chunks of tail_chunks_per_super chunks
- * (so that the last wave of scan CTAs still covers the SMs).  Host-side query:
- * it reads the device's SM count and launches nothing.
- * Errors: SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED, as for ssd_fwd. */
+ * split_sequences sequences are cut into super-chunks of super_tokens tokens, the
+ * remaining ones into super-chunks of tail_super_tokens tokens.  fused = 1: one
+ * persistent kernel runs every stage for two heads of one B/C group per work item
+ * (S = 128, H = 64, an even number of heads per group), and work_items is the length
+ * of its work list.  Host-side query: it reads the device's SM count and launches
+ * nothing.  Errors: SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED, as for ssd_fwd. */
 typedef struct {
     int32_t tensor_cores;          /* 1: tcgen05 kernels for chunk_state and chunk_scan   */
-    int32_t chunks_per_super;      /* R of the first split_sequences sequences            */
-    int32_t n_super;               /* their super-chunks per sequence (ceil(nc / R))      */
+    int32_t fused;                 /* 1: the single fused kernel (implies tensor_cores)   */
+    int32_t super_tokens;          /* tokens per super-chunk, first split_sequences seqs  */
+    int32_t n_super;               /* their super-chunks per sequence                     */
+    int32_t split_sequences;       /* sequences cut with super_tokens (<= B * nh)         */
+    int32_t tail_super_tokens;     /* tokens per super-chunk of the remaining sequences   */
+    int32_t tail_n_super;          /* their super-chunks per sequence                     */
     int32_t kernel_launches;       /* kernels per ssd_fwd call (0 for an empty problem)   */
     int32_t memsets;               /* cudaMemsetAsync calls per ssd_fwd call              */
-    int32_t split_sequences;       /* sequences cut with chunks_per_super (<= B * nh)     */
-    int32_t tail_chunks_per_super; /* R of the remaining sequences                        */
-    int32_t tail_n_super;          /* their super-chunks per sequence                     */
+    int32_t work_items;            /* fused: work items (tickets) per call; 0 otherwise   */
 } ssd_plan;
 
 ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan);
@@ -267,23 +277,34 @@ ssd_status ssd_s6_fwd(const ssd_s6_desc *desc, const void *x, const void *delta,
  * still provides all inputs and outputs.  It calls no cudaMalloc, cudaFree or
  * other allocating routine.
  *
- *  - The first call on a device looks up the device address of the array
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture on that device.
+ *  - The first call in a CUDA context looks up the device address of the array
+ *    (cudaGetSymbolAddress) in that context, with its device current; make that
+ *    first call before any stream capture on that device.  The address is cached
+ *    per context.
  *  - Problems whose workspace (ssd_fwd_workspace_size) exceeds
  *    SSD_NOALLOC_SCRATCH_BYTES are rejected with SSD_ERR_TOO_LARGE before
  *    anything is launched.
  *  - All calls in the process share the one array per device: calls whose
  *    executions overlap on the GPU (different streams, or different host
  *    threads without ordering) race on it and give wrong results.  Order them
- *    on one stream.  The array keeps the previous call's contents; the forward
- *    pass writes every scratch byte it reads, so nothing needs clearing.
+ *    on one stream.  The array keeps the previous call's contents; each call
+ *    clears the parts that must start at zero (the error word and the counters
+ *    of the work list) and writes every other scratch byte before reading it.
+ *  - A bounded wait that expired inside the call is reported by
+ *    ssd_fwd_noalloc_check (the error word lives in the array too).
  * Arguments, layouts and the other errors are those of ssd_fwd.            */
 #define SSD_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
 ssd_status ssd_fwd_noalloc(const ssd_desc *desc, const void *x, const void *dt, const float *A,
                            const void *Bm, const void *Cm, const float *D, const float *h0,
                            void *y, float *h_final, ssd_stream_t stream);
+
+/* The ssd_fwd_check of ssd_fwd_noalloc: synchronises `stream` and reports whether the last
+ * ssd_fwd_noalloc call in the current context hit a bounded device-side wait that expired
+ * (SSD_ERR_TIMEOUT: its outputs are invalid) or completed normally (SSD_OK).  Like
+ * ssd_fwd_noalloc it allocates nothing; SSD_ERR_CUDA if the array's address cannot be
+ * looked up or the copy of the error word fails. */
+ssd_status ssd_fwd_noalloc_check(ssd_stream_t stream);
 
 #ifdef __cplusplus
 }

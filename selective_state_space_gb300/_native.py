@@ -11,6 +11,8 @@ LIB_PATH = os.path.join(_PKG, "_build", "libssd.so")
 
 SSD_F32, SSD_BF16 = 0, 1
 SSD_FLAG_FORCE_SIMT = 1
+SSD_FLAG_EXPIRE_WAITS = 2   # test hook: every bounded device wait expires at once
+NOALLOC_SCRATCH_BYTES = 32 << 20   # SSD_NOALLOC_SCRATCH_BYTES of include/ssd.h
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_WORKSPACE",
           4: "SSD_ERR_CUDA", 5: "SSD_ERR_TOO_LARGE", 6: "SSD_ERR_TIMEOUT"}
 
@@ -19,7 +21,7 @@ EXPORTS = ("ssd_status_string", "ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_f
            "ssd_fwd_check",
            "ssd_step",
            "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_bwd_workspace_size",
-           "ssd_bwd", "ssd_s6_fwd", "ssd_fwd_noalloc")
+           "ssd_bwd", "ssd_s6_fwd", "ssd_fwd_noalloc", "ssd_fwd_noalloc_check")
 
 
 class Desc(ctypes.Structure):
@@ -36,10 +38,10 @@ class S6Desc(ctypes.Structure):
 
 
 class Plan(ctypes.Structure):
-    _fields_ = [("tensor_cores", ctypes.c_int32), ("chunks_per_super", ctypes.c_int32), ("n_super", ctypes.c_int32),
-                ("kernel_launches", ctypes.c_int32), ("memsets", ctypes.c_int32),
-                ("split_sequences", ctypes.c_int32), ("tail_chunks_per_super", ctypes.c_int32),
-                ("tail_n_super", ctypes.c_int32)]
+    _fields_ = [("tensor_cores", ctypes.c_int32), ("fused", ctypes.c_int32), ("super_tokens", ctypes.c_int32),
+                ("n_super", ctypes.c_int32), ("split_sequences", ctypes.c_int32),
+                ("tail_super_tokens", ctypes.c_int32), ("tail_n_super", ctypes.c_int32),
+                ("kernel_launches", ctypes.c_int32), ("memsets", ctypes.c_int32), ("work_items", ctypes.c_int32)]
 
 
 class SSDError(RuntimeError):
@@ -89,6 +91,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ssd_fwd_check.restype = st
         lib.ssd_fwd_noalloc.argtypes = [DP] + [P] * 9 + [P]
         lib.ssd_fwd_noalloc.restype = st
+        lib.ssd_fwd_noalloc_check.argtypes = [P]
+        lib.ssd_fwd_noalloc_check.restype = st
         lib.ssd_bwd_workspace_size.argtypes = [DP, ctypes.POINTER(ctypes.c_size_t)]
         lib.ssd_bwd_workspace_size.restype = st
         lib.ssd_bwd.argtypes = [DP] + [P] * 17 + [ctypes.c_size_t, P]

@@ -73,15 +73,14 @@ def uses_tensor_cores(desc: Desc) -> bool:
 
 
 def fwd_plan(desc: Desc) -> dict:
-    """How ssd_fwd runs ``desc`` on the current device (ssd_fwd_plan): path, chunks per
-    super-chunk and super-chunks per sequence for the first ``split_sequences``
-    sequences and for the rest (``tail_*``), kernel launches and memsets per call."""
+    """How ssd_fwd runs ``desc`` on the current device (ssd_fwd_plan): path (tensor cores,
+    and whether the single fused kernel runs every stage), tokens per super-chunk and
+    super-chunks per sequence for the first ``split_sequences`` sequences and for the rest
+    (``tail_*``), kernel launches and memsets per call, and the fused kernel's work items."""
     p = _native.Plan()
     check("ssd_fwd_plan", _native.load().ssd_fwd_plan(ctypes.byref(desc), ctypes.byref(p)))
-    return {"tensor_cores": bool(p.tensor_cores), "chunks_per_super": int(p.chunks_per_super),
-            "n_super": int(p.n_super), "split_sequences": int(p.split_sequences),
-            "tail_chunks_per_super": int(p.tail_chunks_per_super), "tail_n_super": int(p.tail_n_super),
-            "kernel_launches": int(p.kernel_launches), "memsets": int(p.memsets)}
+    return {name: (bool(getattr(p, name)) if name in ("tensor_cores", "fused") else int(getattr(p, name)))
+            for name, _ in _native.Plan._fields_}
 
 
 def alloc_workspace(desc: Desc, device) -> torch.Tensor:

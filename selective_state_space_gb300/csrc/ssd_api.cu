@@ -1,5 +1,6 @@
 // ssd_api.cu -- the extern "C" entry points of libssd.so (declared in include/ssd.h):
 // argument validation, workspace carving and the stage sequence of the forward pass.
+#include <cuda.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -31,7 +32,7 @@ ssd_status check_desc(const ssd_desc *d, Problem *pr, bool need_seq)
     if (d->nheads % d->ngroups != 0) return SSD_ERR_INVALID_ARG;
     if (d->in_dtype != SSD_F32 && d->in_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
     if (d->out_dtype != SSD_F32 && d->out_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
-    if (d->reserved != 0 || (d->flags & ~SSD_FLAG_FORCE_SIMT) != 0) return SSD_ERR_INVALID_ARG;
+    if (d->reserved != 0 || (d->flags & ~(SSD_FLAG_FORCE_SIMT | SSD_FLAG_EXPIRE_WAITS)) != 0) return SSD_ERR_INVALID_ARG;
     if (need_seq && (d->seqlen < 0 || d->chunk < 1)) return SSD_ERR_INVALID_ARG;
     if (d->dstate > 256 || d->headdim > 1024) return SSD_ERR_UNSUPPORTED;
     if (need_seq && d->chunk > 1024) return SSD_ERR_UNSUPPORTED;
@@ -95,6 +96,13 @@ ssd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_E
 bool use_tensor_cores(const ssd_desc *desc, const Problem &pr)
 {
     return !(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr);
+}
+
+// Bound on the waits inside the tensor-core kernels: 250 ms, or none at all (every wait that is
+// not satisfied at once expires) under SSD_FLAG_EXPIRE_WAITS, the test hook of the timeout path.
+unsigned long long wait_limit_ns(const ssd_desc *desc)
+{
+    return (desc->flags & SSD_FLAG_EXPIRE_WAITS) ? 0ull : 250000000ull;
 }
 
 int device_sms()
@@ -195,6 +203,48 @@ void plan_parts(const Problem &pr, const ssd::ScanSplit &sp, PlanPart out[2])
     out[1] = PlanPart{ssd::SeqRange{sp.split, pr.B * pr.nh - sp.split}, sp.R1, sp.nsup1, sp.base1};
 }
 
+// ---- work list of the fused kernel (two heads per item; see fused_plan.cuh) ----------------
+
+bool use_fused(const ssd_desc *desc, const Problem &pr)
+{
+    return use_tensor_cores(desc, pr) && ssd::scan_seqs_per_cta(pr) == 2;
+}
+
+// The fused kernel's plan for this shape on this device (fused_plan.cuh: the search
+// simulates every candidate schedule), cached per (pairs, sub-chunks, chunks, SMs).
+ssd::FusedPlan choose_fused_plan(const Problem &pr)
+{
+    const int sms = device_sms();
+    const int npair = (int)(pr.B * pr.nh / 2);
+    const int nsub = (int)((pr.L + ssd::kSubChunk - 1) / ssd::kSubChunk);
+    const int nc = (int)pr.nc;
+    struct Entry { int npair, nsub, nc, sms; ssd::FusedPlan plan; };
+    static std::mutex mu;
+    static Entry cache[16];
+    static int used = 0, next = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache[i].npair == npair && cache[i].nsub == nsub && cache[i].nc == nc && cache[i].sms == sms)
+                return cache[i].plan;
+    }
+    const ssd::FusedPlan best = ssd::fused_search(npair, nsub, nc, sms, ssd::fused_pass_slices());
+    std::lock_guard<std::mutex> lock(mu);
+    const int slot = used < 16 ? used++ : (next++ % 16);
+    cache[slot] = Entry{npair, nsub, nc, sms, best};
+    return best;
+}
+
+// Workspace of the fused path, carved from the standard one: the header (error word, ticket)
+// with the per-pair counters right after it (one memset clears both), the log2 decays where
+// the float32 dt copy would be, and the two state arrays where they always are.
+ssd::FusedWork carve_fused(const Workspace &w)
+{
+    return ssd::FusedWork{w.err, (int *)w.G, w.dtT, w.s_local, w.h_start};
+}
+
+size_t fused_clear_bytes(const Problem &pr) { return kWsAlign + (size_t)(pr.B * pr.nh) * sizeof(int); }
+
 ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const float *A,
                     const void *Bm, const void *Cm, const float *D, const float *h0, void *y,
                     float *h_final, void *workspace, size_t ws_bytes, cudaStream_t st,
@@ -231,6 +281,17 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
 
     auto rec = [&](int i) -> bool { return !events || cudaEventRecord((cudaEvent_t)events[i], st) == cudaSuccess; };
     const bool tc = use_tensor_cores(desc, pr);
+    if (use_fused(desc, pr)) {
+        // one kernel for every stage (ssd_fused.cu); the stage events 0..5 stay empty
+        const ssd::FusedPlan fp = choose_fused_plan(pr);
+        if (cudaMemsetAsync(w.err, 0, fused_clear_bytes(pr), st) != cudaSuccess) return SSD_ERR_CUDA;
+        for (int i = 0; i < 7; ++i)
+            if (!rec(i)) return SSD_ERR_CUDA;
+        if (ssd::launch_fused_pair(pr, x, dt, A, Bm, Cm, D, h0, h_final, y, fp, carve_fused(w), wait_limit_ns(desc),
+                                   st) != cudaSuccess || !rec(7))
+            return SSD_ERR_CUDA;
+        return SSD_OK;
+    }
     if (cudaMemsetAsync(w.err, 0, sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
     ssd::ScanSplit sp{};
     PlanPart parts[2];
@@ -341,18 +402,30 @@ ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan)
     p.tensor_cores = use_tensor_cores(desc, pr) ? 1 : 0;
     if (pr.B == 0 || pr.nh == 0 || pr.L == 0) {
         // nothing to scan: at most one copy or memset of h_final, issued only if h_final is given
-        p.chunks_per_super = 1;
+        p.super_tokens = (int32_t)std::min<int64_t>(pr.T, 0x7fffffff);
         *plan = p;
         return SSD_OK;
     }
-    if (p.tensor_cores) {
+    const int32_t nseq = (int32_t)(pr.B * pr.nh);
+    if (use_fused(desc, pr)) {
+        const ssd::FusedPlan fp = choose_fused_plan(pr);
+        p.fused = 1;
+        p.super_tokens = (int32_t)std::min<int64_t>(fp.R0 * ssd::kSubChunk, pr.L);
+        p.n_super = fp.nsup0;
+        p.split_sequences = 2 * fp.split;
+        p.tail_super_tokens = (int32_t)std::min<int64_t>(fp.R1 * ssd::kSubChunk, pr.L);
+        p.tail_n_super = fp.nsup1;
+        p.kernel_launches = 1;
+        p.memsets = 1;                         // the error word, the ticket and the per-pair counters
+        p.work_items = fp.n_items;
+    } else if (p.tensor_cores) {
         const ssd::ScanSplit sp = choose_tc_plan(pr);
         PlanPart parts[2];
         plan_parts(pr, sp, parts);
-        p.chunks_per_super = sp.R0;
+        p.super_tokens = (int32_t)std::min<int64_t>(sp.R0 * pr.T, pr.L);
         p.n_super = sp.nsup0;
         p.split_sequences = (int32_t)sp.split;
-        p.tail_chunks_per_super = sp.R1;
+        p.tail_super_tokens = (int32_t)std::min<int64_t>(sp.R1 * pr.T, pr.L);
         p.tail_n_super = sp.nsup1;
         p.kernel_launches = 2;                 // cumsum and scan
         p.memsets = 1;                         // the error word
@@ -362,10 +435,10 @@ ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan)
             if (ssd::chunk_state_tc_memsets(pr, q.seqs, q.R, q.nsup - 1)) p.memsets += 1;
         }
     } else {
-        p.chunks_per_super = 1;
+        p.super_tokens = (int32_t)std::min<int64_t>(pr.T, pr.L);
         p.n_super = (int32_t)pr.nc;
-        p.split_sequences = (int32_t)(pr.B * pr.nh);
-        p.tail_chunks_per_super = 1;
+        p.split_sequences = nseq;
+        p.tail_super_tokens = p.super_tokens;
         p.tail_n_super = (int32_t)pr.nc;
         p.kernel_launches = 4;
         p.memsets = 1;
@@ -604,29 +677,60 @@ ssd_status ssd_s6_fwd(const ssd_s6_desc *desc, const void *x, const void *delta,
 // pass (graph capture in progress, allocator-less runtimes, plug-ins whose host
 // owns all allocations): the scratch lives in this file-scope device array,
 // which every GPU that loads libssd.so keeps for the life of the process.
-// Host code must not hand the array's name to a kernel -- on the host it is
-// only a stand-in symbol -- so the device address is looked up once per device
-// with cudaGetSymbolAddress and cached.
+// Host code must not hand the array's name to a kernel -- on the host it is only a
+// stand-in symbol -- so its device address is looked up with cudaGetSymbolAddress while
+// the device is current, and cached per CUDA context (the address belongs to the context
+// the module is loaded in, so a context created later -- after cudaDeviceReset, or a
+// host application's own context -- gets its own lookup).
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 std::mutex g_noalloc_mutex;
-void *g_noalloc_addr[kMaxDevices];   // device address of g_noalloc_scratch, per device ordinal
+struct NoallocEntry {
+    CUcontext ctx;
+    void *addr;
+};
+NoallocEntry g_noalloc[kMaxContexts];
+int g_noalloc_used = 0;
 
-// Device address of the scratch array on the current device (nullptr on error).
+// cuCtxGetCurrent through the runtime's driver entry-point query (the library does not link
+// the driver API directly, so it loads where no driver is installed).
+CUresult current_context(CUcontext *ctx)
+{
+    using Fn = CUresult (*)(CUcontext *);
+    static Fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (Fn)p;
+    });
+    return fn ? fn(ctx) : CUDA_ERROR_NOT_INITIALIZED;
+}
+
+// Device address of the scratch array in the current context (nullptr on error).  The
+// lookup itself makes the device's primary context current when no context is.
 void *noalloc_scratch_address()
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
-        g_noalloc_addr[dev] = p;
+    CUcontext ctx = nullptr;
+    if (current_context(&ctx) == CUDA_SUCCESS && ctx) {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        for (int i = 0; i < g_noalloc_used; ++i)
+            if (g_noalloc[i].ctx == ctx) return g_noalloc[i].addr;
     }
-    return g_noalloc_addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    if (current_context(&ctx) != CUDA_SUCCESS || !ctx) return p;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    for (int i = 0; i < g_noalloc_used; ++i)
+        if (g_noalloc[i].ctx == ctx) return g_noalloc[i].addr;
+    const int slot = g_noalloc_used < kMaxContexts ? g_noalloc_used++ : kMaxContexts - 1;
+    g_noalloc[slot] = NoallocEntry{ctx, p};
+    return p;
 }
 }  // namespace
 
@@ -643,4 +747,11 @@ extern "C" ssd_status ssd_fwd_noalloc(const ssd_desc *desc, const void *x, const
     if (!scratch) return SSD_ERR_CUDA;
     return fwd_impl(desc, x, dt, A, Bm, Cm, D, h0, y, h_final, scratch, SSD_NOALLOC_SCRATCH_BYTES,
                     (cudaStream_t)stream, nullptr);
+}
+
+extern "C" ssd_status ssd_fwd_noalloc_check(ssd_stream_t stream)
+{
+    void *scratch = noalloc_scratch_address();
+    if (!scratch) return SSD_ERR_CUDA;
+    return ssd_fwd_check(scratch, stream);
 }

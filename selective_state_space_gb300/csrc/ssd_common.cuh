@@ -13,6 +13,9 @@ namespace ssd {
 // (blog section "Kernel 1: cumulative sum": the cumsum is scaled by log2(e)).
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Tokens per tensor-core sub-chunk (the M of the MMAs that walk a sequence).
+constexpr int64_t kSubChunk = 128;
+
 // Validated problem sizes, passed by value to kernels and launchers.
 struct Problem {
     int64_t B, L, nh, H, S, G, T, nc, hpg;
