@@ -228,7 +228,7 @@ ssd::FusedPlan choose_fused_plan(const Problem &pr)
             if (cache[i].npair == npair && cache[i].nsub == nsub && cache[i].nc == nc && cache[i].sms == sms)
                 return cache[i].plan;
     }
-    const ssd::FusedPlan best = ssd::fused_search(npair, nsub, nc, sms, ssd::fused_pass_slices());
+    const ssd::FusedPlan best = ssd::fused_search(npair, nsub, pr.B * pr.nh * pr.nc, sms, ssd::fused_pass_slices());
     std::lock_guard<std::mutex> lock(mu);
     const int slot = used < 16 ? used++ : (next++ % 16);
     cache[slot] = Entry{npair, nsub, nc, sms, best};

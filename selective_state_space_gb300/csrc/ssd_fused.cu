@@ -76,25 +76,31 @@ struct FusedCfg {
     // item ring [kRing], group broadcasts [3][2], abort flag
     static constexpr uint32_t kMisc = kTot + 128;
     static constexpr uint32_t kBars = kMisc + 64;
-    static constexpr int kNumBars = 19 + 2 * kRing;
+    static constexpr int kNumBars = 22 + 2 * kRing;
     static constexpr uint32_t kSmem = kBars + kNumBars * 8 + 8;
     static constexpr uint32_t kTcb = 0, kTy = 128, kTst = 384, kTmemCols = 512;
     static constexpr int kThreads = 608;
     static constexpr int kSlices = 16;                         // PASS slices per cut pair
+    static constexpr int kPassBatch = 16;                      // chained states staged per PASS copy (a power of 2)
+    static_assert(2 * kPassBatch == 32, "one decay per lane of a warp");
+    static_assert(2 * kPassBatch * (64 * 128 / kSlices) * 4 == 4 * kAtom, "PASS staging = w o x + bf16 state");
     static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
-// fFull/fFree: the C/B stage (loaded / read by its last MMA); fCb: C B^T done; fYs: C h^T
-// done; fHReady: bf16 state copy written and the decayed state back in TMEM (SCAN);
-// fXReady: w o x written; fPReady: P built and C h^T scaled; fIntra0/1: P x into Y buffer
-// 0/1 done; fUpdate: the state update (or, when it is skipped, every MMA before it) done;
-// fEpi0/1: Y buffer 0/1 drained; fXFull/fYSt: x slots (loaded / free again); fRingFull/
-// fRingEmpty: item ring slots; fDone: every MMA of the CTA done (before TMEM is freed).
-// Every barrier a role waits on by parity is one its own progress keeps within one phase
-// of the wait.
+// fFull0/1, fFree0/1: the two halves of the C/B stage (loaded / read by their last MMA): a
+// SCAN sub-chunk loads C into half 0 and B into half 1, a STATE sub-chunk loads only B, into
+// the halves in turn, so that one STATE sub-chunk's B loads while the previous one's update
+// reads the other half; fCb: C B^T done; fYs: C h^T done; fHReady: bf16 state copy written
+// and the decayed state back in TMEM (SCAN); fXReady: w o x written; fPReady: P built and
+// C h^T scaled; fIntra0/1: P x into Y buffer 0/1 done; fUpdate: the state update (or, when it
+// is skipped, every MMA before it) done; fEpi0/1: Y buffer 0/1 drained; fStage: a bulk copy
+// of the state warps into the w o x and bf16-state buffers landed (PASS items); fXFull/fYSt:
+// x slots (loaded / free again); fRingFull/fRingEmpty: item ring slots; fDone: every MMA of
+// the CTA done (before TMEM is freed).  Every barrier a role waits on by parity is one its
+// own progress keeps within one phase of the wait.
 enum FusedBar {
-    fFull = 0, fFree, fCb, fYs, fHReady, fXReady, fPReady, fIntra0, fIntra1, fUpdate, fEpi0, fEpi1,
-    fXFull0, fYSt0 = fXFull0 + 3, fRingFull0 = fYSt0 + 3, fRingEmpty0 = fRingFull0 + FusedCfg::kRing,
+    fFull0 = 0, fFull1, fFree0, fFree1, fCb, fYs, fHReady, fXReady, fPReady, fIntra0, fIntra1, fUpdate, fEpi0,
+    fEpi1, fStage, fXFull0, fYSt0 = fXFull0 + 3, fRingFull0 = fYSt0 + 3, fRingEmpty0 = fRingFull0 + FusedCfg::kRing,
     fDone = fRingEmpty0 + FusedCfg::kRing, fNumBars
 };
 static_assert(fNumBars == FusedCfg::kNumBars, "fused barriers");
@@ -169,9 +175,13 @@ __device__ __forceinline__ void cumsum_from_totals(const float2 *tot, int w4, fl
     total = all;
 }
 
+// The work item of ticket t (one out-of-line copy for every role: item boundaries are rare,
+// and the decoder's divisions would otherwise sit in each role's instruction stream).
+__device__ __noinline__ FusedItem item_of(const FusedPlan &pl, int t) { return fused_item(pl, t); }
+
 // Bounded wait until *p >= target (acquire: writes released before the increment are
 // visible to this thread afterwards).
-__device__ __forceinline__ bool wait_count(const int *p, int target, uint64_t wait_ns)
+__device__ __noinline__ bool wait_count(const int *p, int target, uint64_t wait_ns)
 {
     const long long c0 = clock64();
     const long long limit = (long long)(wait_ns * 5 / 2);
@@ -192,13 +202,93 @@ __device__ __forceinline__ uint32_t load_dt2(const __nv_bfloat16 *dt, const Prob
     return __ldg(reinterpret_cast<const unsigned int *>(dt + ((int64_t)b * pr.L + t) * pr.nh + hA));
 }
 
+// A PASS item, run by the 128 state warps (thread r; `leader` is r == 0):
+// h_start(m + 1) = 2^(log2 decay of m) h_start(m) + s_local(m), h_start(0) = h0 (or 0), for one
+// slice of the state elements of both heads of the pair, once every STATE item of the pair is
+// done.  kPassBatch chained states at a time are staged by bulk copies into the w o x and
+// bf16-state buffers (free once the MMAs of the items before are done): stage[head][k][slice].
+// One out-of-line copy: PASS items are rare, and their code stays out of the state warps'
+// per-sub-chunk instruction stream.
+__device__ __noinline__ void run_pass(const FusedItem &it, uint8_t *smem, uint64_t *bars, int r, int lane, bool leader,
+                                      int bhA, const float *__restrict__ h0, const float *s_loc, const float *sdec,
+                                      float *h_st, int *cnt, int npair, int qc, uint64_t wait_ns, int *err, bool &ok,
+                                      int &nstage, int &pass_issued)
+{
+    using Cfg = FusedCfg;
+    constexpr int64_t HS = 64 * 128;
+    constexpr int kPer = (int)(HS / Cfg::kSlices);
+    bool fail = false;
+    if (leader) {
+        if (!wait_count(cnt + it.pair, it.nsup - 1, wait_ns)) fail = true;
+        if (qc > 0 && !mbar_wait(smem_u32(&bars[fUpdate]), (qc - 1) & 1, wait_ns)) fail = true;
+    }
+    if (tc::named_bar_or(kBarState, 128, fail)) { ok = false; tc::set_error(err, tc::kErrTimeout); }
+    float *stage = (float *)(smem + Cfg::kWx);
+    const int64_t e = (int64_t)it.slice * kPer + 4 * r;   // this thread's 4 elements
+    float4 h[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        h[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (h0) {   // (h0 need only be 4-byte aligned)
+            const float *p0 = h0 + (int64_t)(bhA + hh) * HS + e;
+            h[hh] = make_float4(__ldcg(p0), __ldcg(p0 + 1), __ldcg(p0 + 2), __ldcg(p0 + 3));
+        }
+    }
+#pragma unroll 1
+    for (int m0 = 0; m0 < it.nsup - 1; m0 += Cfg::kPassBatch) {
+        const int nb = min(Cfg::kPassBatch, it.nsup - 1 - m0);
+        if (leader && ok) {
+            // the generic-proxy reads of the previous batch come before these async writes
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(smem_u32(&bars[fStage]), (uint32_t)(2 * nb * kPer * 4));
+            for (int hh = 0; hh < 2; ++hh)
+                for (int k = 0; k < nb; ++k)
+                    bulk_load(smem_u32(stage + (hh * Cfg::kPassBatch + k) * kPer),
+                              s_loc + (it.slot + (int64_t)hh * it.nsup + m0 + k) * HS + (int64_t)it.slice * kPer,
+                              (uint32_t)(kPer * 4), smem_u32(&bars[fStage]));
+            ++pass_issued;
+        }
+        if (ok && !mbar_wait(smem_u32(&bars[fStage]), nstage & 1, wait_ns)) {
+            ok = false;
+            tc::set_error(err, tc::kErrTimeout);
+        }
+        ++nstage;
+        if (ok) {
+            // the batch's decays, one per lane (head 0 in lanes 0..15, head 1 in 16..31), loaded
+            // together and handed out by shuffles
+            const int kl = lane & (Cfg::kPassBatch - 1), hl = lane / Cfg::kPassBatch;
+            float dl = 1.f;
+            if (kl < nb) dl = exp2f(__ldcg(sdec + it.slot + (int64_t)hl * it.nsup + m0 + kl));
+#pragma unroll 1
+            for (int k = 0; k < nb; ++k) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int64_t sl = it.slot + (int64_t)hh * it.nsup + m0 + k;
+                    const float d = __shfl_sync(0xffffffffu, dl, hh * Cfg::kPassBatch + k);
+                    const float4 sv = *reinterpret_cast<const float4 *>(stage + (hh * Cfg::kPassBatch + k) * kPer + 4 * r);
+                    h[hh].x = fmaf(d, h[hh].x, sv.x);
+                    h[hh].y = fmaf(d, h[hh].y, sv.y);
+                    h[hh].z = fmaf(d, h[hh].z, sv.z);
+                    h[hh].w = fmaf(d, h[hh].w, sv.w);
+                    *reinterpret_cast<float4 *>(h_st + (sl + 1) * HS + e) = h[hh];
+                }
+            }
+        }
+        // every thread is done with the batch before the next one overwrites it
+        tc::named_bar_sync(kBarState, 128);
+    }
+    __threadfence();
+    tc::named_bar_sync(kBarState, 128);
+    if (leader) atomicAdd(cnt + npair + it.pair, 1);
+}
+
 template <bool kRagged>
 __global__ void __launch_bounds__(FusedCfg::kThreads, 1)
 k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
                 const __nv_bfloat16 *__restrict__ dt, const float *__restrict__ Ap, const float *__restrict__ Dp,
                 const float *__restrict__ h0, float *__restrict__ h_final, float *s_loc, float *h_st, float *sdec,
-                int *hdr, int *cnt, Problem pr, FusedPlan pl, unsigned long long wait_ns)
+                int *hdr, int *cnt, Problem pr, const __grid_constant__ FusedPlan pl, unsigned long long wait_ns)
 {
     using Cfg = FusedCfg;
     constexpr int S = 128, kXS = Cfg::kXStages;
@@ -241,7 +331,15 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         if (lane == 0) {
             prefetch_tmap(&tmC);
             prefetch_tmap(&tmB);
-            int qc = 0;                                 // sub-chunks loaded so far
+            int uses0 = 0, uses1 = 0;                   // loads into each half of the C/B stage so far
+            int sh = 0;                                 // the half the next STATE sub-chunk loads into
+            // expect and load a C or B tile (two 64-column atoms) into half hv of the stage
+            auto load_half = [&](int hv, const CUtensorMap *map, int g, int t0, int b) {
+                const uint32_t full = smem_u32(&bars[fFull0 + hv]);
+                mbar_arrive_expect_tx(full, 2 * kAtom);
+                for (int a = 0; a < 2; ++a)
+                    tma_load_4d(smem_u32(smem + hv * Cfg::kCBytes + a * kAtom), map, full, 64 * a, g, t0, b);
+            };
             for (int n = 0;; ++n) {
                 const int s = n % Cfg::kRing;
                 if (n >= Cfg::kRing &&
@@ -257,21 +355,34 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 ring_slot[s] = t;
                 mbar_arrive(smem_u32(&bars[fRingFull0 + s]));
                 if (t < 0) break;
-                const FusedItem it = fused_item(pl, t);
+                const FusedItem it = item_of(pl, t);
                 if (it.kind == kItemPass) continue;
                 const int b = (int)((2 * it.pair) / pr.nh), g = (int)(((2 * it.pair) % pr.nh) / pr.hpg);
                 const bool scan = it.kind == kItemScan;
-                for (int q = 0; q < it.nq; ++q, ++qc) {
+#pragma unroll 1
+                for (int q = 0; q < it.nq; ++q) {
                     const int t0 = (it.sub_begin + q) * kQ;
-                    if (qc >= 1 && !mbar_wait(smem_u32(&bars[fFree]), (qc - 1) & 1, wait_ns)) { ok = false; break; }
-                    const uint32_t full = smem_u32(&bars[fFull]);
-                    mbar_arrive_expect_tx(full, scan ? Cfg::kCBStage : 2 * kAtom);
-                    for (int a = 0; a < 2; ++a) {
-                        if (scan) tma_load_4d(smem_u32(smem + a * kAtom), &tmC, full, 64 * a, g, t0, b);
-                        tma_load_4d(smem_u32(smem + Cfg::kCBytes + a * kAtom), &tmB, full, 64 * a, g, t0, b);
+                    if (scan) {
+                        // C into half 0, B into half 1
+                        if ((uses0 >= 1 && !mbar_wait(smem_u32(&bars[fFree0]), (uses0 - 1) & 1, wait_ns)) ||
+                            (uses1 >= 1 && !mbar_wait(smem_u32(&bars[fFree1]), (uses1 - 1) & 1, wait_ns))) {
+                            ok = false;
+                            break;
+                        }
+                        load_half(0, &tmC, g, t0, b);
+                        load_half(1, &tmB, g, t0, b);
+                        ++uses0;
+                        ++uses1;
+                    } else {
+                        // B into the halves in turn
+                        const int hv = sh, u = hv ? uses1 : uses0;
+                        sh ^= 1;
+                        if (u >= 1 && !mbar_wait(smem_u32(&bars[fFree0 + hv]), (u - 1) & 1, wait_ns)) { ok = false; break; }
+                        load_half(hv, &tmB, g, t0, b);
+                        if (hv) ++uses1; else ++uses0;
                     }
-                    // the tiles two sub-chunks ahead into L2: the single stage reloads right after its
-                    // last MMA has read it, so the load latency is on the critical path
+                    // the tiles two sub-chunks ahead into L2: a half reloads right after its last MMA
+                    // has read it, so the load latency is on the critical path
                     if (q + 2 < it.nq) {
                         for (int a = 0; a < 2; ++a) {
                             if (scan) tma_prefetch_4d(&tmC, 64 * a, g, t0 + 2 * kQ, b);
@@ -282,8 +393,9 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 if (!ok) break;
             }
             if (!ok) { tc::set_error(err, tc::kErrTimeout); *abort_flag = 1; }
-            // retire: the last load must have landed before the CTA may exit
-            if (qc > 0) mbar_wait(smem_u32(&bars[fFull]), (qc - 1) & 1, tc::kWaitNs);
+            // retire: the last load into each half must have landed before the CTA may exit
+            if (uses0 > 0) mbar_wait(smem_u32(&bars[fFull0]), (uses0 - 1) & 1, tc::kWaitNs);
+            if (uses1 > 0) mbar_wait(smem_u32(&bars[fFull1]), (uses1 - 1) & 1, tc::kWaitNs);
         }
         __syncwarp();
     } else if (warp == 14) {
@@ -294,7 +406,7 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             for (int n = 0;; ++n) {
                 const int t = ring.take(n, ok);
                 if (t < 0) break;
-                const FusedItem it = fused_item(pl, t);
+                const FusedItem it = item_of(pl, t);
                 if (it.kind == kItemPass) continue;
                 const int bhA = 2 * it.pair, b = (int)(bhA / pr.nh), hA = (int)(bhA % pr.nh);
                 if (it.kind == kItemScan && it.m == 0 && h0) {
@@ -337,7 +449,8 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             const uint32_t s0 = smem_u32(smem);
             const uint64_t dC = smem_desc(s0, 16, 1024);                        // C [i][s], K-major
             const uint64_t dBk = smem_desc(s0 + Cfg::kCBytes, 16, 1024);        // B [j][s], K-major
-            const uint64_t dBm = smem_desc(s0 + Cfg::kCBytes, kAtom, 1024);     // B^T [s][t], MN-major
+            const uint64_t dBm0 = smem_desc(s0, kAtom, 1024);                   // B^T [s][t], MN-major, half 0
+            const uint64_t dBm = smem_desc(s0 + Cfg::kCBytes, kAtom, 1024);     // B^T [s][t], MN-major, half 1
             const uint64_t dX = smem_desc(s0 + Cfg::kX, kAtom, 1024);           // x [t][p], MN-major
             const uint64_t dHc = smem_desc(s0 + Cfg::kHc, kAtom, 1024);         // h bf16 [s][p], 2 atoms along N
             const uint64_t dWx = smem_desc(s0 + Cfg::kWx, kAtom, 1024);         // w o x [t][p], 2 atoms along N
@@ -350,36 +463,48 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 mma_commit(smem_u32(&bars[fCb]));
             };
             int n = 0, qc = 0, qs = 0;
+            int uses0 = 0, uses1 = 0;                  // loads into each half of the C/B stage consumed so far
+            int sh = 0;                                // the half of the next STATE sub-chunk
             bool cb_issued = false;                    // C B^T of the next SCAN sub-chunk already issued
             int pending = -3;                          // an item taken ahead (-3: none)
+            auto wait_cb_tiles = [&]() -> bool {       // C (half 0) and B (half 1) of the next SCAN sub-chunk
+                return mbar_wait(smem_u32(&bars[fFull0]), uses0 & 1, wait_ns) &&
+                       mbar_wait(smem_u32(&bars[fFull1]), uses1 & 1, wait_ns);
+            };
             while (ok) {
                 int t;
                 if (pending != -3) { t = pending; pending = -3; }
                 else t = ring.take(n++, ok);
                 if (t < 0) break;
-                const FusedItem it = fused_item(pl, t);
+                const FusedItem it = item_of(pl, t);
                 if (it.kind == kItemPass) continue;
                 if (it.kind == kItemState) {
+#pragma unroll
                     for (int q = 0; q < it.nq; ++q, ++qc) {
+                        const int hv = sh;
+                        sh ^= 1;
                         // B landed and w o x written (the state warps have also read the x slot)
-                        if (!mbar_wait(smem_u32(&bars[fFull]), qc & 1, wait_ns) ||
+                        if (!mbar_wait(smem_u32(&bars[fFull0 + hv]), (hv ? uses1 : uses0) & 1, wait_ns) ||
                             !mbar_wait(smem_u32(&bars[fXReady]), qc & 1, wait_ns)) { ok = false; break; }
                         tc_fence_after();
+                        const uint64_t dB = hv ? dBm : dBm0;
 #pragma unroll
                         for (int kk = 0; kk < kQ / 16; ++kk)
-                            mma_bf16(tmem + Cfg::kTst, adv(dBm, kk * 2048), adv(dWx, kk * 2048), id_up, 1u);
+                            mma_bf16(tmem + Cfg::kTst, adv(dB, kk * 2048), adv(dWx, kk * 2048), id_up, 1u);
                         mma_commit(smem_u32(&bars[fUpdate]));
-                        mma_commit(smem_u32(&bars[fFree]));
+                        mma_commit(smem_u32(&bars[fFree0 + hv]));
+                        if (hv) ++uses1; else ++uses0;
                         mbar_arrive(smem_u32(&bars[fYSt0 + qc % kXS]));   // the x slot is free again
                     }
                     continue;
                 }
                 const bool final = it.m == it.nsup - 1 && h_final;
+#pragma unroll
                 for (int q = 0; q < it.nq; ++q, ++qc, ++qs) {
                     const int xs = qc % kXS;
                     const uint32_t ty = tmem + Cfg::kTy + (uint32_t)(qs & 1) * 128;
                     if (!cb_issued) {
-                        if (!mbar_wait(smem_u32(&bars[fFull]), qc & 1, wait_ns)) { ok = false; break; }
+                        if (!wait_cb_tiles()) { ok = false; break; }
                         tc_fence_after();
                         issue_cb();
                     }
@@ -408,7 +533,10 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                             mma_bf16(tmem + Cfg::kTst, adv(dBm, kk * 2048), adv(dWx, kk * 2048), id_up, 1u);
                     }
                     mma_commit(smem_u32(&bars[fUpdate]));
-                    mma_commit(smem_u32(&bars[fFree]));      // CB, C h^T and the update have read C and B
+                    mma_commit(smem_u32(&bars[fFree0]));     // CB and C h^T have read C,
+                    mma_commit(smem_u32(&bars[fFree1]));     // CB and the update have read B
+                    ++uses0;
+                    ++uses1;
                     // Y_h += P_h x_h (P from TMEM) once P is built and C h^T scaled
                     if (!mbar_wait(smem_u32(&bars[fPReady]), qs & 1, wait_ns)) { ok = false; break; }
                     tc_fence_after();
@@ -420,23 +548,27 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                                         adv(dX, xs * Cfg::kXSlot + hh * kAtom + kk * 2048), id_yi, 1u);
                     }
                     mma_commit(smem_u32(&bars[fIntra0 + (qs & 1)]));
-                    // C B^T of the next sub-chunk over the P just read (in issue order), when that
-                    // sub-chunk is a SCAN one: the P warps start on it while this one finishes
-                    bool next_scan = q + 1 < it.nq;
-                    if (!next_scan) {
-                        while (pending == -3) {
-                            const int t2 = ring.take(n++, ok);
-                            if (t2 >= 0 && fused_item(pl, t2).kind == kItemPass) continue;
-                            pending = t2;
-                        }
-                        next_scan = pending >= 0 && fused_item(pl, pending).kind == kItemScan;
-                    }
-                    if (next_scan && ok) {
-                        if (!mbar_wait(smem_u32(&bars[fFull]), (qc + 1) & 1, wait_ns)) { ok = false; break; }
+                    // C B^T of the next sub-chunk of the item over the P just read (in issue order): the P
+                    // warps start on it while this one finishes
+                    if (q + 1 < it.nq) {
+                        if (!wait_cb_tiles()) { ok = false; break; }
                         tc_fence_after();
                         issue_cb();
                         cb_issued = true;
                     }
+                }
+                if (!ok) break;
+                // the same for the first sub-chunk of the next item, when that item is a SCAN one
+                while (pending == -3) {
+                    const int t2 = ring.take(n++, ok);
+                    if (t2 >= 0 && item_of(pl, t2).kind == kItemPass) continue;
+                    pending = t2;
+                }
+                if (ok && pending >= 0 && item_of(pl, pending).kind == kItemScan) {
+                    if (!wait_cb_tiles()) { ok = false; break; }
+                    tc_fence_after();
+                    issue_cb();
+                    cb_issued = true;
                 }
             }
             if (!ok) { tc::set_error(err, tc::kErrTimeout); *abort_flag = 1; }
@@ -455,56 +587,15 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         uint8_t *hc = smem + Cfg::kHc;
         float2 *tot = (float2 *)(smem + Cfg::kTot);    // [2 buffers][4 warps]
         int qc = 0;
+        int nstage = 0, pass_issued = 0;               // bulk copies into the staging buffers: waited, issued
         for (int n = 0;; ++n) {
             const int t = ring.group_take(n, leader, kBarState, 128, bcast_state, ok, err);
             if (t < 0) break;
-            const FusedItem it = fused_item(pl, t);
+            const FusedItem it = item_of(pl, t);
             const int bhA = 2 * it.pair, b = (int)(bhA / pr.nh), hA = (int)(bhA % pr.nh);
             if (it.kind == kItemPass) {
-                // h_start(m + 1) = 2^(log2 decay of m) h_start(m) + s_local(m), h_start(0) = h0 (or 0),
-                // for this slice of the state elements of both heads, once every STATE item of the pair
-                // is done
-                bool fail = false;
-                if (leader && !wait_count(cnt + it.pair, it.nsup - 1, wait_ns)) fail = true;
-                if (tc::named_bar_or(kBarState, 128, fail)) { ok = false; tc::set_error(err, tc::kErrTimeout); }
-                if (ok) {
-                    const int64_t e = (int64_t)it.slice * (HS / Cfg::kSlices) + 4 * r;
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int64_t sl = it.slot + (int64_t)hh * it.nsup;    // slot of super-chunk 0
-                        float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (h0) {   // (h0 need only be 4-byte aligned)
-                            const float *p0 = h0 + (int64_t)(bhA + hh) * HS + e;
-                            h = make_float4(__ldcg(p0), __ldcg(p0 + 1), __ldcg(p0 + 2), __ldcg(p0 + 3));
-                        }
-#pragma unroll 1
-                        for (int m0 = 0; m0 < it.nsup - 1; m0 += 4) {
-                            float4 sv[4];
-                            float dv[4];
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                if (m0 + k < it.nsup - 1) {
-                                    sv[k] = __ldcg(reinterpret_cast<const float4 *>(s_loc + (sl + m0 + k) * HS + e));
-                                    dv[k] = __ldcg(sdec + sl + m0 + k);
-                                }
-                            }
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                if (m0 + k < it.nsup - 1) {
-                                    const float d = exp2f(dv[k]);
-                                    h.x = fmaf(d, h.x, sv[k].x);
-                                    h.y = fmaf(d, h.y, sv[k].y);
-                                    h.z = fmaf(d, h.z, sv[k].z);
-                                    h.w = fmaf(d, h.w, sv[k].w);
-                                    *reinterpret_cast<float4 *>(h_st + (sl + m0 + k + 1) * HS + e) = h;
-                                }
-                            }
-                        }
-                    }
-                }
-                __threadfence();
-                tc::named_bar_sync(kBarState, 128);
-                if (leader) atomicAdd(cnt + pl.npair + it.pair, 1);
+                run_pass(it, smem, bars, r, lane, leader, bhA, h0, s_loc, sdec, h_st, cnt, pl.npair, qc, wait_ns, err, ok,
+                         nstage, pass_issued);
                 continue;
             }
             const bool scan = it.kind == kItemScan;
@@ -523,6 +614,58 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             }
             float2 dsum = make_float2(0.f, 0.f);        // log2 decay of the whole item (STATE)
             uint32_t n_dt = load_dt2<kRagged>(dt, pr, b, hA, (int64_t)it.sub_begin * kQ + r);
+            // The entering state, as it is, into the state columns of TMEM before the sub-chunk loop
+            // (which then always starts from TMEM), once the MMAs of the items before are done with
+            // them: from memory with 16-byte alignment by two bulk copies into the w o x and
+            // bf16-state buffers ([head][p][s] float32), else by plain loads, or zeros.
+            {
+                const bool staged = srcA && ((uintptr_t)srcA & 15u) == 0 && ((hstride * 4) & 15) == 0;
+                if (qc > 0 && ok && !mbar_wait(smem_u32(&bars[fUpdate]), (qc - 1) & 1, wait_ns)) {
+                    ok = false;
+                    tc::set_error(err, tc::kErrTimeout);
+                }
+                if (staged) {
+                    if (leader && ok) {
+                        fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(smem_u32(&bars[fStage]), (uint32_t)(2 * HS * 4));
+                        for (int hh = 0; hh < 2; ++hh)
+                            bulk_load(smem_u32(smem + Cfg::kWx + hh * HS * 4), srcA + hh * hstride,
+                                      (uint32_t)(HS * 4), smem_u32(&bars[fStage]));
+                        ++pass_issued;
+                    }
+                    if (ok && !mbar_wait(smem_u32(&bars[fStage]), nstage & 1, wait_ns)) {
+                        ok = false;
+                        tc::set_error(err, tc::kErrTimeout);
+                    }
+                    ++nstage;
+                }
+                if (ok) {
+                    const float *stg = (const float *)(smem + Cfg::kWx) + r;
+#pragma unroll 1
+                    for (int hc32 = 0; hc32 < 4; ++hc32) {
+                        const int hh = hc32 >> 1, c32 = 32 * (hc32 & 1);
+                        uint32_t v[32];
+                        if (staged) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(stg[(hh * 64 + c32 + j) * S]);
+                        } else if (srcA) {
+                            const float *src = srcA + hh * hstride + r;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__ldcg(src + (int64_t)(c32 + j) * S));
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = 0u;
+                        }
+                        const uint32_t ta = tmem + lane_base + Cfg::kTst + 64 * hh + c32;
+                        tmem_st16(ta + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                        tmem_st16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    }
+                    tmem_st_wait();
+                }
+                // every thread has read the staging buffers before the hand-off writes the bf16 copy
+                // over them
+                if (staged) tc::named_bar_sync(kBarState, 128);
+            }
             for (int q = 0; q < it.nq; ++q, ++qc) {
                 const int xs = qc % kXS;
                 const float2 dtp = tc::unpack_bf16x2(n_dt);
@@ -538,11 +681,9 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 dsum.y += gl.y;
                 // the update of qc - 1 has produced the state and read w o x (and C h^T of the same
                 // sub-chunk, issued before it, has read the bf16 copy)
-                if (qc > 0 && ok) {
-                    if (!mbar_wait(smem_u32(&bars[fUpdate]), (qc - 1) & 1, wait_ns)) {
-                        ok = false;
-                        tc::set_error(err, tc::kErrTimeout);
-                    }
+                if (q > 0 && ok && !mbar_wait(smem_u32(&bars[fUpdate]), (qc - 1) & 1, wait_ns)) {
+                    ok = false;
+                    tc::set_error(err, tc::kErrTimeout);
                 }
                 if (ok) {
                     tc_fence_after();
@@ -554,20 +695,9 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                         const float dec = exp2f(hh ? gl.y : gl.x);
                         const uint32_t ta = tmem + lane_base + Cfg::kTst + 64 * hh + c32;
                         uint32_t v[32];
-                        if (q == 0) {
-                            if (srcA) {
-                                const float *src = srcA + hh * hstride + r;
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__ldcg(src + (int64_t)(c32 + j) * S));
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] = 0u;
-                            }
-                        } else {
-                            tmem_ld16(ta + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                            tmem_ld16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-                            tmem_ld_wait();
-                        }
+                        tmem_ld16(ta + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                        tmem_ld16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                        tmem_ld_wait();
                         if (scan) {
                             uint8_t *hrow = hc + hh * kAtom;
 #pragma unroll
@@ -640,7 +770,7 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                     for (int hh = 0; hh < 2; ++hh) {
                         float *dst = scan ? h_final + (int64_t)(bhA + hh) * HS + r
                                           : s_loc + (it.slot + (int64_t)hh * it.nsup) * HS + r;
-#pragma unroll
+#pragma unroll 1
                         for (int c0 = 0; c0 < 64; c0 += 16) {
                             uint32_t v[16];
                             tmem_ld16(tmem + lane_base + Cfg::kTst + 64 * hh + c0, v);
@@ -663,6 +793,8 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             }
         }
         if (!ok) *abort_flag = 1;
+        // retire: a staging copy whose wait expired must land before the CTA may exit
+        if (leader && pass_issued > 0) mbar_wait(smem_u32(&bars[fStage]), (pass_issued - 1) & 1, tc::kWaitNs);
     } else if (warp < 14) {
         // ---- P warps: P and the scaled C h^T of each SCAN sub-chunk ---------------------------
         const int half = (warp - 6) >> 2;              // columns 64 half .. 64 half + 63; C h^T of head `half`
@@ -679,7 +811,7 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         for (int n = 0;; ++n) {
             const int t = ring.group_take(n, leader, kBarP, 256, bcast_p, ok, err);
             if (t < 0) break;
-            const FusedItem it = fused_item(pl, t);
+            const FusedItem it = item_of(pl, t);
             if (it.kind != kItemScan) continue;
             const int bhA = 2 * it.pair, b = (int)(bhA / pr.nh), hA = (int)(bhA % pr.nh);
             const float2 a2 = make_float2(Ap[hA] * kLog2e, Ap[hA + 1] * kLog2e);
@@ -825,7 +957,7 @@ k_ssd_fwd_fused(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         for (int n = 0;; ++n) {
             const int t = ring.group_take(n, leader, kBarEpi, 128, bcast_epi, ok, err);
             if (t < 0) break;
-            const FusedItem it = fused_item(pl, t);
+            const FusedItem it = item_of(pl, t);
             if (it.kind == kItemPass) continue;
             if (it.kind == kItemState) { qc += it.nq; continue; }
             const int bhA = 2 * it.pair, b = (int)(bhA / pr.nh), hA = (int)(bhA % pr.nh);
@@ -910,6 +1042,7 @@ cudaError_t launch_fused_pair(const Problem &pr, const void *x, const void *dt, 
     auto kern = pr.L % kQ == 0 ? k_ssd_fwd_fused<false> : k_ssd_fwd_fused<true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FusedCfg::kSmem);
     if (e != cudaSuccess) return e;
+
     const int grid = pl.n_items < tc::current_sms() ? pl.n_items : tc::current_sms();
     kern<<<grid, FusedCfg::kThreads, FusedCfg::kSmem, st>>>(mC, mB, mX, mY, (const __nv_bfloat16 *)dt, A, D, h0,
                                                            h_final, w.s_local, w.h_start, w.sdec, w.hdr, w.cnt, pr,
