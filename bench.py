@@ -39,9 +39,8 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 STAGES = ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")
 KERNEL_SOURCES = {  # the files that hold each kernel (for the traffic record's freshness check)
     "chunk_cumsum": ["ssd_simt.cu"], "state_passing": ["ssd_simt.cu"],
-    "chunk_state": ["ssd_tc.cu", "sm100_ptx.cuh", "tc_common.cuh"],
-    "chunk_scan": ["ssd_tc.cu", "sm100_ptx.cuh", "tc_common.cuh"],
-    "k_ssd_fwd_fused": ["ssd_fused.cu", "fused_plan.cuh", "sm100_ptx.cuh", "tc_common.cuh"],
+    "chunk_state": ["ssd_tc.cu", "sm100_ptx.cuh"],
+    "chunk_scan": ["ssd_tc.cu", "sm100_ptx.cuh"],
 }
 
 
@@ -63,11 +62,7 @@ def stage_bytes(s: workloads.Shape, plan: dict):
     the intermediates it moves counted: G, the float32 dt copy, the super-chunk states and the
     super-chunk-start states, all float32; 0 for a stage that does not launch.  A plan cuts the
     sequences ((batch, head) pairs) in two parts; chunk_state and state_passing run per part and
-    their bytes are summed.  With the fused kernel (plan["fused"]) every stage is one launch,
-    reported under "chunk_scan": the compulsory I/O, plus the x and B of the super-chunks whose
-    state a STATE item computes (read a second time), plus each such state written once, read
-    once and written once more as the entering state by the PASS items, and read by its SCAN
-    item.  Also the whole-step compulsory I/O ("step": each input read once, each
+    their bytes are summed.  Also the whole-step compulsory I/O ("step": each input read once, each
     output written once, intermediates excluded)."""
     e = esize(s.dtype)
     Bsz, L, nh, H, S, G, T, nc = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups, s.chunk, s.nchunks
@@ -85,15 +80,6 @@ def stage_bytes(s: workloads.Shape, plan: dict):
     split = plan["split_sequences"]
     parts = [(0, split, plan["super_tokens"], plan["n_super"]),
              (split, nseq - split, plan["tail_super_tokens"], plan["tail_n_super"])]
-    if plan["fused"]:
-        extra = 0.0
-        for lo, n, tok, nsup in parts:
-            if n == 0 or nsup <= 1:
-                continue
-            frac = (nsup - 1) * tok / L                 # share of each cut sequence a STATE item reads
-            groups = len({(bh // nh, (bh % nh) // hpg) for bh in range(lo, lo + n)})
-            extra += frac * (n * L * (H * e + e) + groups * L * S * e) + 4 * n * (nsup - 1) * hs
-        return {"chunk_cumsum": 0, "chunk_state": 0, "state_passing": 0, "chunk_scan": step + extra, "step": step}
     cs = sp = carried = 0.0
     if plan["tensor_cores"]:
         parts = [(lo, n, tok // T, nsup) for lo, n, tok, nsup in parts]
@@ -786,10 +772,10 @@ def main():
     peaks, peak_kind = load_peaks()
     sb = stage_bytes(shape, plan)
     top = max(STAGES, key=lambda s_: stage_ms[s_] if sb[s_] else -1.0)
-    kname = "k_ssd_fwd_fused" if plan["fused"] else top
-    # the dominant kernel's algorithmic bytes are the compulsory I/O it owns -- every
-    # input read once and every output written once (intermediates excluded); the fused kernel and
-    # the scan of the four-stage path both read every input and write every output of the step
+    kname = top
+    # the dominant kernel's algorithmic bytes are the compulsory I/O of the step --
+    # every input read once and every output written once, intermediates excluded (the scan reads
+    # every input and writes every output of the step)
     alg_top = sb["step"]
     achieved = alg_top / (stage_ms[top] * 1e-3) / 1e9
     # a kernel timed inside a long step: burst copy bandwidth is the only HBM figure measured

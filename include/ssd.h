@@ -83,11 +83,13 @@ typedef struct {
  * exist for the shape (both are GPU code; this exists for cross-checking). */
 #define SSD_FLAG_FORCE_SIMT 1
 
-/* Test hook of the failure path: every bounded wait inside the tensor-core kernels that is
- * not satisfied at once expires (a bound of zero instead of 250 ms).  The call then winds
- * down without hanging -- each kernel still retires the copies and MMAs it has issued --
- * and ssd_fwd_check reports SSD_ERR_TIMEOUT; its outputs are invalid.  Never set it in
- * production code. */
+/* Test hook of the failure path: the tensor-core kernels run in a build of their own in
+ * which every wait for another warp's work tests its barrier once and expires unless the
+ * phase is already complete (the normal kernels wait up to 250 ms).  The call then winds
+ * down without hanging -- each CTA still waits for the copies and MMAs it has issued
+ * before it releases its tensor memory -- and ssd_fwd_check reports SSD_ERR_TIMEOUT; its
+ * outputs are invalid.  The CUDA-core kernels have no such waits and ignore the flag.
+ * Never set it in production code. */
 #define SSD_FLAG_EXPIRE_WAITS 2
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -108,18 +110,16 @@ ssd_status ssd_fwd_path(const ssd_desc *desc, int32_t *uses_tensor_cores);
 
 /* How ssd_fwd runs `desc` on the current device (written to *plan): which path,
  * how each sequence ((batch, head) pair, in b * nh + h order) is cut into
- * super-chunks (a tensor-core CTA walks one super-chunk of one sequence, or of two,
- * with the state on chip; the CUDA-core path uses one chunk), and how many kernels and
+ * super-chunks (the tensor-core scan walks one super-chunk per CTA with the
+ * state on chip; the CUDA-core path uses one chunk), and how many kernels and
  * cudaMemsetAsync calls one ssd_fwd call issues on its stream.  The first
- * split_sequences sequences are cut into super-chunks of super_tokens tokens, the
- * remaining ones into super-chunks of tail_super_tokens tokens.  fused = 1: one
- * persistent kernel runs every stage for two heads of one B/C group per work item
- * (S = 128, H = 64, an even number of heads per group), and work_items is the length
- * of its work list.  Host-side query: it reads the device's SM count and launches
- * nothing.  Errors: SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED, as for ssd_fwd. */
+ * split_sequences sequences are cut into super-chunks of super_tokens tokens,
+ * the remaining ones into super-chunks of tail_super_tokens tokens (so that the
+ * last wave of scan CTAs still covers the SMs).  Host-side query: it reads the
+ * device's SM count and launches nothing.
+ * Errors: SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED, as for ssd_fwd. */
 typedef struct {
     int32_t tensor_cores;          /* 1: tcgen05 kernels for chunk_state and chunk_scan   */
-    int32_t fused;                 /* 1: the single fused kernel (implies tensor_cores)   */
     int32_t super_tokens;          /* tokens per super-chunk, first split_sequences seqs  */
     int32_t n_super;               /* their super-chunks per sequence                     */
     int32_t split_sequences;       /* sequences cut with super_tokens (<= B * nh)         */
@@ -127,7 +127,6 @@ typedef struct {
     int32_t tail_n_super;          /* their super-chunks per sequence                     */
     int32_t kernel_launches;       /* kernels per ssd_fwd call (0 for an empty problem)   */
     int32_t memsets;               /* cudaMemsetAsync calls per ssd_fwd call              */
-    int32_t work_items;            /* fused: work items (tickets) per call; 0 otherwise   */
 } ssd_plan;
 
 ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan);
@@ -288,8 +287,9 @@ ssd_status ssd_s6_fwd(const ssd_s6_desc *desc, const void *x, const void *delta,
  *    executions overlap on the GPU (different streams, or different host
  *    threads without ordering) race on it and give wrong results.  Order them
  *    on one stream.  The array keeps the previous call's contents; each call
- *    clears the parts that must start at zero (the error word and the counters
- *    of the work list) and writes every other scratch byte before reading it.
+ *    clears what must start at zero (the error word, and the partial state
+ *    sums when its plan adds them with atomics) and writes every other
+ *    scratch byte before reading it.
  *  - A bounded wait that expired inside the call is reported by
  *    ssd_fwd_noalloc_check (the error word lives in the array too).
  * Arguments, layouts and the other errors are those of ssd_fwd.            */

@@ -38,10 +38,9 @@ class S6Desc(ctypes.Structure):
 
 
 class Plan(ctypes.Structure):
-    _fields_ = [("tensor_cores", ctypes.c_int32), ("fused", ctypes.c_int32), ("super_tokens", ctypes.c_int32),
-                ("n_super", ctypes.c_int32), ("split_sequences", ctypes.c_int32),
-                ("tail_super_tokens", ctypes.c_int32), ("tail_n_super", ctypes.c_int32),
-                ("kernel_launches", ctypes.c_int32), ("memsets", ctypes.c_int32), ("work_items", ctypes.c_int32)]
+    _fields_ = [("tensor_cores", ctypes.c_int32), ("super_tokens", ctypes.c_int32), ("n_super", ctypes.c_int32),
+                ("split_sequences", ctypes.c_int32), ("tail_super_tokens", ctypes.c_int32),
+                ("tail_n_super", ctypes.c_int32), ("kernel_launches", ctypes.c_int32), ("memsets", ctypes.c_int32)]
 
 
 class SSDError(RuntimeError):

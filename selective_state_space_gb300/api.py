@@ -73,13 +73,12 @@ def uses_tensor_cores(desc: Desc) -> bool:
 
 
 def fwd_plan(desc: Desc) -> dict:
-    """How ssd_fwd runs ``desc`` on the current device (ssd_fwd_plan): path (tensor cores,
-    and whether the single fused kernel runs every stage), tokens per super-chunk and
-    super-chunks per sequence for the first ``split_sequences`` sequences and for the rest
-    (``tail_*``), kernel launches and memsets per call, and the fused kernel's work items."""
+    """How ssd_fwd runs ``desc`` on the current device (ssd_fwd_plan): path, tokens per
+    super-chunk and super-chunks per sequence for the first ``split_sequences`` sequences
+    and for the rest (``tail_*``), kernel launches and memsets per call."""
     p = _native.Plan()
     check("ssd_fwd_plan", _native.load().ssd_fwd_plan(ctypes.byref(desc), ctypes.byref(p)))
-    return {name: (bool(getattr(p, name)) if name in ("tensor_cores", "fused") else int(getattr(p, name)))
+    return {name: (bool(getattr(p, name)) if name == "tensor_cores" else int(getattr(p, name)))
             for name, _ in _native.Plan._fields_}
 
 

@@ -58,14 +58,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase)
     return ok != 0;
 }
 
+// Non-blocking test of the same condition (mbarrier.test_wait never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t phase)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with parity `phase` to complete; false once about `limit_ns` has
 // passed.  The bound is kept in SM clock cycles (cheap to read; 2.5 cycles per ns covers
 // clocks up to 2.5 GHz, so at lower clocks the bound is longer, never shorter) and is
-// checked every 64 polls so that polling stays tight.  The first poll is inlined at each
-// call site; the polling loop is one out-of-line copy, so that the many call sites of the
-// warp-specialised kernels do not each carry it through the instruction cache.
-static __device__ __noinline__ bool mbar_wait_poll(uint32_t bar, uint32_t phase, uint64_t limit_ns)
+// checked every 64 polls so that polling stays tight.  A bound of 0 tests once without
+// suspending (try_wait itself may suspend the thread until the phase completes).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, uint64_t limit_ns)
 {
+    if (limit_ns == 0) return mbar_test_wait(bar, phase);
+    if (mbar_try_wait(bar, phase)) return true;
     const long long c0 = clock64();
     const long long limit = (long long)(limit_ns * 5 / 2);
     uint32_t spins = 0;
@@ -73,12 +88,6 @@ static __device__ __noinline__ bool mbar_wait_poll(uint32_t bar, uint32_t phase,
         if ((++spins & 63u) == 0 && clock64() - c0 > limit) return false;
     }
     return true;
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, uint64_t limit_ns)
-{
-    if (mbar_try_wait(bar, phase)) return true;
-    return mbar_wait_poll(bar, phase, limit_ns);
 }
 
 // 2^x with the hardware approximation (PTX ex2.approx.ftz.f32): relative error near

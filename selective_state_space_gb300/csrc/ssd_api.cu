@@ -50,6 +50,7 @@ ssd_status check_desc(const ssd_desc *d, Problem *pr, bool need_seq)
     pr->hpg = d->ngroups ? d->nheads / d->ngroups : 1;
     pr->in_dt = d->in_dtype;
     pr->out_dt = d->out_dtype;
+    pr->wait_ns = (d->flags & SSD_FLAG_EXPIRE_WAITS) ? 0ull : 250000000ull;
     if (need_seq && pr->nc > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
     return SSD_OK;
 }
@@ -96,13 +97,6 @@ ssd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_E
 bool use_tensor_cores(const ssd_desc *desc, const Problem &pr)
 {
     return !(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr);
-}
-
-// Bound on the waits inside the tensor-core kernels: 250 ms, or none at all (every wait that is
-// not satisfied at once expires) under SSD_FLAG_EXPIRE_WAITS, the test hook of the timeout path.
-unsigned long long wait_limit_ns(const ssd_desc *desc)
-{
-    return (desc->flags & SSD_FLAG_EXPIRE_WAITS) ? 0ull : 250000000ull;
 }
 
 int device_sms()
@@ -203,48 +197,6 @@ void plan_parts(const Problem &pr, const ssd::ScanSplit &sp, PlanPart out[2])
     out[1] = PlanPart{ssd::SeqRange{sp.split, pr.B * pr.nh - sp.split}, sp.R1, sp.nsup1, sp.base1};
 }
 
-// ---- work list of the fused kernel (two heads per item; see fused_plan.cuh) ----------------
-
-bool use_fused(const ssd_desc *desc, const Problem &pr)
-{
-    return use_tensor_cores(desc, pr) && ssd::scan_seqs_per_cta(pr) == 2;
-}
-
-// The fused kernel's plan for this shape on this device (fused_plan.cuh: the search
-// simulates every candidate schedule), cached per (pairs, sub-chunks, chunks, SMs).
-ssd::FusedPlan choose_fused_plan(const Problem &pr)
-{
-    const int sms = device_sms();
-    const int npair = (int)(pr.B * pr.nh / 2);
-    const int nsub = (int)((pr.L + ssd::kSubChunk - 1) / ssd::kSubChunk);
-    const int nc = (int)pr.nc;
-    struct Entry { int npair, nsub, nc, sms; ssd::FusedPlan plan; };
-    static std::mutex mu;
-    static Entry cache[16];
-    static int used = 0, next = 0;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        for (int i = 0; i < used; ++i)
-            if (cache[i].npair == npair && cache[i].nsub == nsub && cache[i].nc == nc && cache[i].sms == sms)
-                return cache[i].plan;
-    }
-    const ssd::FusedPlan best = ssd::fused_search(npair, nsub, pr.B * pr.nh * pr.nc, sms, ssd::fused_pass_slices());
-    std::lock_guard<std::mutex> lock(mu);
-    const int slot = used < 16 ? used++ : (next++ % 16);
-    cache[slot] = Entry{npair, nsub, nc, sms, best};
-    return best;
-}
-
-// Workspace of the fused path, carved from the standard one: the header (error word, ticket)
-// with the per-pair counters right after it (one memset clears both), the log2 decays where
-// the float32 dt copy would be, and the two state arrays where they always are.
-ssd::FusedWork carve_fused(const Workspace &w)
-{
-    return ssd::FusedWork{w.err, (int *)w.G, w.dtT, w.s_local, w.h_start};
-}
-
-size_t fused_clear_bytes(const Problem &pr) { return kWsAlign + (size_t)(pr.B * pr.nh) * sizeof(int); }
-
 ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const float *A,
                     const void *Bm, const void *Cm, const float *D, const float *h0, void *y,
                     float *h_final, void *workspace, size_t ws_bytes, cudaStream_t st,
@@ -281,17 +233,6 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
 
     auto rec = [&](int i) -> bool { return !events || cudaEventRecord((cudaEvent_t)events[i], st) == cudaSuccess; };
     const bool tc = use_tensor_cores(desc, pr);
-    if (use_fused(desc, pr)) {
-        // one kernel for every stage (ssd_fused.cu); the stage events 0..5 stay empty
-        const ssd::FusedPlan fp = choose_fused_plan(pr);
-        if (cudaMemsetAsync(w.err, 0, fused_clear_bytes(pr), st) != cudaSuccess) return SSD_ERR_CUDA;
-        for (int i = 0; i < 7; ++i)
-            if (!rec(i)) return SSD_ERR_CUDA;
-        if (ssd::launch_fused_pair(pr, x, dt, A, Bm, Cm, D, h0, h_final, y, fp, carve_fused(w), wait_limit_ns(desc),
-                                   st) != cudaSuccess || !rec(7))
-            return SSD_ERR_CUDA;
-        return SSD_OK;
-    }
     if (cudaMemsetAsync(w.err, 0, sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
     ssd::ScanSplit sp{};
     PlanPart parts[2];
@@ -407,19 +348,7 @@ ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan)
         return SSD_OK;
     }
     const int32_t nseq = (int32_t)(pr.B * pr.nh);
-    if (use_fused(desc, pr)) {
-        const ssd::FusedPlan fp = choose_fused_plan(pr);
-        p.fused = 1;
-        p.super_tokens = (int32_t)std::min<int64_t>(fp.R0 * ssd::kSubChunk, pr.L);
-        p.n_super = fp.nsup0;
-        p.split_sequences = 2 * fp.split;
-        p.tail_super_tokens = (int32_t)std::min<int64_t>(fp.R1 * ssd::kSubChunk, pr.L);
-        p.tail_n_super = fp.nsup1;
-        p.kernel_launches = 1;
-        p.memsets = 1;                         // the error word, the ticket and the per-pair counters
-        p.work_items = fp.n_items;
-    } else if (p.tensor_cores) {
-        const ssd::ScanSplit sp = choose_tc_plan(pr);
+    if (p.tensor_cores) {        const ssd::ScanSplit sp = choose_tc_plan(pr);
         PlanPart parts[2];
         plan_parts(pr, sp, parts);
         p.super_tokens = (int32_t)std::min<int64_t>(sp.R0 * pr.T, pr.L);

@@ -21,26 +21,92 @@
 //    warps straight into the swizzled layout the MMA reads.
 //  * One elected thread issues all MMAs; accumulators live in TMEM and are drained
 //    with tcgen05.ld.  Every wait is bounded; on expiry the kernel records an error
-//    bit in the workspace and winds down.
+//    bit in the workspace and winds down: each role stops, the loaders wait for the
+//    copies they issued to land, the MMA thread for its MMAs to complete and the
+//    storer for its bulk stores to finish reading, and only then is TMEM released and
+//    the CTA retired.  A warp enters every wait converged (after a named barrier, an
+//    arrive by all its lanes or a __syncwarp), so its lanes poll the barrier and read the
+//    clock together and agree on the answer: the warp-collective TMEM instructions and the
+//    named barriers after a wait always see whole warps.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "sm100_ptx.cuh"
 #include "ssd_tc.cuh"
-#include "tc_common.cuh"
 
 namespace ssd {
 namespace {
 
 using namespace ptx;
 
-using tc::kAtom;
-using tc::kQ;
-using tc::kWaitNs;
-using tc::mul_bf16x2;
-using tc::named_bar_sync;
-using tc::pack_bf16x2;
-using tc::set_error;
-using tc::sw128;
-using tc::unpack_bf16x2;
-
+constexpr int kQ = 128;                       // tokens per tensor-core sub-chunk (MMA M)
 constexpr int kPB = 64;                       // p-columns per scan unit (one swizzle atom)
+constexpr uint32_t kAtom = kQ * 128;          // bytes of one 128-row x 128-byte swizzled region
+// Bound on every wait: 250 ms (legitimate waits take microseconds).  Each kernel also has an
+// instantiation for the test hook of the timeout path (kExpire, chosen when Problem::wait_ns
+// is 0) in which every wait for another warp's work tests its barrier once and expires if the
+// phase is not complete; the waits for hardware the CTA itself started (a TMA load, an MMA),
+// which always end, keep the full bound there too.
+constexpr uint64_t kRetireNs = 250000000ull;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Two bf16 products (the low and high halves of u times w), rounded to bf16.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t u, __nv_bfloat162 w)
+{
+    __nv_bfloat162 v = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&u), w);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t u)
+{
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
+    return __bfloat1622float2(v);
+}
+
+// Byte offset of 16-byte chunk c of row r inside a 1024-byte-aligned region of
+// 128-byte rows with the 128-byte swizzle (the layout TMA writes and the MMA reads).
+__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + (((c ^ (r & 7u)) & 7u) << 4); }
+
+// Hardware barrier among `nthreads` threads (named barrier `id`).  Callers keep their
+// control flow uniform -- every participating thread reaches every call, errors or
+// not -- so this never waits on a thread that left.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void set_error(int *err, int bit)
+{
+    if (err) atomicOr(err, bit);
+}
+
+// (The two retire helpers run once, at the end of a role; they are kept out of line so that
+// the kernels' hot loops keep their register allocation and code layout.)
+// Wait for the loads a loader issued into a ring of `stages` slots to land: load i (of
+// `issued`) went to slot i % stages, whose barrier bars[first + i % stages] completes phase
+// (i / stages) & 1 when it lands.  A loader re-arms a slot only once the slot's consumers
+// are done with it, which they are only after its previous load landed, so only the last
+// `stages` loads can still be in flight.
+__device__ __noinline__ void retire_loads(uint64_t *bars, int first, int stages, int issued, int *err)
+{
+    for (int i = issued > stages ? issued - stages : 0; i < issued; ++i)
+        if (!mbar_wait(smem_u32(&bars[first + i % stages]), (uint32_t)(i / stages) & 1u, kRetireNs)) set_error(err, 1);
+}
+
+// The MMA thread: wait until every MMA it issued has completed (a commit to `bar`, used for
+// nothing else, arrives once they all have).
+__device__ __noinline__ void retire_mmas(uint32_t bar, int *err)
+{
+    mma_commit(bar);
+    if (!mbar_wait(bar, 0, kRetireNs)) set_error(err, 1);
+}
 
 // Token index t clamped to the sequence, and whether t holds a token: only a kernel built for
 // a ragged last chunk (kRagged) pays for the checks; with whole chunks every t is inside.
@@ -85,8 +151,9 @@ struct StateCfg {
     static constexpr uint32_t kGl = kStages * kStage;
     static constexpr uint32_t kGraw = kGl + 2 * HG * kMaxR * 4;
     static constexpr uint32_t kBars = kGraw + HG * kMaxR * 4;
-    // barriers: full[kStages], free[kStages], x_ready[kStages], done, drained; then the TMEM slot
-    static constexpr int kNumBars = 3 * kStages + 2;
+    // barriers: full[kStages], free[kStages], x_ready[kStages], done, drained, retire; then the
+    // TMEM slot
+    static constexpr int kNumBars = 3 * kStages + 3;
     static constexpr uint32_t kSmem = kBars + kNumBars * 8 + 8 + 1024;
     static constexpr uint32_t kCols = (S / 128) * kN;
     static constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : (kCols <= 64 ? 64 : (kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512)));
@@ -113,7 +180,7 @@ __device__ __forceinline__ StateUnit state_unit(int64_t u, int64_t bhg_lo, int64
     return r;
 }
 
-template <int S, int H, int HG>
+template <int S, int H, int HG, bool kExpire>
 __global__ void __launch_bounds__(192, 1)
 k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmX,
                  const float *__restrict__ G, const __nv_bfloat16 *__restrict__ dt, const float *__restrict__ dtT,
@@ -122,6 +189,7 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
 {
     using Cfg = StateCfg<S, H, HG>;
     constexpr int kN = Cfg::kN, kS = Cfg::kStages, kTok = Cfg::kTok;
+    constexpr uint64_t kWait = kExpire ? 0ull : kRetireNs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float *sGl = (float *)(smem + Cfg::kGl);
@@ -129,6 +197,7 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
     uint64_t *bars = (uint64_t *)(smem + Cfg::kBars);
     uint32_t *tmem_slot = (uint32_t *)(bars + Cfg::kNumBars);
     constexpr int kFullB = 0, kFreeB = kS, kReadyB = 2 * kS, kDoneB = 3 * kS, kDrainedB = 3 * kS + 1;
+    constexpr int kRetireB = 3 * kS + 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int nhq = (int)(pr.nh / HG);
@@ -160,9 +229,11 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
         if (lane == 0) {
             prefetch_tmap(&tmB);
             prefetch_tmap(&tmX);
+            int issued = 0;
             for (int64_t gq = q_lo; gq < q_hi; ++gq) {
                 const int i = (int)(gq - q_lo), st = i % kS;
-                if (i >= kS && !mbar_wait(smem_u32(&bars[kFreeB + st]), ((i / kS) - 1) & 1, kWaitNs)) {
+                // (the MMAs that free a stage wait for its load: free implies landed)
+                if (i >= kS && !mbar_wait(smem_u32(&bars[kFreeB + st]), ((i / kS) - 1) & 1, kWait)) {
                     ok = false; set_error(err, 1); break;
                 }
                 const StateUnit un = state_unit(gq / nq_u, bhg_lo, nbhg, nhq, HG);
@@ -184,7 +255,9 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
                 for (int a = 0; a < kN / 64; ++a)   // atom a: head h0 + a / (H/64), columns 64 * (a % (H/64))
                     tma_load_4d(smem_u32(base + Cfg::kBBytes + a * Cfg::kAtomT), &tmX, full, 64 * (a % (H / 64)),
                                 un.h0 + a / (H / 64), t0, un.b);
+                ++issued;
             }
+            retire_loads(bars, kFullB, kS, issued, err);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -196,10 +269,10 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
                 const bool first = gq == q_lo || gq % nq_u == 0;
                 const bool last = gq + 1 == q_hi || (gq + 1) % nq_u == 0;
                 // a new piece overwrites the accumulator: the previous one must be drained
-                if (first && piece > 0 && !mbar_wait(smem_u32(&bars[kDrainedB]), (piece - 1) & 1, kWaitNs)) {
+                if (first && piece > 0 && !mbar_wait(smem_u32(&bars[kDrainedB]), (piece - 1) & 1, kWait)) {
                     ok = false; set_error(err, 1); break;
                 }
-                if (!mbar_wait(smem_u32(&bars[kReadyB + st]), (i / kS) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
+                if (!mbar_wait(smem_u32(&bars[kReadyB + st]), (i / kS) & 1, kWait)) { ok = false; set_error(err, 1); break; }
                 tc_fence_after();
                 const uint32_t bbase = smem_u32(smem + st * Cfg::kStage);
                 const uint32_t xbase = bbase + Cfg::kBBytes;
@@ -214,6 +287,7 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
                 mma_commit(smem_u32(&bars[kFreeB + st]));
                 if (last) { mma_commit(smem_u32(&bars[kDoneB])); ++piece; }
             }
+            retire_mmas(smem_u32(&bars[kRetireB]), err);
         }
         __syncwarp();
     } else {
@@ -270,7 +344,7 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
                 float lw[HG];                                       // log2 of w / dt, without this row's G
 #pragma unroll
                 for (int hh = 0; hh < HG; ++hh) lw[hh] = gl[hh * Cfg::kMaxR + kl];
-                if (ok && !mbar_wait(smem_u32(&bars[kFullB + st]), (i / kS) & 1, kWaitNs)) { ok = false; set_error(err, 1); }
+                if (ok && !mbar_wait(smem_u32(&bars[kFullB + st]), (i / kS) & 1, kWait)) { ok = false; set_error(err, 1); }
                 if (ok) {
                     if (staged) {
                         const float *side = (const float *)(smem + st * Cfg::kStage + Cfg::kBBytes + Cfg::kXBytes);
@@ -305,7 +379,7 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant_
             }
             // drain the piece: a whole unit is stored, a part of one is added
             const bool whole = p_begin % nq_u == 0 && p_end % nq_u == 0;
-            if (ok && !mbar_wait(smem_u32(&bars[kDoneB]), piece & 1, kWaitNs)) { ok = false; set_error(err, 1); }
+            if (ok && !mbar_wait(smem_u32(&bars[kDoneB]), piece & 1, kWait)) { ok = false; set_error(err, 1); }
             if (ok) {
                 tc_fence_after();
 #pragma unroll
@@ -390,13 +464,13 @@ struct ScanCfg {
 
 // kFull/kFree: the C and B tiles of a C/B stage; kIntra0/1: the Yi MMAs into Yi buffer 0/1
 // are done; kXFull: an x tile; kYSt: the y staged in an x slot has been read by its bulk
-// store (the slot may be reloaded).
+// store (the slot may be reloaded); kRetire: every MMA issued has completed.
 enum ScanBar {
     kFull0 = 0, kFree0 = 2, kCb = 4, kHReady, kXReady, kPReady, kIntra0, kIntra1, kUpdate, kEpi0, kEpi1,
-    kXFull0, kYSt0 = kXFull0 + 4, kNumScanBars = kYSt0 + 4
+    kXFull0, kYSt0 = kXFull0 + 4, kRetire = kYSt0 + 4, kNumScanBars
 };
 
-template <int S, bool kRagged>
+template <int S, bool kRagged, bool kExpire>
 __global__ void __launch_bounds__(448, 1)
 k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
@@ -407,6 +481,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
 {
     using Cfg = ScanCfg<S>;
     constexpr int kCBS = Cfg::kCBStages, kXS = Cfg::kXStages;
+    constexpr uint64_t kWait = kExpire ? 0ull : kRetireNs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float *sG = (float *)(smem + Cfg::kSmall);
@@ -468,11 +543,13 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             prefetch_tmap(&tmC);
             prefetch_tmap(&tmB);
             prefetch_tmap(&tmX);
+            int issued_cb = 0, issued_x = 0;
             for (int q = 0; q < nq && ok; ++q) {
                 const int t0 = (int)(t_begin + (int64_t)q * kQ);
                 // C and B tiles: free once the MMAs reading them (CB, Ys, state update) are done
+                // (those MMAs wait for the tiles: free implies landed)
                 const int cs = q % kCBS;
-                if (q >= kCBS && !mbar_wait(smem_u32(&bars[kFree0 + cs]), ((q / kCBS) - 1) & 1, kWaitNs)) {
+                if (q >= kCBS && !mbar_wait(smem_u32(&bars[kFree0 + cs]), ((q / kCBS) - 1) & 1, kWait)) {
                     ok = false; set_error(err, 1); break;
                 }
                 uint8_t *base = smem + cs * Cfg::kCBStage;
@@ -482,15 +559,19 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                     tma_load_4d(smem_u32(base + a * kAtom), &tmC, full, 64 * a, g, t0, b);
                     tma_load_4d(smem_u32(base + Cfg::kCBytes + a * kAtom), &tmB, full, 64 * a, g, t0, b);
                 }
+                ++issued_cb;
                 // x tile: its slot is free once the y staged there kXS sub-chunks ago is stored
                 const int xs = q % kXS;
-                if (q >= kXS && !mbar_wait(smem_u32(&bars[kYSt0 + xs]), ((q / kXS) - 1) & 1, kWaitNs)) {
+                if (q >= kXS && !mbar_wait(smem_u32(&bars[kYSt0 + xs]), ((q / kXS) - 1) & 1, kWait)) {
                     ok = false; set_error(err, 1); break;
                 }
                 const uint32_t xfull = smem_u32(&bars[kXFull0 + xs]);
                 mbar_arrive_expect_tx(xfull, kAtom);
                 tma_load_4d(smem_u32(smem + Cfg::kX + xs * kAtom), &tmX, xfull, pb * kPB, h, t0, b);
+                ++issued_x;
             }
+            retire_loads(bars, kFull0, kCBS, issued_cb, err);
+            retire_loads(bars, kXFull0, kXS, issued_x, err);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -520,7 +601,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             };
             do {
                 if (nq == 0) break;
-                if (!mbar_wait(smem_u32(&bars[kFull0]), 0, kWaitNs)) { ok = false; break; }
+                if (!mbar_wait(smem_u32(&bars[kFull0]), 0, kWait)) { ok = false; break; }
                 tc_fence_after();
                 issue_cb(0);
                 for (int q = 0; q < nq; ++q) {
@@ -530,7 +611,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                     const uint32_t yi = Cfg::kTyi + (uint32_t)(q & 1) * kPB;
                     // Ys = C h^T (K = s): needs the state copy and a drained Ys buffer; the state group
                     // arrives kHReady after both (one wait here instead of two)
-                    if (!mbar_wait(smem_u32(&bars[kHReady]), q & 1, kWaitNs)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&bars[kHReady]), q & 1, kWait)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < S / 16; ++kk) {
@@ -538,7 +619,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                         mma_bf16(tmem + ys, adv(dC0, off), adv(dH, kk * 2048), id_y, kk > 0 ? 1u : 0u);
                     }
                     // state update h^T += B^T (w o X) (K = t) on the state pre-scaled by the state group
-                    if (!mbar_wait(smem_u32(&bars[kXReady]), q & 1, kWaitNs)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&bars[kXReady]), q & 1, kWait)) { ok = false; break; }
                     tc_fence_after();
                     if (q + 1 < nq || write_final) {
 #pragma unroll
@@ -552,7 +633,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                     }
                     mma_commit(smem_u32(&bars[kFree0 + cs]));     // CB, Ys and the update have read C and B
                     // Yi = D x + P (dt o X) (K = j), P from TMEM: the state group stored D x in the accumulator
-                    if (!mbar_wait(smem_u32(&bars[kPReady]), q & 1, kWaitNs)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&bars[kPReady]), q & 1, kWait)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kQ / 16; ++kk)
@@ -564,7 +645,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                     // epilogue the output group runs after kPReady, so this thread waits for them.
                     if (q + 1 < nq) {
                         if (kCBS == 1) {
-                            if (!mbar_wait(smem_u32(&bars[kFull0]), (q + 1) & 1, kWaitNs)) { ok = false; break; }
+                            if (!mbar_wait(smem_u32(&bars[kFull0]), (q + 1) & 1, kWait)) { ok = false; break; }
                             tc_fence_after();
                         }
                         issue_cb(q + 1);
@@ -572,6 +653,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 }
             } while (0);
             if (!ok) set_error(err, 1);
+            retire_mmas(smem_u32(&bars[kRetire]), err);
         }
         __syncwarp();
     } else if (warp < 6) {
@@ -601,7 +683,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             {
                 const float dec = exp2f(glast - gbase);
                 if (q > 0) {
-                    if (!mbar_wait(smem_u32(&bars[kUpdate]), (q - 1) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
+                    if (!mbar_wait(smem_u32(&bars[kUpdate]), (q - 1) & 1, kWait)) { ok = false; set_error(err, 1); break; }
                     tc_fence_after();
                 }
 #pragma unroll
@@ -652,7 +734,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 // the epilogues arrive in order)
                 if (q >= Cfg::kYsBufs) {
                     const int e = q - Cfg::kYsBufs;
-                    if (!mbar_wait(smem_u32(&bars[kEpi0 + (e & 1)]), (e >> 1) & 1, kWaitNs)) {
+                    if (!mbar_wait(smem_u32(&bars[kEpi0 + (e & 1)]), (e >> 1) & 1, kWait)) {
                         ok = false; set_error(err, 1); break;
                     }
                 }
@@ -662,7 +744,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             // x tile: dt o x in place (Yi operand), w o x into the Xw tile (state-update operand),
             // and D x into this sub-chunk's Yi accumulator (the Yi MMAs accumulate on top of it)
             {
-                if (!mbar_wait(smem_u32(&bars[kXFull0 + xs]), (q / kXS) & 1, kWaitNs)) { ok = false; set_error(err, 1); break; }
+                if (!mbar_wait(smem_u32(&bars[kXFull0 + xs]), (q / kXS) & 1, kWait)) { ok = false; set_error(err, 1); break; }
                 // (the Yi buffer of this sub-chunk was drained before kHReady, above)
                 tc_fence_after();
                 uint8_t *xt = smem + Cfg::kX + xs * kAtom;
@@ -699,7 +781,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         }
         // final state of the sequence, from the last super-chunk of each (batch, head)
         if (ok && write_final && nq > 0) {
-            if (!mbar_wait(smem_u32(&bars[kUpdate]), (nq - 1) & 1, kWaitNs)) { ok = false; set_error(err, 1); }
+            if (!mbar_wait(smem_u32(&bars[kUpdate]), (nq - 1) & 1, kWait)) { ok = false; set_error(err, 1); }
             if (ok) {
                 tc_fence_after();
 #pragma unroll
@@ -760,7 +842,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                 // factored form 2^(G_i - G_e) 2^(G_e - G_j) (G_e = G at the block's last column; both
                 // factors <= 1); blocks that meet the diagonal evaluate 2^(G_i - G_j) per element.
                 // (the CB of qp is issued after the Yi of q, the last reader of the single P buffer)
-                if (ok && !mbar_wait(smem_u32(&bars[kCb]), qp & 1, kWaitNs)) { ok = false; set_error(err, 1); }
+                if (ok && !mbar_wait(smem_u32(&bars[kCb]), qp & 1, kWait)) { ok = false; set_error(err, 1); }
                 if (ok) {
                     tc_fence_after();
                     const int jh = 64 * half;
@@ -811,10 +893,10 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
                         tmem_st8(tp + 8 * blk, pk);
                     }
                     tmem_st_wait();
-                    // the MMA warp issues the next CB right after kPReady: one thread checks that its
+                    // the MMA warp issues the next CB right after kPReady: one warp checks that its
                     // C and B tiles have landed (the stage cannot be reloaded before this arrival)
-                    if (kCBS > 1 && storer && qp + 1 < nq &&
-                        !mbar_wait(smem_u32(&bars[kFull0 + (qp + 1) % kCBS]), ((qp + 1) / kCBS) & 1, kWaitNs)) {
+                    if (kCBS > 1 && warp == 6 && qp + 1 < nq &&
+                        !mbar_wait(smem_u32(&bars[kFull0 + (qp + 1) % kCBS]), ((qp + 1) / kCBS) & 1, kWait)) {
                         ok = false; set_error(err, 1);
                     }
                     tc_fence_before();
@@ -828,7 +910,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             const int xs = (q + kXS) % kXS;
             const float gr = gr_y, gbase = gbase_y;
             uint8_t *ystage = smem + Cfg::kX + xs * kAtom;
-            if (q >= 0 && ok && !mbar_wait(smem_u32(&bars[kIntra0 + (q & 1)]), (q >> 1) & 1, kWaitNs)) {
+            if (q >= 0 && ok && !mbar_wait(smem_u32(&bars[kIntra0 + (q & 1)]), (q >> 1) & 1, kWait)) {
                 ok = false; set_error(err, 1);
             }
             if (q >= 0 && ok) {
@@ -862,13 +944,13 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
             }
             // all rows staged (and the column arrays free for the next sub-chunk)
             group_sync();
-            if (storer && q >= 0) {
+            if (storer && q >= 0 && ok) {
                 // the store of sub-chunk q stays in flight; the slot of sub-chunk q - 1 is
-                // released once its store has read it
-                if (ok) {
-                    tma_store_4d(&tmY, smem_u32(ystage), pb * kPB, h, (int)t0, b);
-                    bulk_commit();
-                }
+                // released once its store has read it.  After an error no slot is released:
+                // its load may still be in flight, and the loader, whose wait then expires,
+                // must not re-arm it
+                tma_store_4d(&tmY, smem_u32(ystage), pb * kPB, h, (int)t0, b);
+                bulk_commit();
                 bulk_wait_read_1();
                 if (q > 0) mbar_arrive(smem_u32(&bars[kYSt0 + (q - 1) % kXS]));
             }
@@ -877,8 +959,625 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         }
         if (storer) {
             bulk_wait_all();
-            if (nq > 0) mbar_arrive(smem_u32(&bars[kYSt0 + (nq - 1) % kXS]));
+            if (nq > 0 && ok) mbar_arrive(smem_u32(&bars[kYSt0 + (nq - 1) % kXS]));
         }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
+}
+
+// ===========================================================================
+// chunk_scan on tensor cores, two heads of one B/C group per CTA (S = 128, H = 64).
+// Same arithmetic as k_chunk_scan_tc; the two heads share every C and B tile, one
+// C B^T product, and the N = 128 MMAs of the state product and the state update:
+//   CB        = C B^T                                   (M = i, N = j, K = s; shared)
+//   P_h[i][j] = CB[i][j] exp2(G_h,i - G_h,j) dt_h,j  if j <= i, else 0
+//             (built by the CUDA cores over CB in place: block k of 16 columns
+//              holds P_A of that block in its first 8 columns, P_B in the last 8)
+//   Y         = C [h_A^T | h_B^T]                       (M = i, N = 2 x 64 p, K = s)
+//   Y_h,i    <- exp2(G_h,i - G_h,base) Y_h,i              (CUDA cores, in TMEM)
+//   Y_h      += P_h x_h                                 (M = i, N = 64, K = j; A from TMEM)
+//   y_h       = Y_h + D_h x_h (bf16)
+//   [h_A^T | h_B^T] <- decayed state + B^T [w_A o x_A | w_B o x_B]   (M = s, N = 128, K = t)
+// Folding dt_j into P leaves the raw x tile as the B operand of P x, so the CUDA cores
+// write one scaled copy of x (w o x, for the update); the epilogue reads the raw tile
+// once more for D x.  The CUDA-core arithmetic runs on pairs (bf16x2 for w o x,
+// float32x2 elsewhere): it is the bulk of the issued instructions.  Scaling C h^T in place before P x
+// accumulates onto it lets one accumulator per sub-chunk hold y, so two of them fit in
+// TMEM and the next sub-chunk's C h^T never waits for this one's epilogue.
+// MMA issue order per sub-chunk: C h^T, update, P x, next CB.  The state chain (update ->
+// hand-off -> w o x -> update) waits on nothing else, and the C/B stage is free for the
+// next tiles once the update has read it.
+// TMEM (512 columns): CB / P 0..127, Y buffers 128..255 and 256..383 (sub-chunk q in
+// buffer q % 2; head A then head B), state 384..511 (h_A^T then h_B^T; lanes = s).
+// Shared memory: one C/B stage, x in a 3-slot ring (the slots also stage y for its bulk
+// stores), w o x, the bf16 state copy.
+// Warps: 0 loads C and B, 14 loads x, 1 issues MMAs, 2..5 hand the state over and write
+// w o x, 6..13 build P and scale C h^T (two warps per TMEM lane quarter, one per 64
+// columns / head), 15..18 write y and issue its bulk stores.
+// ===========================================================================
+struct PairCfg {
+    static constexpr int kXStages = 3;
+    static constexpr uint32_t kCBytes = 2 * kAtom;             // C tile [i][s], K-major (2 atoms of 64 s)
+    static constexpr uint32_t kCBStage = 4 * kAtom;            // C then B [j][s]
+    static constexpr uint32_t kX = kCBStage;                   // x ring: per slot [head][t][p]
+    static constexpr uint32_t kXSlot = 2 * kAtom;
+    static constexpr uint32_t kWx = kX + kXStages * kXSlot;    // w o x, [head][t][p]
+    static constexpr uint32_t kHc = kWx + 2 * kAtom;           // bf16 state copy, [head][s][p]
+    // per head, for the columns j of the sub-chunk being built: Gd_j = G_j - log2 dt_j,
+    // F_j = 2^(G_e - G_j) dt_j (G_e: G at the end of j's 16-column block) and the 8
+    // block-end values G_e
+    static constexpr uint32_t kArrHead = (2 * kQ + 8) * 4;
+    static constexpr uint32_t kArr = kHc + 2 * kAtom;
+    static constexpr uint32_t kBars = kArr + 2 * kArrHead;
+    static constexpr int kNumBars = 19;
+    static constexpr uint32_t kSmem = kBars + kNumBars * 8 + 8;
+    static constexpr uint32_t kTcb = 0, kTy = 128, kTst = 384, kTmemCols = 512;
+    static constexpr int kThreads = 608;
+    static_assert(kSmem <= 227 * 1024, "shared memory");
+};
+
+// pFull/pFree: the C/B stage (loaded / read by CB, the update and C h^T); pYs: C h^T of
+// the sub-chunk done; pIntra0/1: P x into Y buffer 0/1 done; pEpi0/1: Y buffer 0/1
+// drained; pXFull/pYSt: x slots (loaded / the y store has read the slot); pRetire: every
+// MMA issued has completed.  Every barrier a role waits on by parity is one its own
+// progress keeps within one phase of the wait.
+enum PairBar {
+    pFull = 0, pFree, pCb, pYs, pHReady, pXReady, pPReady, pIntra0, pIntra1, pUpdate, pEpi0, pEpi1,
+    pXFull0, pYSt0 = pXFull0 + 3, pRetire = pYSt0 + 3
+};
+static_assert(pRetire + 1 == PairCfg::kNumBars, "pair barriers");
+
+template <bool kRagged, bool kExpire>
+__global__ void __launch_bounds__(PairCfg::kThreads, 1)
+k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+                  const float *__restrict__ G, const __nv_bfloat16 *__restrict__ dt, const float *__restrict__ Dp,
+                  const float *__restrict__ h0, const float *__restrict__ h_start, float *__restrict__ h_final,
+                  Problem pr, ScanSplit sp, int *err)
+{
+    using Cfg = PairCfg;
+    constexpr int S = 128, kXS = Cfg::kXStages;
+    constexpr uint64_t kWait = kExpire ? 0ull : kRetireNs;
+    // the swizzled tiles need a 1024-byte aligned base; the whole budget is used, so the
+    // base is not re-aligned here: a misaligned base is reported and nothing runs
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {
+        if (threadIdx.x == 0) set_error(err, 4);
+        return;
+    }
+    uint64_t *bars = (uint64_t *)(smem + Cfg::kBars);
+    uint32_t *tmem_slot = (uint32_t *)(bars + Cfg::kNumBars);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // CTA -> (part, super-chunk m, head pair), pairs fastest
+    const int64_t nseq_all = pr.B * pr.nh;
+    const int units0 = (int)(sp.split / 2) * sp.nsup0;
+    const bool part1 = (int)blockIdx.x >= units0;
+    const int u = part1 ? (int)blockIdx.x - units0 : (int)blockIdx.x;
+    const int seq_lo = part1 ? (int)sp.split : 0;
+    const int npair = part1 ? (int)((nseq_all - sp.split) / 2) : (int)(sp.split / 2);
+    const int nsup = part1 ? sp.nsup1 : sp.nsup0, R = part1 ? sp.R1 : sp.R0;
+    const int bhA = seq_lo + 2 * (u % npair);
+    const int m = u / npair;
+    const int b = bhA / (int)pr.nh, hA = bhA % (int)pr.nh;
+    const int g = (int)(hA / pr.hpg);
+    const int k_begin = m * R;
+    const int k_end = min((int)pr.nc, k_begin + R);
+    const int qpc = (int)(pr.T / kQ);
+    // sub-chunks of this super-chunk that hold tokens (the last chunk of a sequence may be short;
+    // its tokens past L are zero-filled by TMA, hold the state (dt = 0) and are not stored)
+    const int nq = kRagged ? (int)((min(pr.L, (int64_t)k_end * pr.T) - (int64_t)k_begin * pr.T + kQ - 1) / kQ)
+                           : (k_end - k_begin) * qpc;
+    const int64_t t_begin = (int64_t)k_begin * pr.T;
+    const float *GA = G + (int64_t)bhA * pr.L, *GB = GA + pr.L;
+    const bool write_final = (m == nsup - 1) && h_final;
+    const int64_t hs_idx = (part1 ? sp.base1 : 0) + (int64_t)(bhA - seq_lo) * nsup + m;   // head A; head B: + nsup
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Cfg::kNumBars; ++i) {
+            uint32_t cnt = 1;
+            if (i == pHReady || i == pXReady) cnt = 128;
+            if (i == pEpi0 || i == pEpi1) cnt = 128;
+            if (i == pPReady) cnt = 256;
+            mbar_init(smem_u32(&bars[i]), cnt);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+    // the next kernel may launch now; this one reads G (and the states) of the kernels before
+    pdl_trigger();
+    pdl_wait();
+
+    if (warp == 0) {
+        // ---- C and B tiles (one stage: free once CB, the update and C h^T have read it) -------
+        if (lane == 0) {
+            prefetch_tmap(&tmC);
+            prefetch_tmap(&tmB);
+            int issued = 0;
+            for (int q = 0; q < nq; ++q) {
+                const int t0 = (int)(t_begin + (int64_t)q * kQ);
+                // (the MMAs that free the stage wait for its load: free implies landed)
+                if (q >= 1 && !mbar_wait(smem_u32(&bars[pFree]), (q - 1) & 1, kWait)) {
+                    set_error(err, 1); break;
+                }
+                const uint32_t full = smem_u32(&bars[pFull]);
+                mbar_arrive_expect_tx(full, Cfg::kCBStage);
+                for (int a = 0; a < 2; ++a) {
+                    tma_load_4d(smem_u32(smem + a * kAtom), &tmC, full, 64 * a, g, t0, b);
+                    tma_load_4d(smem_u32(smem + Cfg::kCBytes + a * kAtom), &tmB, full, 64 * a, g, t0, b);
+                }
+                // the tiles two sub-chunks ahead into L2: the single stage reloads right after the
+                // update and C h^T have read it, so its load latency is on the critical path
+                if (q + 2 < nq) {
+                    for (int a = 0; a < 2; ++a) {
+                        tma_prefetch_4d(&tmC, 64 * a, g, t0 + 2 * kQ, b);
+                        tma_prefetch_4d(&tmB, 64 * a, g, t0 + 2 * kQ, b);
+                    }
+                }
+                ++issued;
+            }
+            retire_loads(bars, pFull, 1, issued, err);
+        }
+        __syncwarp();
+    } else if (warp == 14) {
+        // ---- x tiles of both heads (slot of sub-chunk q: free once y of q - 3 is stored) ------
+        if (lane == 0) {
+            // the entering states of both heads into L2 first: the first hand-off reads them
+            // with strided loads, one head after the other
+            for (int hh = 0; hh < 2; ++hh) {
+                const float *src = (m < sp.hs_from) ? (h0 ? h0 + (int64_t)(bhA + hh) * (pr.H * S) : nullptr)
+                                                    : h_start + (hs_idx + hh * nsup) * (int64_t)(pr.H * S);
+                // (h0 need only be 4-byte aligned; a bulk prefetch needs 16)
+                if (src && nq > 0 && ((uintptr_t)src & 15u) == 0)
+                    bulk_prefetch_l2(src, (uint32_t)(pr.H * S * sizeof(float)));
+            }
+            prefetch_tmap(&tmX);
+            int issued = 0;
+            for (int q = 0; q < nq; ++q) {
+                const int t0 = (int)(t_begin + (int64_t)q * kQ);
+                const int xs = q % kXS;
+                if (q >= kXS && !mbar_wait(smem_u32(&bars[pYSt0 + xs]), ((q / kXS) - 1) & 1, kWait)) {
+                    set_error(err, 1); break;
+                }
+                const uint32_t xfull = smem_u32(&bars[pXFull0 + xs]);
+                mbar_arrive_expect_tx(xfull, Cfg::kXSlot);
+                for (int hh = 0; hh < 2; ++hh)
+                    tma_load_4d(smem_u32(smem + Cfg::kX + xs * Cfg::kXSlot + hh * kAtom), &tmX, xfull, 0, hA + hh,
+                                t0, b);
+                ++issued;
+            }
+            retire_loads(bars, pXFull0, kXS, issued, err);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA issuer -----------------------------------------------------------------
+        if (lane == 0) {
+            constexpr uint32_t id_cb = idesc_bf16_f32(128, 128, 0, 0);
+            constexpr uint32_t id_ys = idesc_bf16_f32(128, 128, 0, 1);
+            constexpr uint32_t id_up = idesc_bf16_f32(128, 128, 1, 1);
+            constexpr uint32_t id_yi = idesc_bf16_f32(128, 64, 0, 1);
+            auto adv = [](uint64_t d, uint32_t bytes) -> uint64_t { return d + (uint64_t)(bytes >> 4); };
+            const uint32_t s0 = smem_u32(smem);
+            const uint64_t dC = smem_desc(s0, 16, 1024);                        // C [i][s], K-major
+            const uint64_t dBk = smem_desc(s0 + Cfg::kCBytes, 16, 1024);        // B [j][s], K-major
+            const uint64_t dBm = smem_desc(s0 + Cfg::kCBytes, kAtom, 1024);     // B^T [s][t], MN-major
+            const uint64_t dX = smem_desc(s0 + Cfg::kX, kAtom, 1024);           // x [t][p], MN-major
+            const uint64_t dHc = smem_desc(s0 + Cfg::kHc, kAtom, 1024);         // h bf16 [s][p], 2 atoms along N
+            const uint64_t dWx = smem_desc(s0 + Cfg::kWx, kAtom, 1024);         // w o x [t][p], 2 atoms along N
+            auto issue_cb = [&]() {
+#pragma unroll
+                for (int kk = 0; kk < S / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+                    mma_bf16(tmem + Cfg::kTcb, adv(dC, off), adv(dBk, off), id_cb, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&bars[pCb]));
+            };
+            do {
+                if (nq == 0) break;
+                if (!mbar_wait(smem_u32(&bars[pFull]), 0, kWait)) { ok = false; break; }
+                tc_fence_after();
+                issue_cb();
+                for (int q = 0; q < nq; ++q) {
+                    const int xs = q % kXS;
+                    const uint32_t ty = tmem + Cfg::kTy + (uint32_t)(q & 1) * 128;
+                    // C [h_A^T | h_B^T] into Y buffer q % 2 (drained by the epilogue of q - 2), from the
+                    // bf16 state copy of the hand-off
+                    if (!mbar_wait(smem_u32(&bars[pHReady]), q & 1, kWait) ||
+                        (q >= 2 && !mbar_wait(smem_u32(&bars[pEpi0 + (q & 1)]), ((q - 2) >> 1) & 1, kWait))) {
+                        ok = false; break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < S / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+                        mma_bf16(ty, adv(dC, off), adv(dHc, kk * 2048), id_ys, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&bars[pYs]));
+                    // update on the state the state warps decayed, with their w o x
+                    if (!mbar_wait(smem_u32(&bars[pXReady]), q & 1, kWait)) { ok = false; break; }
+                    tc_fence_after();
+                    if (q + 1 < nq || write_final) {
+#pragma unroll
+                        for (int kk = 0; kk < kQ / 16; ++kk)
+                            mma_bf16(tmem + Cfg::kTst, adv(dBm, kk * 2048), adv(dWx, kk * 2048), id_up, 1u);
+                        mma_commit(smem_u32(&bars[pUpdate]));
+                    }
+                    mma_commit(smem_u32(&bars[pFree]));      // CB, C h^T and the update have read C and B
+                    // Y_h += P_h x_h (P from TMEM) once P is built and C h^T scaled
+                    if (!mbar_wait(smem_u32(&bars[pPReady]), q & 1, kWait)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                        for (int kk = 0; kk < kQ / 16; ++kk)
+                            mma_bf16_ts(ty + 64 * hh, tmem + Cfg::kTcb + 16 * kk + 8 * hh,
+                                        adv(dX, xs * Cfg::kXSlot + hh * kAtom + kk * 2048), id_yi, 1u);
+                    }
+                    mma_commit(smem_u32(&bars[pIntra0 + (q & 1)]));
+                    // next CB over the P just read (in issue order)
+                    if (q + 1 < nq) {
+                        if (!mbar_wait(smem_u32(&bars[pFull]), (q + 1) & 1, kWait)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_cb();
+                    }
+                }
+            } while (0);
+            if (!ok) set_error(err, 1);
+            retire_mmas(smem_u32(&bars[pRetire]), err);
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ---- state warps: state hand-off and w o x ----------------------------------------
+        const int r = 32 * (warp & 3) + lane;          // TMEM lane = state row s / token row t
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        uint8_t *wx = smem + Cfg::kWx;
+        uint8_t *hc = smem + Cfg::kHc;
+        float n_g[2] = {0.f, 0.f}, n_gl[2] = {0.f, 0.f}, n_gb[2] = {0.f, 0.f};
+        uint32_t n_dt = 0;
+        auto load_scalars = [&](int q) {
+            const int64_t t0 = t_begin + (int64_t)q * kQ;
+            const int64_t tr = clamp_t<kRagged>(t0 + r, pr.L), tl = clamp_t<kRagged>(t0 + kQ - 1, pr.L);
+            n_g[0] = GA[tr];
+            n_g[1] = GB[tr];
+            n_gl[0] = GA[tl];
+            n_gl[1] = GB[tl];
+            const bool cs = q % qpc == 0;
+            n_gb[0] = cs ? 0.f : GA[t0 - 1];
+            n_gb[1] = cs ? 0.f : GB[t0 - 1];
+            n_dt = in_seq<kRagged>(t0 + r, pr.L)
+                       ? *reinterpret_cast<const uint32_t *>(dt + ((int64_t)b * pr.L + t0 + r) * pr.nh + hA)
+                       : 0u;
+        };
+        if (nq > 0) load_scalars(0);
+        for (int q = 0; q < nq && ok; ++q) {
+            const int xs = q % kXS;
+            const float g0 = n_g[0], g1 = n_g[1], gl0 = n_gl[0], gl1 = n_gl[1], gb0 = n_gb[0], gb1 = n_gb[1];
+            const float2 dtp = unpack_bf16x2(n_dt);
+            if (q + 1 < nq) load_scalars(q + 1);
+            // the update of q - 1 has produced the state and read w o x (and C h^T of q - 1,
+            // issued before it, has read the bf16 copy)
+            if (q > 0) {
+                if (!mbar_wait(smem_u32(&bars[pUpdate]), (q - 1) & 1, kWait)) {
+                    ok = false; set_error(err, 1); break;
+                }
+                tc_fence_after();
+            }
+            // state (float32, TMEM) -> bf16 copy [s][p] for C h^T, and the state times
+            // 2^(G_last - G_base) back to TMEM for the update to accumulate on
+#pragma unroll 1
+            for (int hc32 = 0; hc32 < 4; ++hc32) {             // head hc32 / 2, columns 32 (hc32 % 2) ..
+                const int hh = hc32 >> 1, c32 = 32 * (hc32 & 1);
+                const float dec = exp2f(hh ? gl1 - gb1 : gl0 - gb0);
+                const uint32_t ta = tmem + lane_base + Cfg::kTst + 64 * hh + c32;
+                uint32_t v[32];
+                if (q == 0) {
+                    // entering state: h0 (zeros if absent) for super-chunks m < hs_from, else h_start
+                    const float *src = (m < sp.hs_from)
+                                           ? (h0 ? h0 + (int64_t)(bhA + hh) * (pr.H * S) : nullptr)
+                                           : h_start + (hs_idx + hh * nsup) * (int64_t)(pr.H * S);
+                    if (src) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(src[(int64_t)(c32 + j) * S + r]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = 0u;
+                    }
+                } else {
+                    tmem_ld16(ta + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_ld_wait();
+                }
+                uint8_t *hrow = hc + hh * kAtom;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 o;
+                    o.x = pack_bf16x2(__uint_as_float(v[8 * c + 0]), __uint_as_float(v[8 * c + 1]));
+                    o.y = pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3]));
+                    o.z = pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5]));
+                    o.w = pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7]));
+                    *(uint4 *)(hrow + sw128(r, (c32 >> 3) + c)) = o;
+                }
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const float2 d2 = __fmul2_rn(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
+                                                 make_float2(dec, dec));
+                    v[j] = __float_as_uint(d2.x);
+                    v[j + 1] = __float_as_uint(d2.y);
+                }
+                tmem_st16(ta + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                tmem_st16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars[pHReady]));
+
+            // x row r of both heads: w o x into the Wx tile (the update of q - 1 has read it)
+            if (!mbar_wait(smem_u32(&bars[pXFull0 + xs]), (q / kXS) & 1, kWait)) { ok = false; set_error(err, 1); break; }
+            // w_t rounded to bf16 and the product taken in bf16 pairs (the product is an MMA
+            // operand, rounded to bf16 either way)
+            const float w0 = dtp.x * exp2f(gl0 - g0), w1 = dtp.y * exp2f(gl1 - g1);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint8_t *xt = smem + Cfg::kX + xs * Cfg::kXSlot + hh * kAtom;
+                uint8_t *wt = wx + hh * kAtom;
+                const __nv_bfloat162 w2 = __float2bfloat162_rn(hh ? w1 : w0);
+                uint4 vx[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) vx[c] = *(const uint4 *)(xt + sw128(r, c));
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 o;
+                    o.x = mul_bf16x2(vx[c].x, w2);
+                    o.y = mul_bf16x2(vx[c].y, w2);
+                    o.z = mul_bf16x2(vx[c].z, w2);
+                    o.w = mul_bf16x2(vx[c].w, w2);
+                    *(uint4 *)(wt + sw128(r, c)) = o;
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&bars[pXReady]));
+        }
+        // final state of the sequence, from the last super-chunk of each (batch, head)
+        if (ok && write_final && nq > 0) {
+            if (!mbar_wait(smem_u32(&bars[pUpdate]), (nq - 1) & 1, kWait)) { ok = false; set_error(err, 1); }
+            if (ok) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    float *dst = h_final + (int64_t)(bhA + hh) * (pr.H * S) + r;
+#pragma unroll
+                    for (int c0 = 0; c0 < 64; c0 += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem + lane_base + Cfg::kTst + 64 * hh + c0, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) dst[(int64_t)(c0 + j) * S] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+        }
+    } else if (warp < 14) {
+        // ---- P warps: P and the scaled C h^T of sub-chunk q ------------------------------------
+        const int half = (warp - 6) >> 2;              // columns 64 half .. 64 half + 63; C h^T of head `half`
+        const int r = 32 * (warp & 3) + lane;          // TMEM lane = token row i
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        float *arr = (float *)(smem + Cfg::kArr);
+        float *myGd = arr + half * (Cfg::kArrHead / 4);  // the arrays this thread fills (head `half`)
+        float *myF = myGd + kQ, *myGe = myF + kQ;
+        auto group_sync = [&]() { named_bar_sync(1, 256); };
+        // per sub-chunk scalars, loaded one ahead: G of row r for both heads, G_base of head
+        // `half`, and for head `half`: dt of row r and G at the end of r's 16-token block
+        float n_g[2] = {0.f, 0.f}, n_gb = 0.f, n_gend = 0.f, n_dt = 0.f;
+        auto load_scalars = [&](int q) {
+            const int64_t t0 = t_begin + (int64_t)q * kQ;
+            const int64_t tr = clamp_t<kRagged>(t0 + r, pr.L);
+            n_g[0] = GA[tr];
+            n_g[1] = GB[tr];
+            const float *Gh = half ? GB : GA;
+            n_gb = (q % qpc == 0) ? 0.f : Gh[t0 - 1];
+            n_gend = Gh[clamp_t<kRagged>(t0 + (r | 15), pr.L)];
+            n_dt = in_seq<kRagged>(t0 + r, pr.L) ? __bfloat162float(dt[((int64_t)b * pr.L + t0 + r) * pr.nh + hA + half])
+                                                 : 0.f;
+        };
+        if (nq > 0) load_scalars(0);
+        for (int q = 0; q < nq; ++q) {
+            // every thread is past P of q - 1 (the arrays are free)
+            group_sync();
+            const float g0 = n_g[0], g1 = n_g[1], gbase = n_gb;
+            {
+                const float gr = half ? g1 : g0;
+                myGd[r] = gr - __log2f(n_dt);                     // dt = 0: +inf, so 2^(G_i - Gd_j) = 0
+                myF[r] = ex2_approx(n_gend - gr) * n_dt;          // 2^(G_e - G_j) <= 1 for A dt <= 0
+                if ((r & 15) == 15) myGe[r >> 4] = gr;
+            }
+            if (q + 1 < nq) load_scalars(q + 1);
+            group_sync();
+            if (ok && !mbar_wait(smem_u32(&bars[pCb]), q & 1, kWait)) { ok = false; set_error(err, 1); }
+            if (ok) {
+                tc_fence_after();
+                const uint32_t tcb = tmem + lane_base + Cfg::kTcb;
+                const float *GdA = arr, *FA = arr + kQ, *GeA = arr + 2 * kQ;
+                const float *GdB = GdA + Cfg::kArrHead / 4, *FB = FA + Cfg::kArrHead / 4, *GeB = GeA + Cfg::kArrHead / 4;
+                // The four 16-column blocks of this half come in two pairs of the same kind
+                // (above the diagonal, left of every row of the warp, or meeting the diagonal).
+                // Per pair: both blocks' C B^T loaded, one wait, then P_A of each block into its
+                // first 8 columns and P_B into its last 8.
+                const int wrow_lo = 32 * (warp & 3), wrow_hi = wrow_lo + 31;
+#pragma unroll 1
+                for (int bp = 0; bp < 2; ++bp) {
+                    const int j0 = 64 * half + 32 * bp;
+                    if (j0 > wrow_hi) {                            // above the diagonal for the whole warp
+                        uint32_t z[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) z[e] = 0u;
+                        tmem_st16(tcb + j0, z);
+                        tmem_st16(tcb + j0 + 16, z);
+                        continue;
+                    }
+                    uint32_t v[32];
+                    tmem_ld16(tcb + j0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(tcb + j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_ld_wait();
+                    if (j0 + 31 < wrow_lo) {                       // left of every row of the warp: factored
+#pragma unroll
+                        for (int k2 = 0; k2 < 2; ++k2) {
+                            const int jb = j0 + 16 * k2;
+                            uint32_t pk[16];
+                            const float eA = ex2_approx(g0 - GeA[jb >> 4]);
+                            const float eB = ex2_approx(g1 - GeB[jb >> 4]);
+                            const float4 *fa = reinterpret_cast<const float4 *>(FA + jb);
+                            const float4 *fb = reinterpret_cast<const float4 *>(FB + jb);
+#pragma unroll
+                            for (int e4 = 0; e4 < 4; ++e4) {
+                                const float4 a = fa[e4], c = fb[e4];
+                                const float2 v01 = make_float2(__uint_as_float(v[16 * k2 + 4 * e4 + 0]),
+                                                               __uint_as_float(v[16 * k2 + 4 * e4 + 1]));
+                                const float2 v23 = make_float2(__uint_as_float(v[16 * k2 + 4 * e4 + 2]),
+                                                               __uint_as_float(v[16 * k2 + 4 * e4 + 3]));
+                                const float2 pA01 = __fmul2_rn(__fmul2_rn(v01, make_float2(eA, eA)), make_float2(a.x, a.y));
+                                const float2 pA23 = __fmul2_rn(__fmul2_rn(v23, make_float2(eA, eA)), make_float2(a.z, a.w));
+                                const float2 pB01 = __fmul2_rn(__fmul2_rn(v01, make_float2(eB, eB)), make_float2(c.x, c.y));
+                                const float2 pB23 = __fmul2_rn(__fmul2_rn(v23, make_float2(eB, eB)), make_float2(c.z, c.w));
+                                pk[2 * e4] = pack_bf16x2(pA01.x, pA01.y);
+                                pk[2 * e4 + 1] = pack_bf16x2(pA23.x, pA23.y);
+                                pk[8 + 2 * e4] = pack_bf16x2(pB01.x, pB01.y);
+                                pk[8 + 2 * e4 + 1] = pack_bf16x2(pB23.x, pB23.y);
+                            }
+                            tmem_st16(tcb + jb, pk);
+                        }
+                    } else {                                       // meets the diagonal: exact, selected
+#pragma unroll
+                        for (int k2 = 0; k2 < 2; ++k2) {
+                            const int jb = j0 + 16 * k2;
+                            uint32_t pk[16];
+                            const float4 *da = reinterpret_cast<const float4 *>(GdA + jb);
+                            const float4 *db = reinterpret_cast<const float4 *>(GdB + jb);
+#pragma unroll
+                            for (int e4 = 0; e4 < 4; ++e4) {
+                                const float4 a = da[e4], c = db[e4];
+                                const float ga[4] = {a.x, a.y, a.z, a.w}, gb[4] = {c.x, c.y, c.z, c.w};
+                                float pa[4], pb[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int j = jb + 4 * e4 + e;
+                                    const float vv = __uint_as_float(v[16 * k2 + 4 * e4 + e]);
+                                    const float xa = vv * ex2_approx(g0 - ga[e]);
+                                    const float xb = vv * ex2_approx(g1 - gb[e]);
+                                    pa[e] = (j <= r) ? xa : 0.f;
+                                    pb[e] = (j <= r) ? xb : 0.f;
+                                }
+                                pk[2 * e4] = pack_bf16x2(pa[0], pa[1]);
+                                pk[2 * e4 + 1] = pack_bf16x2(pa[2], pa[3]);
+                                pk[8 + 2 * e4] = pack_bf16x2(pb[0], pb[1]);
+                                pk[8 + 2 * e4 + 1] = pack_bf16x2(pb[2], pb[3]);
+                            }
+                            tmem_st16(tcb + jb, pk);
+                        }
+                    }
+                }
+                // C h^T of head `half`, row r: Y <- 2^(G_i - G_base) Y before P x accumulates onto it
+                if (!mbar_wait(smem_u32(&bars[pYs]), q & 1, kWait)) { ok = false; set_error(err, 1); }
+                if (ok) {
+                    tc_fence_after();
+                    const float eg = ex2_approx((half ? g1 : g0) - gbase);
+                    const uint32_t ty = tmem + lane_base + Cfg::kTy + (uint32_t)(q & 1) * 128 + 64 * half;
+#pragma unroll 1
+                    for (int c32 = 0; c32 < 64; c32 += 32) {
+                        uint32_t v[32];
+                        tmem_ld16(ty + c32, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                        tmem_ld16(ty + c32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            const float2 s2 = __fmul2_rn(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
+                                                         make_float2(eg, eg));
+                            v[j] = __float_as_uint(s2.x);
+                            v[j + 1] = __float_as_uint(s2.y);
+                        }
+                        tmem_st16(ty + c32, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                        tmem_st16(ty + c32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars[pPReady]));
+            }
+        }
+    } else if (warp >= 15) {
+        // ---- epilogue warps: y = Y + D x of sub-chunk q, staged over its x tile --------------
+        const int r = 32 * (warp & 3) + lane;          // TMEM lane = token row i
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const bool storer = warp == 15 && lane == 0;
+        const float dA = Dp[hA], dB = Dp[hA + 1];
+        for (int q = 0; q < nq; ++q) {
+            const int xs = q % kXS;
+            uint8_t *ystage = smem + Cfg::kX + xs * Cfg::kXSlot;
+            if (ok && !mbar_wait(smem_u32(&bars[pIntra0 + (q & 1)]), (q >> 1) & 1, kWait)) {
+                ok = false; set_error(err, 1);
+            }
+            if (ok) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint32_t ty = tmem + lane_base + Cfg::kTy + (uint32_t)(q & 1) * 128 + 64 * hh;
+                    uint8_t *yrow = ystage + hh * kAtom;
+                    const float dh = hh ? dB : dA;
+                    // the x row this y then overwrites (same thread, same row)
+#pragma unroll 1
+                    for (int c32 = 0; c32 < 64; c32 += 32) {
+                        uint32_t v[32];
+                        tmem_ld16(ty + c32, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                        tmem_ld16(ty + c32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                        uint4 xv[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) xv[c] = *(const uint4 *)(yrow + sw128(r, (c32 >> 3) + c));
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t in[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 yv = __ffma2_rn(unpack_bf16x2(in[e]), make_float2(dh, dh),
+                                                             make_float2(__uint_as_float(v[8 * c + 2 * e]),
+                                                                         __uint_as_float(v[8 * c + 2 * e + 1])));
+                                o[e] = pack_bf16x2(yv.x, yv.y);
+                            }
+                            *(uint4 *)(yrow + sw128(r, (c32 >> 3) + c)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars[pEpi0 + (q & 1)]));
+                fence_proxy_async_smem();
+            }
+            // all rows staged (every epilogue thread reaches this, errors or not)
+            named_bar_sync(2, 128);
+            if (storer) {
+                // the slot goes back to the x loader as soon as the store has read it (the x load
+                // for three sub-chunks ahead then has a whole period to land).  After an error
+                // the slot is not released: its load may still be in flight, and the loader,
+                // whose wait then expires, must not re-arm it
+                if (ok) {
+                    const int t0 = (int)(t_begin + (int64_t)q * kQ);
+                    tma_store_4d(&tmY, smem_u32(ystage), 0, hA, t0, b);
+                    tma_store_4d(&tmY, smem_u32(ystage + kAtom), 0, hA + 1, t0, b);
+                    bulk_commit();
+                    bulk_wait_read();
+                    mbar_arrive(smem_u32(&bars[pYSt0 + xs]));
+                }
+            }
+            __syncwarp();
+        }
+        if (storer) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -887,8 +1586,33 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
 
 // ---- host side ---------------------------------------------------------------------
 
-using tc::current_sms;
-using tc::make_map_4d;
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    });
+    return fn;
+}
+
+// 4-D bf16 tensor [d3][d2][d1][d0] (d0 contiguous), box {64, 1, rows, 1}, 128-byte swizzle.
+bool make_map_4d(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3, uint32_t rows)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {d0, d1, d2, d3};
+    cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+    cuuint32_t box[4] = {64, 1, rows, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // Whether cutting `total` stages into `grid` equal slices puts a cut inside a unit of
 // `nq_u` stages.
@@ -897,6 +1621,14 @@ bool slices_split_units(int64_t total, int64_t grid, int64_t nq_u)
     for (int64_t c = 1; c < grid; ++c)
         if ((total * c / grid) % nq_u != 0) return true;
     return false;
+}
+
+int current_sms()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    return sms > 0 ? sms : 1;
 }
 
 // chunk_state CTAs for `total` stages in units of nq_u.  With enough work, one CTA per
@@ -930,7 +1662,7 @@ cudaError_t state_launch(const Problem &pr, SeqRange seqs, const void *x, const 
     CUtensorMap mB, mX;
     if (!make_map_4d(&mB, Bm, pr.S, pr.G, pr.L, pr.B, Cfg::kTok) || !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, Cfg::kTok))
         return cudaErrorInvalidValue;
-    auto kern = k_chunk_state_tc<S, H, HG>;
+    auto kern = pr.wait_ns ? k_chunk_state_tc<S, H, HG, false> : k_chunk_state_tc<S, H, HG, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t grid = state_grid(total, nq_u);
@@ -953,7 +1685,8 @@ cudaError_t scan_launch(const Problem &pr, const void *x, const void *dt, const 
         !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, kQ) || !make_map_4d(&mY, y, pr.H, pr.nh, pr.L, pr.B, kQ))
         return cudaErrorInvalidValue;
     using Cfg = ScanCfg<S>;
-    auto kern = pr.L % pr.T == 0 ? k_chunk_scan_tc<S, false> : k_chunk_scan_tc<S, true>;
+    auto kern = pr.L % pr.T == 0 ? (pr.wait_ns ? k_chunk_scan_tc<S, false, false> : k_chunk_scan_tc<S, false, true>)
+                                 : (pr.wait_ns ? k_chunk_scan_tc<S, true, false> : k_chunk_scan_tc<S, true, true>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t grid = (sp.split * sp.nsup0 + (pr.B * pr.nh - sp.split) * sp.nsup1) * (pr.H / kPB);
@@ -963,10 +1696,30 @@ cudaError_t scan_launch(const Problem &pr, const void *x, const void *dt, const 
                       (const __nv_bfloat16 *)dt, D, h0, h_start, h_final, (__nv_bfloat16 *)y, pr, sp, err);
 }
 
+cudaError_t scan_pair_launch(const Problem &pr, const void *x, const void *dt, const void *Bm, const void *Cm,
+                             const float *D, const float *G, const float *h0, const float *h_start, float *h_final,
+                             void *y, const ScanSplit &sp, int *err, cudaStream_t st)
+{
+    // head pairs: the run [0, split) and the rest hold whole pairs
+    if ((sp.split & 1) || ((pr.B * pr.nh - sp.split) & 1)) return cudaErrorInvalidValue;
+    CUtensorMap mC, mB, mX, mY;
+    if (!make_map_4d(&mC, Cm, pr.S, pr.G, pr.L, pr.B, kQ) || !make_map_4d(&mB, Bm, pr.S, pr.G, pr.L, pr.B, kQ) ||
+        !make_map_4d(&mX, x, pr.H, pr.nh, pr.L, pr.B, kQ) || !make_map_4d(&mY, y, pr.H, pr.nh, pr.L, pr.B, kQ))
+        return cudaErrorInvalidValue;
+    auto kern = pr.L % pr.T == 0 ? (pr.wait_ns ? k_chunk_scan_pair<false, false> : k_chunk_scan_pair<false, true>)
+                                 : (pr.wait_ns ? k_chunk_scan_pair<true, false> : k_chunk_scan_pair<true, true>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)PairCfg::kSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = (sp.split / 2) * sp.nsup0 + ((pr.B * pr.nh - sp.split) / 2) * sp.nsup1;
+    if (grid == 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(PairCfg::kThreads), PairCfg::kSmem, st, mC, mB,
+                      mX, mY, G, (const __nv_bfloat16 *)dt, D, h0, h_start, h_final, pr, sp, err);
+}
+
 }  // namespace
 
-// 2 when the fused kernel (ssd_fused.cu, two heads of one group per work item) takes the
-// shape: S = 128, H = 64 and an even number of heads per group.
 int scan_seqs_per_cta(const Problem &pr)
 {
     return (pr.S == 128 && pr.H == 64 && pr.hpg % 2 == 0) ? 2 : 1;
@@ -1040,6 +1793,8 @@ cudaError_t launch_chunk_scan_tc(const Problem &pr, const void *x, const void *d
                                  const float *D, const float *G, const float *h0, const float *h_start, float *h_final,
                                  void *y, const ScanSplit &sp, int *err, cudaStream_t st)
 {
+    if (scan_seqs_per_cta(pr) == 2)
+        return scan_pair_launch(pr, x, dt, Bm, Cm, D, G, h0, h_start, h_final, y, sp, err, st);
     if (pr.S == 128) return scan_launch<128>(pr, x, dt, Bm, Cm, D, G, h0, h_start, h_final, y, sp, err, st);
     if (pr.S == 256) return scan_launch<256>(pr, x, dt, Bm, Cm, D, G, h0, h_start, h_final, y, sp, err, st);
     return cudaErrorNotSupported;

@@ -2,7 +2,6 @@
 // and chunk_scan stages, for the shapes they are specialised for.
 #pragma once
 
-#include "fused_plan.cuh"
 #include "ssd_common.cuh"
 
 namespace ssd {
@@ -48,28 +47,5 @@ cudaError_t launch_chunk_scan_tc(const Problem &pr, const void *x, const void *d
                                  const void *Cm, const float *D, const float *G, const float *h0,
                                  const float *h_start, float *h_final, void *y, const ScanSplit &sp,
                                  int *err, cudaStream_t st);
-
-// ---- the fused forward kernel (ssd_fused.cu): S = 128, H = 64, heads in pairs of one group ----
-// Workspace of one call: hdr[0] the error word, hdr[1] the ticket counter; cnt[2 * npair] the
-// finished STATE items and the finished PASS items of each pair (hdr and cnt zeroed by the
-// caller before the launch); sdec: the log2 decay of each cut super-chunk; s_local: the state
-// each cut super-chunk produces from zero; h_start: the state entering each super-chunk.  The
-// state arrays are indexed by FusedItem::slot (head B: slot + nsup).
-struct FusedWork {
-    int *hdr;
-    int *cnt;
-    float *sdec;
-    float *s_local;
-    float *h_start;
-};
-
-// PASS slices per cut pair (the plan's nslice).
-int fused_pass_slices();
-
-// One launch of the fused kernel over the work list of `pl`.  wait_ns bounds every wait of a
-// kernel role on another (on expiry the error word gets a bit and the kernel winds down).
-cudaError_t launch_fused_pair(const Problem &pr, const void *x, const void *dt, const float *A, const void *Bm,
-                              const void *Cm, const float *D, const float *h0, float *h_final, void *y,
-                              const FusedPlan &pl, const FusedWork &w, unsigned long long wait_ns, cudaStream_t st);
 
 }  // namespace ssd

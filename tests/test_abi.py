@@ -132,39 +132,30 @@ def test_step_and_stage_validation(lib):
 def test_fwd_plan_is_consistent(lib):
     """ssd_fwd_plan: host-side query; the plan must be self-consistent for every path."""
     P = _native.Plan
-    # bf16 layer shape, two heads per group pair: the fused kernel, nsub = 32 sub-chunks of 128 tokens
+    # bf16 layer shape on the tensor-core path: nc = 16 chunks of 256 tokens
     d = desc(batch=4, seqlen=4096, nheads=80, headdim=64, dstate=128, ngroups=1, chunk=256,
              in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16)
     p = P()
     assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0
-    assert p.tensor_cores == 1 and p.fused == 1
-    nc, nsub, nseq, L = 16, 32, 4 * 80, 4096
+    assert p.tensor_cores == 1
+    nc, nseq, L, T = 16, 4 * 80, 4096, 256
     for tokens, nsup in ((p.super_tokens, p.n_super), (p.tail_super_tokens, p.tail_n_super)):
-        assert tokens % 128 == 0 and 128 <= tokens <= L
-        assert nsup == -(-L // tokens) and 1 <= nsup <= nc    # at most one state slot per chunk
-    assert 0 < p.split_sequences <= nseq and p.split_sequences % 2 == 0
-    assert (p.kernel_launches, p.memsets) == (1, 1)
-    # work items: per cut pair (nsup - 1) STATE items and 16 PASS items; per pair nsup SCAN items
-    parts = [(p.split_sequences // 2, p.n_super), ((nseq - p.split_sequences) // 2, p.tail_n_super)]
-    assert p.work_items == sum(n * ns + (n * (ns - 1) + 16 * n if ns > 1 else 0) for n, ns in parts)
-    # the same shape asks for the same plan (plans are cached per shape)
-    q = P()
-    assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(q)) == 0 and bytes(q) == bytes(p)
-    # wide state: the four-stage tensor-core path (cumsum, chunk_state and state_passing when the
-    # sequences are cut, scan)
-    w = desc(batch=32, seqlen=1024, nheads=64, headdim=128, dstate=256, ngroups=4, chunk=128,
-             in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16)
-    assert lib.ssd_fwd_plan(ctypes.byref(w), ctypes.byref(p)) == 0
-    assert p.tensor_cores == 1 and p.fused == 0 and p.work_items == 0
-    assert p.super_tokens % 128 == 0 and p.n_super == -(-1024 // p.super_tokens)
-    parts = [(p.split_sequences, p.n_super), (32 * 64 - p.split_sequences, p.tail_n_super)]
+        assert tokens % T == 0 and T <= tokens <= L          # whole chunks
+        assert nsup == -(-L // tokens) and 1 <= nsup <= nc
+    assert 0 < p.split_sequences <= nseq
+    # the split falls on a whole chunk_state head group (4 heads of one group here)
+    assert p.split_sequences % 4 == 0
+    parts = [(p.split_sequences, p.n_super), (nseq - p.split_sequences, p.tail_n_super)]
     assert p.kernel_launches == 2 + sum(2 for n, ns in parts if n > 0 and ns > 1)
     assert 1 <= p.memsets <= 3
+    # the same shape asks for the same plan
+    q = P()
+    assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(q)) == 0 and bytes(q) == bytes(p)
     # forced CUDA-core path: one chunk per super-chunk, four stages, no split
     d.flags = 1
     assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0
-    assert (p.tensor_cores, p.fused, p.super_tokens, p.n_super, p.kernel_launches, p.memsets) == (0, 0, 256, nc, 4, 1)
-    assert (p.split_sequences, p.tail_super_tokens, p.tail_n_super, p.work_items) == (nseq, 256, nc, 0)
+    assert (p.tensor_cores, p.super_tokens, p.n_super, p.kernel_launches, p.memsets) == (0, T, nc, 4, 1)
+    assert (p.split_sequences, p.tail_super_tokens, p.tail_n_super) == (nseq, T, nc)
     # empty sequence: nothing launched
     d = desc(seqlen=0)
     assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0 and p.kernel_launches == 0
