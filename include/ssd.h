@@ -287,7 +287,7 @@ ssd_status ssd_s6_fwd(const ssd_s6_desc *desc, const void *x, const void *delta,
  *    executions overlap on the GPU (different streams, or different host
  *    threads without ordering) race on it and give wrong results.  Order them
  *    on one stream.  The array keeps the previous call's contents; each call
- *    clears what must start at zero (the error word, and the partial state
+ *    clears what must start at zero (the error word, a counter, and the partial state
  *    sums when its plan adds them with atomics) and writes every other
  *    scratch byte before reading it.
  *  - A bounded wait that expired inside the call is reported by

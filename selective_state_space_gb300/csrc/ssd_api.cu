@@ -57,7 +57,8 @@ ssd_status check_desc(const ssd_desc *d, Problem *pr, bool need_seq)
 
 size_t esize(int dt) { return dt == SSD_BF16 ? 2 : 4; }
 
-// Workspace: [error word | G [B][nh][L] | s_local [B][nh][nc][H][S] | h_start [B][nh][nc][H][S]],
+// Workspace: [error word, count of finished cumsum CTAs (a 256-byte header) | G [B][nh][L] |
+// s_local [B][nh][nc][H][S] | h_start [B][nh][nc][H][S]],
 // all float32, sized for one state per chunk (the largest any path uses).
 struct Workspace {
     int *err;
@@ -233,7 +234,9 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
 
     auto rec = [&](int i) -> bool { return !events || cudaEventRecord((cudaEvent_t)events[i], st) == cudaSuccess; };
     const bool tc = use_tensor_cores(desc, pr);
-    if (cudaMemsetAsync(w.err, 0, sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
+    // the error word and, next to it, the count of finished cumsum CTAs
+    if (cudaMemsetAsync(w.err, 0, 2 * sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
+    unsigned *g_count = reinterpret_cast<unsigned *>(w.err + 1);
     ssd::ScanSplit sp{};
     PlanPart parts[2];
     // the float32 copy of dt is read by chunk_state only: the sequences of the parts it runs for.
@@ -244,6 +247,8 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
     int64_t dtT_lo = 0, dtT_hi = 0;
     if (tc) {
         sp = choose_tc_plan(pr);
+        sp.g_count = g_count;
+        sp.g_target = ssd::cumsum_ctas(pr);
         plan_parts(pr, sp, parts);
         for (const PlanPart &p : parts) {
             if (!staged) break;
@@ -253,8 +258,8 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
         }
     }
     if (!rec(0) ||
-        ssd::launch_chunk_cumsum(pr, dt, A, w.G, dtT_hi > dtT_lo ? w.dtT : nullptr, dtT_lo, dtT_hi, st) !=
-            cudaSuccess ||
+        ssd::launch_chunk_cumsum(pr, dt, A, w.G, dtT_hi > dtT_lo ? w.dtT : nullptr, dtT_lo, dtT_hi, st,
+                                 tc ? g_count : nullptr) != cudaSuccess ||
         !rec(1))
         return SSD_ERR_CUDA;
 

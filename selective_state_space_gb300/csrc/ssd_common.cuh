@@ -67,9 +67,12 @@ struct SeqRange {
 
 // Host-side launchers (one per stage).  Each returns the launch status.
 // dtT (nullable): also write dt as float32 in the [b][h][L] layout of G, for the sequences
-// (b * nh + h) in [dtT_lo, dtT_hi) only.
+// (b * nh + h) in [dtT_lo, dtT_hi) only.  count (nullable, zeroed beforehand): each CTA adds 1
+// to it once its part of G is written and visible device-wide; there are cumsum_ctas(pr) CTAs.
 cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *A, float *G,
-                                float *dtT, int64_t dtT_lo, int64_t dtT_hi, cudaStream_t st);
+                                float *dtT, int64_t dtT_lo, int64_t dtT_hi, cudaStream_t st,
+                                unsigned *count = nullptr);
+unsigned cumsum_ctas(const Problem &pr);
 cudaError_t launch_chunk_state_simt(const Problem &pr, const void *x, const void *dt,
                                     const void *Bm, const float *G, float *s_local,
                                     cudaStream_t st);

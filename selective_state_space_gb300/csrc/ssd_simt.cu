@@ -30,7 +30,8 @@ namespace {
 template <typename Tin>
 __global__ void __launch_bounds__(256)
 k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *__restrict__ G,
-               float *__restrict__ dtT, int64_t dtT_lo, int64_t dtT_hi, int64_t L, int nh, int T)
+               float *__restrict__ dtT, int64_t dtT_lo, int64_t dtT_hi, int64_t L, int nh, int T,
+               unsigned *count)
 {
     extern __shared__ float tile[];   // [T][33] in-run cumsum, then (dtT only) [T][33] dt
     __shared__ float run_sum[32][33]; // [run][head] run totals (T <= 1024: at most 32 runs)
@@ -93,6 +94,12 @@ k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *_
             float *dd = dtT + bh * L + t0;
             for (int t = lane; t < n; t += 32) dd[t] = tile[(T + t) * 33 + j];
         }
+    }
+    if (count) {
+        // this CTA's G is written: make it visible device-wide, then count the CTA
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) atomicAdd(count, 1u);
     }
 }
 
@@ -173,10 +180,14 @@ k_chunk_state_simt(const Tin *__restrict__ x, const Tin *__restrict__ dt,
 // only and h_final = h_nm is written when nm == nsup (and h_final is not NULL).
 // With R = 1 this is the blog's per-chunk loop.  VEC consecutive state elements
 // per thread (float4 when H*S allows), consecutive threads on consecutive
-// elements: every step is a coalesced 128-bit stream.
+// elements: every step is a coalesced 128-bit stream.  Blocks of 1024 threads: the
+// work is a few dependent load rounds per sequence, so a few large CTAs finish as
+// soon as many small ones, and hold fewer SMs that the scan's CTAs could start on.
 // ---------------------------------------------------------------------------
+constexpr int kPassThreads = 1024;
+
 template <int VEC>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kPassThreads)
 k_state_passing(const float *__restrict__ G, const float *__restrict__ s_local,
                 const float *__restrict__ h0, float *__restrict__ h_start,
                 float *__restrict__ h_final, Problem pr, SeqRange seqs, int R, int nsup, int nm)
@@ -184,7 +195,7 @@ k_state_passing(const float *__restrict__ G, const float *__restrict__ s_local,
     using V = typename std::conditional<VEC == 4, float4, float>::type;
     constexpr int kBatch = 8;                     // states loaded together (independent loads)
     constexpr int kWin = 1024;                    // super-chunks whose decays are staged at once
-    constexpr int kTile = 256;                    // chunk-end G values loaded together (= block size)
+    constexpr int kTile = kPassThreads;           // chunk-end G values loaded together (= block size)
     __shared__ float sdec[kWin];                  // exp2 of each super-chunk's total log2 decay
     __shared__ float sdl[kWin];                   // the total log2 decays, summed tile by tile
     __shared__ float sgl[kTile];                  // G at the end of each chunk of the tile
@@ -495,8 +506,13 @@ size_t scan_smem_bytes(const Problem &pr)
 
 }  // namespace
 
+unsigned cumsum_ctas(const Problem &pr)
+{
+    return (unsigned)(pr.nc * ((pr.nh + 31) / 32) * pr.B);
+}
+
 cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *A, float *G,
-                                float *dtT, int64_t dtT_lo, int64_t dtT_hi, cudaStream_t st)
+                                float *dtT, int64_t dtT_lo, int64_t dtT_hi, cudaStream_t st, unsigned *count)
 {
     dim3 grid((unsigned)pr.nc, (unsigned)((pr.nh + 31) / 32), (unsigned)pr.B);
     const size_t smem = sizeof(float) * 33 * (size_t)pr.T * (dtT ? 2 : 1);
@@ -504,11 +520,13 @@ cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *
     if (pr.in_dt == SSD_BF16) {
         auto kern = k_chunk_cumsum<__nv_bfloat16>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
-        kern<<<grid, 256, smem, st>>>((const __nv_bfloat16 *)dt, A, G, dtT, dtT_lo, dtT_hi, pr.L, (int)pr.nh, (int)pr.T);
+        kern<<<grid, 256, smem, st>>>((const __nv_bfloat16 *)dt, A, G, dtT, dtT_lo, dtT_hi, pr.L, (int)pr.nh, (int)pr.T,
+                                      count);
     } else {
         auto kern = k_chunk_cumsum<float>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
-        kern<<<grid, 256, smem, st>>>((const float *)dt, A, G, dtT, dtT_lo, dtT_hi, pr.L, (int)pr.nh, (int)pr.T);
+        kern<<<grid, 256, smem, st>>>((const float *)dt, A, G, dtT, dtT_lo, dtT_hi, pr.L, (int)pr.nh, (int)pr.T,
+                                      count);
     }
     return cudaGetLastError();
 }
@@ -537,12 +555,12 @@ cudaError_t launch_state_passing(const Problem &pr, SeqRange seqs, const float *
     const bool v4 = (HS % 4 == 0) && ((uintptr_t)s_local % 16 == 0) && ((uintptr_t)h_start % 16 == 0) &&
                     (!h0 || (uintptr_t)h0 % 16 == 0) && (!h_final || (uintptr_t)h_final % 16 == 0);
     const int vec = v4 ? 4 : 1;
-    dim3 grid((unsigned)((HS / vec + 255) / 256), (unsigned)(seqs.n < 65535 ? seqs.n : 65535));
+    dim3 grid((unsigned)((HS / vec + kPassThreads - 1) / kPassThreads), (unsigned)(seqs.n < 65535 ? seqs.n : 65535));
     if (v4)
-        return launch_pdl(k_state_passing<4>, grid, dim3(256), 0, st, G, s_local, h0, h_start, h_final, pr, seqs, R,
-                          nsup, nm);
-    return launch_pdl(k_state_passing<1>, grid, dim3(256), 0, st, G, s_local, h0, h_start, h_final, pr, seqs, R, nsup,
-                      nm);
+        return launch_pdl(k_state_passing<4>, grid, dim3(kPassThreads), 0, st, G, s_local, h0, h_start, h_final, pr,
+                          seqs, R, nsup, nm);
+    return launch_pdl(k_state_passing<1>, grid, dim3(kPassThreads), 0, st, G, s_local, h0, h_start, h_final, pr, seqs,
+                      R, nsup, nm);
 }
 
 template <typename Tin, typename Tout>

@@ -100,6 +100,26 @@ __device__ __noinline__ void retire_loads(uint64_t *bars, int first, int stages,
         if (!mbar_wait(smem_u32(&bars[first + i % stages]), (uint32_t)(i / stages) & 1u, kRetireNs)) set_error(err, 1);
 }
 
+// Thread 0 of a CTA: wait until *count reaches target; false once about limit_ns has passed
+// (0: one test).  The acquire load orders the CTA's later reads (after a barrier) behind the
+// writes the count stands for.
+__device__ __noinline__ bool wait_count(const unsigned *count, unsigned target, uint64_t limit_ns)
+{
+    auto ready = [&]() {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+        return v >= target;
+    };
+    if (ready()) return true;
+    if (limit_ns == 0) return false;
+    const long long c0 = clock64(), limit = (long long)(limit_ns * 5 / 2);
+    while (!ready()) {
+        if (clock64() - c0 > limit) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
 // The MMA thread: wait until every MMA it issued has completed (a commit to `bar`, used for
 // nothing else, arrives once they all have).
 __device__ __noinline__ void retire_mmas(uint32_t bar, int *err)
@@ -533,9 +553,17 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
-    // the next kernel may launch now; this one reads G (and the states) of the kernels before
+    // the next kernel may launch now.  A CTA that enters from h0 reads only G of the kernels
+    // before, so it waits for the cumsum's CTAs alone (when the launcher passed their count);
+    // the others wait for every kernel before (their entering states come last).  G is then
+    // read through L2 (__ldcg): it may be written while this grid runs.
     pdl_trigger();
-    pdl_wait();
+    if (sp.g_count && m < sp.hs_from) {
+        if (threadIdx.x == 0 && !wait_count(sp.g_count, sp.g_target, kWait)) set_error(err, 1);
+        __syncthreads();
+    } else {
+        pdl_wait();
+    }
 
     if (warp == 0) {
         // ---- TMA producer ---------------------------------------------------------------
@@ -668,10 +696,10 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         auto load_scalars = [&](int q) {
             const int64_t t0 = t_begin + (int64_t)q * kQ;
             const int64_t tr = clamp_t<kRagged>(t0 + r, pr.L), tl = clamp_t<kRagged>(t0 + kQ - 1, pr.L);
-            n_gr = Gh[tr];
+            n_gr = __ldcg(Gh + tr);
             n_dt = in_seq<kRagged>(t0 + r, pr.L) ? __bfloat162float(dt[((int64_t)b * pr.L + t0 + r) * pr.nh + h]) : 0.f;
-            n_glast = Gh[tl];
-            n_gbase = (q % qpc == 0) ? 0.f : Gh[t0 - 1];
+            n_glast = __ldcg(Gh + tl);
+            n_gbase = (q % qpc == 0) ? 0.f : __ldcg(Gh + t0 - 1);
         };
         if (nq > 0) load_scalars(0);
         for (int q = 0; q < nq && ok; ++q) {
@@ -814,9 +842,9 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__
         float n_gr = 0.f, n_gend = 0.f, n_gbase = 0.f;
         auto load_scalars = [&](int q) {
             const int64_t t0 = t_begin + (int64_t)q * kQ;
-            n_gr = Gh[clamp_t<kRagged>(t0 + r, pr.L)];
-            n_gend = Gh[clamp_t<kRagged>(t0 + (r | 15), pr.L)];  // G at the end of row r's 16-token block
-            n_gbase = (q % qpc == 0) ? 0.f : Gh[t0 - 1];
+            n_gr = __ldcg(Gh + clamp_t<kRagged>(t0 + r, pr.L));
+            n_gend = __ldcg(Gh + clamp_t<kRagged>(t0 + (r | 15), pr.L));  // G at the end of row r's 16-token block
+            n_gbase = (q % qpc == 0) ? 0.f : __ldcg(Gh + t0 - 1);
         };
         // Software-pipelined by one sub-chunk: iteration q builds P of sub-chunk q + 1, then
         // writes y of sub-chunk q.  The MMAs of q + 1 wait on that P, while the y of q waits
@@ -1091,9 +1119,17 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
-    // the next kernel may launch now; this one reads G (and the states) of the kernels before
+    // the next kernel may launch now.  A CTA that enters from h0 reads only G of the kernels
+    // before, so it waits for the cumsum's CTAs alone (when the launcher passed their count);
+    // the others wait for every kernel before (their entering states come last).  G is then
+    // read through L2 (__ldcg): it may be written while this grid runs.
     pdl_trigger();
-    pdl_wait();
+    if (sp.g_count && m < sp.hs_from) {
+        if (threadIdx.x == 0 && !wait_count(sp.g_count, sp.g_target, kWait)) set_error(err, 1);
+        __syncthreads();
+    } else {
+        pdl_wait();
+    }
 
     if (warp == 0) {
         // ---- C and B tiles (one stage: free once CB, the update and C h^T have read it) -------
@@ -1244,13 +1280,13 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
         auto load_scalars = [&](int q) {
             const int64_t t0 = t_begin + (int64_t)q * kQ;
             const int64_t tr = clamp_t<kRagged>(t0 + r, pr.L), tl = clamp_t<kRagged>(t0 + kQ - 1, pr.L);
-            n_g[0] = GA[tr];
-            n_g[1] = GB[tr];
-            n_gl[0] = GA[tl];
-            n_gl[1] = GB[tl];
+            n_g[0] = __ldcg(GA + tr);
+            n_g[1] = __ldcg(GB + tr);
+            n_gl[0] = __ldcg(GA + tl);
+            n_gl[1] = __ldcg(GB + tl);
             const bool cs = q % qpc == 0;
-            n_gb[0] = cs ? 0.f : GA[t0 - 1];
-            n_gb[1] = cs ? 0.f : GB[t0 - 1];
+            n_gb[0] = cs ? 0.f : __ldcg(GA + t0 - 1);
+            n_gb[1] = cs ? 0.f : __ldcg(GB + t0 - 1);
             n_dt = in_seq<kRagged>(t0 + r, pr.L)
                        ? *reinterpret_cast<const uint32_t *>(dt + ((int64_t)b * pr.L + t0 + r) * pr.nh + hA)
                        : 0u;
@@ -1379,11 +1415,11 @@ k_chunk_scan_pair(const __grid_constant__ CUtensorMap tmC, const __grid_constant
         auto load_scalars = [&](int q) {
             const int64_t t0 = t_begin + (int64_t)q * kQ;
             const int64_t tr = clamp_t<kRagged>(t0 + r, pr.L);
-            n_g[0] = GA[tr];
-            n_g[1] = GB[tr];
+            n_g[0] = __ldcg(GA + tr);
+            n_g[1] = __ldcg(GB + tr);
             const float *Gh = half ? GB : GA;
-            n_gb = (q % qpc == 0) ? 0.f : Gh[t0 - 1];
-            n_gend = Gh[clamp_t<kRagged>(t0 + (r | 15), pr.L)];
+            n_gb = (q % qpc == 0) ? 0.f : __ldcg(Gh + t0 - 1);
+            n_gend = __ldcg(Gh + clamp_t<kRagged>(t0 + (r | 15), pr.L));
             n_dt = in_seq<kRagged>(t0 + r, pr.L) ? __bfloat162float(dt[((int64_t)b * pr.L + t0 + r) * pr.nh + hA + half])
                                                  : 0.f;
         };

@@ -30,11 +30,17 @@ cudaError_t launch_chunk_state_tc(const Problem &pr, SeqRange seqs, const void *
 // super-chunk of one 64-column block of H.  Super-chunk m of sequence bh enters from
 // h0 (zeros if NULL) when m < hs_from, else from the state at h_start index
 // bh * nsup0 + m (first part) or base1 + (bh - split) * nsup1 + m (second part).
+// When g_count is set, the CTAs that enter from h0 (m < hs_from) read nothing but G from the
+// kernels before the scan: instead of waiting for all of them to finish, they wait until
+// *g_count reaches g_target (the cumsum CTAs count themselves there, see launch_chunk_cumsum),
+// so they do not wait for the chunk_state and state_passing launches the other CTAs need.
 struct ScanSplit {
     int64_t split;
     int R0, nsup0, R1, nsup1;
     int hs_from;
     int64_t base1;
+    const unsigned *g_count;
+    unsigned g_target;
 };
 
 // Sequences per scan CTA: 2 (two heads of one B/C group) when S = 128, H = 64 and the
