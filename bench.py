@@ -9,6 +9,9 @@ resident in HBM.  The headline workload is the Mamba-2-2.7B-shaped layer
 Its inputs and outputs (367 MB) are larger than the 129 MB L2, so no L2 flush
 is done between steps.
 
+The default line also carries ``second_workload``: the long-context prefill
+(B=1, L=65536, 32 heads, 8 B/C groups) timed the same way in the same run.
+
 Under torchrun (N > 1) every rank runs its own replica of the workload
 (independent problems, no collective on the data path); value = tokens of all
 ranks / max-over-ranks time.  ``--impl reference`` times the CPU oracle on a
@@ -211,6 +214,26 @@ def _head_windows(s, width):
             lo = hi
 
 
+def cpu_model() -> str:
+    """The host CPU's model name, as lscpu or /proc/cpuinfo reports it."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(inp, budget_s: float):
     """The oracle as it stands, timed on a bounded sample of (batch, head) pairs at
     full sequence length, with every core this process may use."""
@@ -232,7 +255,7 @@ def cpu_baseline(inp, budget_s: float):
             break
     el = time.perf_counter() - t0
     tokens_equiv = done * s.seqlen / s.nheads      # (batch, head) pairs -> whole-workload tokens
-    return {"value": tokens_equiv / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": tokens_equiv / el, "unit": UNIT, "cores": cores, "model": cpu_model(), "kind": "oracle",
             "sample": f"{done} (batch, head) pairs (workload has {s.batch * s.nheads}) at full length L={s.seqlen}, "
                       f"sequential float64 recurrence, {el:.1f} s; tokens/s scaled to the whole workload"}
 
@@ -338,11 +361,13 @@ def run_decode(args, shape):
            + 2 * shape.batch * shape.ngroups * shape.dstate * e + 2 * shape.nheads * 4)
     flush = alg < 2 * L2_BYTES
     scrub = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev) if flush else None
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clk:
+        # warm-up inside the sampled window, right before the timed steps (the sampler's start-up
+        # leaves the GPU idle for a moment)
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
         if not flush:
             start.record(stream)
             for _ in range(args.steps):
@@ -418,7 +443,7 @@ def bwd_cpu_baseline(inp, gin, budget_s: float):
         if time.perf_counter() - t0 >= budget_s:
             break
     el = time.perf_counter() - t0
-    return {"value": done * s.seqlen / s.nheads / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": done * s.seqlen / s.nheads / el, "unit": UNIT, "cores": cores, "model": cpu_model(), "kind": "oracle",
             "sample": f"{done} (batch, head) pairs (workload has {s.batch * s.nheads}) at full length L={s.seqlen}, "
                       f"reverse-mode float64 recurrence, {el:.1f} s; tokens/s scaled to the whole workload"}
 
@@ -462,11 +487,11 @@ def run_bwd(args, shape):
         return api.ssd_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], dy, shape.chunk, d["h0"], dhf,
                            workspace=ws, stream=stream)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clk:
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
         start.record(stream)
         for _ in range(args.steps):
             step()
@@ -530,7 +555,7 @@ def s6_cpu_baseline(inp, budget_s: float):
             done += cores
     el = time.perf_counter() - t0
     tok = done * s.seqlen / s.dim                             # channels -> whole-workload tokens (B L per B dim)
-    return {"value": tok / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+    return {"value": tok / el, "unit": "tokens/s", "cores": cores, "model": cpu_model(), "kind": "oracle",
             "sample": f"{done} channels (workload has {s.batch * s.dim}) at full length L={s.seqlen}, sequential "
                       f"float64 recurrence, {el:.1f} s; tokens/s scaled to the whole workload"}
 
@@ -576,11 +601,11 @@ def run_s6(args, shape):
     def step():
         api.s6_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["h0"], y=y, stream=stream)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clk:
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
         ms = 0.0
         if not flush:
             start.record(stream)
@@ -625,6 +650,52 @@ def run_s6(args, shape):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = s6_cpu_baseline(inp, args.cpu_budget_s)
     print(json.dumps(line), flush=True)
+
+
+def time_fwd_device(shape, steps: int, warmup: int, dev) -> tuple:
+    """ms per ssd_fwd step of `shape` with its inputs resident (back to back, or each step
+    alone after an L2 flush when the workload fits in L2), and its plan."""
+    from selective_state_space_gb300 import api
+    inp = workloads.make_inputs(shape)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.tensors().items()}
+    desc = api.desc_for(d["x"], d["B"], shape.chunk)
+    plan = api.fwd_plan(desc)
+    ws = api.alloc_workspace(desc, dev)
+    y = torch.empty_like(d["x"])
+    hf = torch.empty((shape.batch, shape.nheads, shape.headdim, shape.dstate), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        api.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], shape.chunk, d["h0"], y=y, h_final=hf,
+                    workspace=ws, stream=stream)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if not needs_l2_flush(shape):
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        ms = start.elapsed_time(end)
+    else:
+        scrub = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
+        ms = 0.0
+        for i in range(steps):
+            scrub.fill_(i & 0xff)
+            start.record(stream)
+            step()
+            end.record(stream)
+            torch.cuda.synchronize()
+            ms += start.elapsed_time(end)
+    return ms / steps, plan
+
+
+# The second workload the default line also reports, timed in the same run: the long-context
+# prefill, whose super-chunk cut needs the chunk_state and state_passing passes in full.
+SECOND_WORKLOAD = "long-prefill-64k"
 
 
 def main():
@@ -689,20 +760,21 @@ def main():
         api.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], shape.chunk, d["h0"], y=y, h_final=hf,
                     workspace=ws, stream=stream, events=events)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
     for row in ev:          # torch creates the underlying CUDA event on first record
         for e in row:
             e.record(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
     flush = needs_l2_flush(shape)
     scrub = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev) if flush else None
     with ClockSampler(local_rank) as clk:
+        # warm-up inside the sampled window, right before the timed steps (the sampler's start-up
+        # leaves the GPU idle for a moment)
+        for _ in range(max(3, args.warmup)):
+            step()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
         # the headline: K plain forward passes, nothing else on the stream (or, for a
         # workload that fits in L2, each pass timed alone after an L2 flush)
         if not flush:
@@ -805,6 +877,19 @@ def main():
         "gpu_launches": plan["kernel_launches"] * args.steps,
         "clocks": clk.summary(),
     }
+    if shape.name == "mamba2-2.7b-layer":
+        # the second workload, timed the same way in the same process, on this rank alone
+        s2 = workloads.by_name(SECOND_WORKLOAD)
+        with ClockSampler(local_rank) as clk2:
+            ms2, plan2 = time_fwd_device(s2, args.steps, args.warmup, dev)
+        sb2 = stage_bytes(s2, plan2)
+        roof2 = max(sb2["step"] / (peak * 1e9), alg_flops(s2) / (float(peaks["bf16_tflops"]) * 1e12)) * 1e3
+        line["second_workload"] = {
+            "workload": s2.name, "config": config_of(s2), "ms_per_step": ms2, "steps": args.steps,
+            "warmup": max(3, args.warmup), "value": s2.tokens / (ms2 * 1e-3), "unit": UNIT,
+            "step_roofline": {"alg_bytes": sb2["step"], "roofline_ms": roof2, "frac": roof2 / ms2},
+            "plan": plan2, "clocks": clk2.summary(),
+        }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_budget_s)
     print(json.dumps(line), flush=True)

@@ -51,6 +51,16 @@ typedef struct CUevent_st *ssd_event_t;     /* identical to cudaEvent_t  */
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
+/* ssd_desc.dt_dtype: dt in the dtype of x, Bm and Cm (the default), or dt in float32 beside
+ * bfloat16 x, Bm, Cm.  The blog's first kernel ("Kernel 1: cumulative sum") takes dt up to
+ * float32 before the cumulative sum of A dt, which sets every decay; with SSD_DT_FLOAT32 that
+ * sum runs on the caller's float32 dt, and the later stages, where dt enters only products that
+ * are rounded to bfloat16 as tensor-core operands, read a bfloat16 copy the cumsum writes into
+ * the workspace.  Accepted by ssd_fwd, ssd_fwd_timed, ssd_fwd_noalloc, ssd_fwd_plan,
+ * ssd_fwd_workspace_size, ssd_fwd_path and ssd_chunk_cumsum; the other entry points return
+ * SSD_ERR_UNSUPPORTED for it. */
+typedef enum { SSD_DT_AS_INPUTS = 0, SSD_DT_FLOAT32 = 1 } ssd_dt_dtype;
+
 typedef enum {
     SSD_OK = 0,
     SSD_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, negative size, bad dtype, G does not divide nh */
@@ -76,7 +86,7 @@ typedef struct {
     int32_t in_dtype;   /* ssd_dtype of x, dt, Bm, Cm */
     int32_t out_dtype;  /* ssd_dtype of y */
     int32_t flags;      /* SSD_FLAG_* bits, 0 by default */
-    int32_t reserved;   /* must be 0 */
+    int32_t dt_dtype;   /* ssd_dt_dtype of dt, SSD_DT_AS_INPUTS (0) by default */
 } ssd_desc;
 
 /* Use the CUDA-core kernels for every stage even where tensor-core kernels
@@ -98,7 +108,8 @@ const char *ssd_status_string(ssd_status s);
 /* Bytes of device workspace ssd_fwd needs for `desc` (written to *bytes).
  * The workspace holds an error word, the in-chunk cumsum G, a float32 copy
  * of dt in G's [b][h][L] layout, the local (super-)chunk states and the
- * (super-)chunk-start states, all float32.
+ * (super-)chunk-start states, all float32, and with SSD_DT_FLOAT32 a bfloat16
+ * copy of dt in its own layout.
  * Errors: SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED. */
 ssd_status ssd_fwd_workspace_size(const ssd_desc *desc, size_t *bytes);
 

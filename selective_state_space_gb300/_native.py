@@ -12,6 +12,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libssd.so")
 SSD_F32, SSD_BF16 = 0, 1
 SSD_FLAG_FORCE_SIMT = 1
 SSD_FLAG_EXPIRE_WAITS = 2   # test hook: every bounded device wait expires at once
+SSD_DT_AS_INPUTS, SSD_DT_FLOAT32 = 0, 1   # ssd_desc.dt_dtype
 NOALLOC_SCRATCH_BYTES = 32 << 20   # SSD_NOALLOC_SCRATCH_BYTES of include/ssd.h
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_WORKSPACE",
           4: "SSD_ERR_CUDA", 5: "SSD_ERR_TOO_LARGE", 6: "SSD_ERR_TIMEOUT"}
@@ -28,7 +29,7 @@ class Desc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
                 ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
                 ("chunk", ctypes.c_int64), ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
-                ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32), ("dt_dtype", ctypes.c_int32)]
 
 
 class S6Desc(ctypes.Structure):

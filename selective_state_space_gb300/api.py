@@ -43,21 +43,25 @@ def _stream(stream) -> Optional[int]:
 
 
 def make_desc(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, in_dtype, out_dtype,
-              flags: int = 0) -> Desc:
+              flags: int = 0, dt_dtype: int = 0) -> Desc:
     d = Desc()
     d.batch, d.seqlen, d.nheads, d.headdim = batch, seqlen, nheads, headdim
     d.dstate, d.ngroups, d.chunk = dstate, ngroups, chunk
     d.in_dtype = _dtype_code(in_dtype) if isinstance(in_dtype, torch.dtype) else int(in_dtype)
     d.out_dtype = _dtype_code(out_dtype) if isinstance(out_dtype, torch.dtype) else int(out_dtype)
-    d.flags, d.reserved = flags, 0
+    d.flags, d.dt_dtype = flags, dt_dtype
     return d
 
 
-def desc_for(x: torch.Tensor, Bm: torch.Tensor, chunk: int, out_dtype=None, flags: int = 0) -> Desc:
+def desc_for(x: torch.Tensor, Bm: torch.Tensor, chunk: int, out_dtype=None, flags: int = 0, dt=None) -> Desc:
+    """The descriptor of a forward pass on these tensors; a float32 ``dt`` beside bfloat16
+    ``x`` selects SSD_DT_FLOAT32."""
     batch, seqlen, nheads, headdim = x.shape
     ngroups, dstate = Bm.shape[2], Bm.shape[3]
+    dt_dtype = (_native.SSD_DT_FLOAT32 if dt is not None and dt.dtype == torch.float32 and x.dtype == torch.bfloat16
+                else _native.SSD_DT_AS_INPUTS)
     return make_desc(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, x.dtype,
-                     out_dtype or x.dtype, flags)
+                     out_dtype or x.dtype, flags, dt_dtype)
 
 
 def workspace_size(desc: Desc) -> int:
@@ -92,12 +96,13 @@ def ssd_fwd(x, dt, A, B, C, D, chunk: int, h0=None, *, y=None, h_final=None, wan
             check_errors: bool = False):
     """Chunked SSD forward.  Returns (y, h_final or None).
 
-    x [B,L,nh,H], dt [B,L,nh], B/C [B,L,G,S] in float32 or bfloat16 (same dtype);
+    x [B,L,nh,H], dt [B,L,nh], B/C [B,L,G,S] in float32 or bfloat16 (same dtype; dt may
+    also be float32 beside bfloat16 x, B, C);
     A, D [nh] float32; h0 [B,nh,H,S] float32 or None.  ``events`` (8 CUDA events)
     selects ssd_fwd_timed, which records them around the four stages.
     ``check_errors`` synchronises and raises if a bounded device wait expired.
     """
-    desc = desc_for(x, B, chunk, out_dtype, flags)
+    desc = desc_for(x, B, chunk, out_dtype, flags, dt)
     batch, seqlen, nheads, headdim = x.shape
     dstate = B.shape[3]
     if y is None:

@@ -32,7 +32,9 @@ ssd_status check_desc(const ssd_desc *d, Problem *pr, bool need_seq)
     if (d->nheads % d->ngroups != 0) return SSD_ERR_INVALID_ARG;
     if (d->in_dtype != SSD_F32 && d->in_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
     if (d->out_dtype != SSD_F32 && d->out_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
-    if (d->reserved != 0 || (d->flags & ~(SSD_FLAG_FORCE_SIMT | SSD_FLAG_EXPIRE_WAITS)) != 0) return SSD_ERR_INVALID_ARG;
+    if ((d->dt_dtype != SSD_DT_AS_INPUTS && d->dt_dtype != SSD_DT_FLOAT32) ||
+        (d->flags & ~(SSD_FLAG_FORCE_SIMT | SSD_FLAG_EXPIRE_WAITS)) != 0)
+        return SSD_ERR_INVALID_ARG;
     if (need_seq && (d->seqlen < 0 || d->chunk < 1)) return SSD_ERR_INVALID_ARG;
     if (d->dstate > 256 || d->headdim > 1024) return SSD_ERR_UNSUPPORTED;
     if (need_seq && d->chunk > 1024) return SSD_ERR_UNSUPPORTED;
@@ -50,6 +52,7 @@ ssd_status check_desc(const ssd_desc *d, Problem *pr, bool need_seq)
     pr->hpg = d->ngroups ? d->nheads / d->ngroups : 1;
     pr->in_dt = d->in_dtype;
     pr->out_dt = d->out_dtype;
+    pr->dt_f32 = d->dt_dtype == SSD_DT_FLOAT32 && d->in_dtype == SSD_BF16;
     pr->wait_ns = (d->flags & SSD_FLAG_EXPIRE_WAITS) ? 0ull : 250000000ull;
     if (need_seq && pr->nc > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
     return SSD_OK;
@@ -58,14 +61,15 @@ ssd_status check_desc(const ssd_desc *d, Problem *pr, bool need_seq)
 size_t esize(int dt) { return dt == SSD_BF16 ? 2 : 4; }
 
 // Workspace: [error word, count of finished cumsum CTAs (a 256-byte header) | G [B][nh][L] |
-// s_local [B][nh][nc][H][S] | h_start [B][nh][nc][H][S]],
-// all float32, sized for one state per chunk (the largest any path uses).
+// dtT [B][nh][L] | s_local [B][nh][nc][H][S] | h_start [B][nh][nc][H][S] | dt16 [B][L][nh]],
+// float32 but dt16, states sized for one per chunk (the largest any path uses).
 struct Workspace {
     int *err;
     float *G;
     float *dtT;       // dt as float32, [b][h][L] (written by the cumsum, read by chunk_state)
     float *s_local;
     float *h_start;
+    __nv_bfloat16 *dt16;   // SSD_DT_FLOAT32 only: dt rounded to bfloat16 in dt's layout (written by the cumsum)
     size_t bytes;
 };
 
@@ -83,6 +87,11 @@ Workspace carve(const Problem &pr, void *base)
     w.s_local = (float *)(p + e_bytes + 2 * g_bytes);
     w.h_start = (float *)(p + e_bytes + 2 * g_bytes + s_bytes);
     w.bytes = e_bytes + 2 * g_bytes + 2 * s_bytes;
+    w.dt16 = nullptr;
+    if (pr.dt_f32) {
+        w.dt16 = (__nv_bfloat16 *)(p + w.bytes);
+        w.bytes += align_up(sizeof(__nv_bfloat16) * (size_t)(pr.B * pr.L * pr.nh), kWsAlign);
+    }
     return w;
 }
 
@@ -259,9 +268,11 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
     }
     if (!rec(0) ||
         ssd::launch_chunk_cumsum(pr, dt, A, w.G, dtT_hi > dtT_lo ? w.dtT : nullptr, dtT_lo, dtT_hi, st,
-                                 tc ? g_count : nullptr) != cudaSuccess ||
+                                 tc ? g_count : nullptr, w.dt16) != cudaSuccess ||
         !rec(1))
         return SSD_ERR_CUDA;
+    // with a float32 dt beside bfloat16 inputs, the stages after the cumsum read its bfloat16 copy
+    if (pr.dt_f32) dt = w.dt16;
 
     if (tc) {
         const int64_t HS = pr.H * pr.S;
@@ -418,6 +429,7 @@ ssd_status ssd_step(const ssd_desc *desc, const void *x, const void *dt, const f
     Problem pr;
     ssd_status s = check_desc(desc, &pr, false);
     if (s != SSD_OK) return s;
+    if (pr.dt_f32) return SSD_ERR_UNSUPPORTED;
     if (pr.B == 0 || pr.nh == 0) return SSD_OK;
     if (!x || !dt || !A || !Bm || !Cm || !D || !h || !y) return SSD_ERR_INVALID_ARG;
     if (!aligned(x, 4) || !aligned(dt, 2) || !aligned(Bm, 2) || !aligned(Cm, 2) || !aligned(y, 2) ||
@@ -443,6 +455,7 @@ ssd_status ssd_chunk_state(const ssd_desc *desc, const void *x, const void *dt, 
     Problem pr;
     ssd_status s = check_desc(desc, &pr, true);
     if (s != SSD_OK) return s;
+    if (pr.dt_f32) return SSD_ERR_UNSUPPORTED;
     if (!nonempty(pr)) return SSD_OK;
     if (!x || !dt || !Bm || !G || !s_local) return SSD_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(Bm, 16) || !aligned(G, 16) || !aligned(s_local, 16))
@@ -481,6 +494,7 @@ ssd_status ssd_chunk_scan(const ssd_desc *desc, const void *x, const void *dt, c
     Problem pr;
     ssd_status s = check_desc(desc, &pr, true);
     if (s != SSD_OK) return s;
+    if (pr.dt_f32) return SSD_ERR_UNSUPPORTED;
     if (!nonempty(pr)) return SSD_OK;
     if (!x || !dt || !Bm || !Cm || !D || !G || !h_start || !y) return SSD_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(Bm, 16) || !aligned(Cm, 16) || !aligned(G, 16) ||
@@ -505,7 +519,7 @@ ssd_status ssd_bwd_workspace_size(const ssd_desc *desc, size_t *bytes)
     if (!bytes) return SSD_ERR_INVALID_ARG;
     ssd_status s = check_desc(desc, &pr, true);
     if (s != SSD_OK) return s;
-    if (!ssd::bwd_supported(pr)) return SSD_ERR_UNSUPPORTED;
+    if (pr.dt_f32 || !ssd::bwd_supported(pr)) return SSD_ERR_UNSUPPORTED;
     *bytes = nonempty(pr) ? ssd::bwd_workspace(pr, nullptr, nullptr) : 0;
     return SSD_OK;
 }
@@ -519,7 +533,7 @@ ssd_status ssd_bwd(const ssd_desc *desc, const void *x, const void *dt, const fl
     Problem pr;
     ssd_status s = check_desc(desc, &pr, true);
     if (s != SSD_OK) return s;
-    if (!ssd::bwd_supported(pr)) return SSD_ERR_UNSUPPORTED;
+    if (pr.dt_f32 || !ssd::bwd_supported(pr)) return SSD_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     const size_t es = esize(pr.in_dt);
     const size_t nstate = (size_t)(pr.B * pr.nh * pr.H * pr.S);

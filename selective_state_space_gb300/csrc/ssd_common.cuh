@@ -17,6 +17,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct Problem {
     int64_t B, L, nh, H, S, G, T, nc, hpg;
     int in_dt, out_dt;
+    int dt_f32;           // 1: dt is float32 while x, B, C are bfloat16 (SSD_DT_FLOAT32)
     // 0 selects the tensor-core kernels built for the test hook of the timeout path (every
     // wait for another warp's work not satisfied at once expires); else 250 ms, the bound
     // the normal kernels have built in
@@ -69,9 +70,11 @@ struct SeqRange {
 // dtT (nullable): also write dt as float32 in the [b][h][L] layout of G, for the sequences
 // (b * nh + h) in [dtT_lo, dtT_hi) only.  count (nullable, zeroed beforehand): each CTA adds 1
 // to it once its part of G is written and visible device-wide; there are cumsum_ctas(pr) CTAs.
+// dt is float32 when pr.dt_f32 (else in the input dtype); dt16 (nullable): also write dt
+// rounded to bfloat16 in its own [b][t][h] layout.
 cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *A, float *G,
                                 float *dtT, int64_t dtT_lo, int64_t dtT_hi, cudaStream_t st,
-                                unsigned *count = nullptr);
+                                unsigned *count = nullptr, __nv_bfloat16 *dt16 = nullptr);
 unsigned cumsum_ctas(const Problem &pr);
 cudaError_t launch_chunk_state_simt(const Problem &pr, const void *x, const void *dt,
                                     const void *Bm, const float *G, float *s_local,

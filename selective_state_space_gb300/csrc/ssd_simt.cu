@@ -31,7 +31,7 @@ template <typename Tin>
 __global__ void __launch_bounds__(256)
 k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *__restrict__ G,
                float *__restrict__ dtT, int64_t dtT_lo, int64_t dtT_hi, int64_t L, int nh, int T,
-               unsigned *count)
+               unsigned *count, __nv_bfloat16 *__restrict__ dt16)
 {
     extern __shared__ float tile[];   // [T][33] in-run cumsum, then (dtT only) [T][33] dt
     __shared__ float run_sum[32][33]; // [run][head] run totals (T <= 1024: at most 32 runs)
@@ -53,6 +53,11 @@ k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *_
         if (32 * r + 32 <= n) {                // whole run inside the chunk: no per-token checks
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = to_f32(__ldg(src + (int64_t)i * nh));
+            if (dt16 && h < nh) {
+                __nv_bfloat16 *d16 = dt16 + ((int64_t)b * L + t0 + 32 * r) * nh + h;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) d16[(int64_t)i * nh] = __float2bfloat16_rn(v[i]);
+            }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 acc += a * v[i];
@@ -65,6 +70,10 @@ k_chunk_cumsum(const Tin *__restrict__ dt, const float *__restrict__ A, float *_
         } else {                               // the chunk ends inside this run
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = (32 * r + i < n) ? to_f32(__ldg(src + (int64_t)i * nh)) : 0.f;
+            if (dt16 && h < nh) {
+                __nv_bfloat16 *d16 = dt16 + ((int64_t)b * L + t0 + 32 * r) * nh + h;
+                for (int i = 0; i < 32 && 32 * r + i < n; ++i) d16[(int64_t)i * nh] = __float2bfloat16_rn(v[i]);
+            }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 acc += a * v[i];
@@ -512,21 +521,22 @@ unsigned cumsum_ctas(const Problem &pr)
 }
 
 cudaError_t launch_chunk_cumsum(const Problem &pr, const void *dt, const float *A, float *G,
-                                float *dtT, int64_t dtT_lo, int64_t dtT_hi, cudaStream_t st, unsigned *count)
+                                float *dtT, int64_t dtT_lo, int64_t dtT_hi, cudaStream_t st, unsigned *count,
+                                __nv_bfloat16 *dt16)
 {
     dim3 grid((unsigned)pr.nc, (unsigned)((pr.nh + 31) / 32), (unsigned)pr.B);
     const size_t smem = sizeof(float) * 33 * (size_t)pr.T * (dtT ? 2 : 1);
     cudaError_t e;
-    if (pr.in_dt == SSD_BF16) {
+    if (pr.in_dt == SSD_BF16 && !pr.dt_f32) {
         auto kern = k_chunk_cumsum<__nv_bfloat16>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
         kern<<<grid, 256, smem, st>>>((const __nv_bfloat16 *)dt, A, G, dtT, dtT_lo, dtT_hi, pr.L, (int)pr.nh, (int)pr.T,
-                                      count);
+                                      count, nullptr);
     } else {
         auto kern = k_chunk_cumsum<float>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
         kern<<<grid, 256, smem, st>>>((const float *)dt, A, G, dtT, dtT_lo, dtT_hi, pr.L, (int)pr.nh, (int)pr.T,
-                                      count);
+                                      count, dt16);
     }
     return cudaGetLastError();
 }

@@ -93,8 +93,9 @@ class Inputs:
         return dict(x=self.x, dt=self.dt, A=self.A, B=self.B, C=self.C, D=self.D, h0=self.h0)
 
 
-def make_inputs(shape: Shape, seed: Optional[int] = None) -> Inputs:
-    """Draw one workload on the CPU (deterministic for a given seed)."""
+def make_inputs(shape: Shape, seed: Optional[int] = None, dt_dtype: Optional[str] = None) -> Inputs:
+    """Draw one workload on the CPU (deterministic for a given seed).  dt_dtype ("f32" or
+    "bf16") overrides the dtype dt is cast to (by default the shape's input dtype)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(shape.seed if seed is None else seed)
     Bsz, L, nh, H, S, G = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate, shape.ngroups
@@ -130,7 +131,7 @@ def make_inputs(shape: Shape, seed: Optional[int] = None) -> Inputs:
         for b in range(Bsz):
             idx = torch.randperm(L, generator=g)[:nz]
             dt[b, idx, :] = 0.0
-    dt = dt.to(dt_)
+    dt = dt.to(torch_dtype(dt_dtype) if dt_dtype else dt_)
     return Inputs(shape, x.contiguous(), dt.contiguous(), A.contiguous(), Bm.contiguous(),
                   Cm.contiguous(), D.contiguous(), None if h0 is None else h0.contiguous())
 

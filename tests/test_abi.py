@@ -46,7 +46,7 @@ def test_status_strings(lib):
 def desc(**kw):
     d = _native.Desc()
     base = dict(batch=2, seqlen=512, nheads=8, headdim=64, dstate=128, ngroups=2, chunk=256,
-                in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16, flags=0, reserved=0)
+                in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16, flags=0, dt_dtype=0)
     base.update(kw)
     for k, v in base.items():
         setattr(d, k, v)
@@ -76,7 +76,7 @@ def test_workspace_size_arithmetic(lib):
 @pytest.mark.parametrize("bad,code", [
     (dict(ngroups=3), 1), (dict(nheads=-1), 1), (dict(headdim=0), 1), (dict(dstate=0), 1),
     (dict(chunk=0), 1), (dict(seqlen=-5), 1), (dict(in_dtype=7), 1), (dict(out_dtype=-1), 1),
-    (dict(flags=1 << 8), 1), (dict(reserved=1), 1),
+    (dict(flags=1 << 8), 1), (dict(dt_dtype=2), 1), (dict(dt_dtype=-1), 1),
     (dict(dstate=257), 2), (dict(headdim=2048), 2), (dict(chunk=4096), 2),
 ])
 def test_bad_descriptors_rejected(lib, bad, code):
@@ -267,3 +267,26 @@ def test_s6_argument_validation(lib):
     # nothing to do: no batch rows, or no tokens and no final state requested
     assert lib.ssd_s6_fwd(ctypes.byref(s6desc(batch=0)), *args) == 0
     assert lib.ssd_s6_fwd(ctypes.byref(s6desc(seqlen=0)), *args) == 0
+
+
+def test_float32_dt_beside_bfloat16_inputs(lib):
+    """SSD_DT_FLOAT32: the forward pass takes it (its workspace grows by a bfloat16 copy of dt);
+    the entry points that read dt directly after the cumsum refuse it."""
+    base, f32dt = desc(), desc(dt_dtype=_native.SSD_DT_FLOAT32)
+    nb, nf = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(base), ctypes.byref(nb)) == 0
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(f32dt), ctypes.byref(nf)) == 0
+    copy = 2 * 512 * 8 * 2                      # B * L * nh bfloat16
+    assert nf.value - nb.value == (copy + 255) // 256 * 256
+    p = _native.Plan()
+    assert lib.ssd_fwd_plan(ctypes.byref(f32dt), ctypes.byref(p)) == 0 and p.tensor_cores == 1
+    fake = 1 << 20   # refused before any pointer is used
+    assert lib.ssd_step(ctypes.byref(f32dt), fake, fake, fake, fake, fake, fake, fake, fake, None) == 2
+    assert lib.ssd_bwd_workspace_size(ctypes.byref(f32dt), ctypes.byref(nb)) == 2
+    assert lib.ssd_chunk_state(ctypes.byref(f32dt), fake, fake, fake, fake, fake, None) == 2
+    assert lib.ssd_chunk_scan(ctypes.byref(f32dt), fake, fake, fake, fake, fake, fake, fake, fake, None) == 2
+    # with float32 inputs the field changes nothing
+    f = desc(in_dtype=_native.SSD_F32, out_dtype=_native.SSD_F32)
+    g = desc(in_dtype=_native.SSD_F32, out_dtype=_native.SSD_F32, dt_dtype=_native.SSD_DT_FLOAT32)
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(f), ctypes.byref(nb)) == 0
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(g), ctypes.byref(nf)) == 0 and nb.value == nf.value
