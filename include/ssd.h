@@ -157,7 +157,11 @@ ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan);
  * order, so results may differ between calls at the level of float rounding.
  * The work is ordered on `stream` like any other stream work; inside the call
  * the kernels after the first use programmatic dependent launch (each starts
- * while the previous one finishes and waits for its results). */
+ * while the previous one finishes and waits for its results).
+ * dt is the positive step (the softplus output) and must be >= 0; it is not
+ * scanned for sign.  A negative dt gives NaN outputs on the tensor-core path
+ * (which evaluates the in-chunk decay times dt as one exp2 of G - log2 dt) and
+ * is carried through the recurrence as written on the CUDA-core path. */
 ssd_status ssd_fwd(const ssd_desc *desc, const void *x, const void *dt, const float *A,
                    const void *Bm, const void *Cm, const float *D, const float *h0, void *y,
                    float *h_final, void *workspace, size_t ws_bytes, ssd_stream_t stream);
