@@ -182,6 +182,28 @@ ssd_status ssd_fwd_timed(const ssd_desc *desc, const void *x, const void *dt, co
  * in the workspace's error word instead of hanging. */
 ssd_status ssd_fwd_check(const void *workspace, ssd_stream_t stream);
 
+/* Forward pass on inputs and outputs in host memory (a convenience over ssd_fwd for callers
+ * that hold them on the host; no counterpart on the pages).  x, dt, A, Bm, Cm, D, h0 (nullable)
+ * are read from host memory and y, h_final (nullable) written to host memory, in the layouts
+ * of ssd_fwd; page-locked host memory lets the copies run asynchronously.  The batch is cut
+ * into up to 8 slices of whole batch rows: the library's two copy streams (one per direction,
+ * one pair per device, created on first use) move slice k in and out while the forward pass
+ * of the others runs on `stream`, so copies and computation overlap.  device_buffer: caller-
+ * owned device memory of ssd_fwd_host_buffer_size() bytes, 256-byte aligned (inputs, outputs,
+ * workspace; nothing is allocated).  The call only enqueues: `stream` reaches the point after
+ * the outputs are in host memory once it is done, and the host buffers must stay valid until
+ * then.  Calls on one device are enqueued under a lock; a call's copies start after all work
+ * enqueued on `stream` before it.  Errors: those of ssd_fwd; SSD_ERR_WORKSPACE for a missing,
+ * misaligned or short device_buffer. */
+ssd_status ssd_fwd_host_buffer_size(const ssd_desc *desc, size_t *bytes);
+ssd_status ssd_fwd_host(const ssd_desc *desc, const void *x, const void *dt, const float *A,
+                        const void *Bm, const void *Cm, const float *D, const float *h0,
+                        void *y, float *h_final, void *device_buffer, size_t buffer_bytes,
+                        ssd_stream_t stream);
+/* The ssd_fwd_check of ssd_fwd_host: synchronises `stream` and reports SSD_ERR_TIMEOUT if a
+ * bounded device-side wait expired in any slice of the last call on device_buffer. */
+ssd_status ssd_fwd_host_check(const void *device_buffer, ssd_stream_t stream);
+
 /* One recurrent decode step for every (batch, head) (blog section "Mamba-2
  * architecture": the recurrent form suits sequential inference).
  * desc.seqlen and desc.chunk are ignored.  Layouts:

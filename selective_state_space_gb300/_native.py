@@ -22,7 +22,8 @@ EXPORTS = ("ssd_status_string", "ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_f
            "ssd_fwd_check",
            "ssd_step",
            "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_bwd_workspace_size",
-           "ssd_bwd", "ssd_s6_fwd", "ssd_fwd_noalloc", "ssd_fwd_noalloc_check")
+           "ssd_bwd", "ssd_s6_fwd", "ssd_fwd_noalloc", "ssd_fwd_noalloc_check", "ssd_fwd_host_buffer_size",
+           "ssd_fwd_host", "ssd_fwd_host_check")
 
 
 class Desc(ctypes.Structure):
@@ -93,6 +94,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ssd_fwd_noalloc.restype = st
         lib.ssd_fwd_noalloc_check.argtypes = [P]
         lib.ssd_fwd_noalloc_check.restype = st
+        lib.ssd_fwd_host_buffer_size.argtypes = [DP, ctypes.POINTER(ctypes.c_size_t)]
+        lib.ssd_fwd_host_buffer_size.restype = st
+        lib.ssd_fwd_host.argtypes = [DP] + [P] * 10 + [ctypes.c_size_t, P]
+        lib.ssd_fwd_host.restype = st
+        lib.ssd_fwd_host_check.argtypes = [P, P]
+        lib.ssd_fwd_host_check.restype = st
         lib.ssd_bwd_workspace_size.argtypes = [DP, ctypes.POINTER(ctypes.c_size_t)]
         lib.ssd_bwd_workspace_size.restype = st
         lib.ssd_bwd.argtypes = [DP] + [P] * 17 + [ctypes.c_size_t, P]

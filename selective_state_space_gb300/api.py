@@ -124,6 +124,40 @@ def ssd_fwd(x, dt, A, B, C, D, chunk: int, h0=None, *, y=None, h_final=None, wan
     return y, h_final
 
 
+def host_buffer_size(desc: Desc) -> int:
+    n = ctypes.c_size_t(0)
+    check("ssd_fwd_host_buffer_size",
+          _native.load().ssd_fwd_host_buffer_size(ctypes.byref(desc), ctypes.byref(n)))
+    return int(n.value)
+
+
+def _host_ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("ssd_fwd_host takes host tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def ssd_fwd_host(x, dt, A, B, C, D, chunk: int, h0=None, *, y, h_final=None, device_buffer, out_dtype=None,
+                 flags: int = 0, stream=None, check_errors: bool = False):
+    """Chunked SSD forward on host tensors (ssd_fwd_host): inputs read from, y and h_final
+    written to host memory (pinned memory lets the copies overlap the computation);
+    ``device_buffer`` is a device tensor of ``host_buffer_size(desc)`` bytes.  Only enqueues
+    on ``stream``; synchronise it (or pass ``check_errors``) before reading y."""
+    desc = desc_for(x, B, chunk, out_dtype, flags, dt)
+    lib = _native.load()
+    check("ssd_fwd_host", lib.ssd_fwd_host(ctypes.byref(desc), _host_ptr(x), _host_ptr(dt), _host_ptr(A),
+                                           _host_ptr(B), _host_ptr(C), _host_ptr(D), _host_ptr(h0), _host_ptr(y),
+                                           _host_ptr(h_final), _ptr(device_buffer), device_buffer.numel(),
+                                           _stream(stream)))
+    if check_errors:
+        check("ssd_fwd_host_check", lib.ssd_fwd_host_check(_ptr(device_buffer), _stream(stream)))
+    return y, h_final
+
+
 def ssd_step(x, dt, A, B, C, D, h, *, y=None, out_dtype=None, stream=None):
     """One decode step.  x [B,nh,H], dt [B,nh], B/C [B,G,S], h [B,nh,H,S] float32 (updated in place).
     Returns y [B,nh,H]."""

@@ -311,6 +311,134 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
 
 bool nonempty(const Problem &pr) { return pr.B > 0 && pr.nh > 0 && pr.L > 0; }
 
+// ---- forward pass on host buffers (ssd_fwd_host) -------------------------------------------
+// The problem is cut into up to kHostParts slices: runs of whole batch rows when there are
+// enough rows, else token ranges of whole chunks within each row (a row's ranges run in order;
+// each range enters from the state the one before it left, through the device buffer).  Slice
+// k's inputs go to the device on the library's copy-in stream, its forward pass runs on the
+// caller's stream once they have landed, and its outputs come back on the copy-out stream once
+// it is done: the copies of one slice overlap the computation and the copies of the others.
+// Every slice has its own 256-byte-aligned device regions (a slice of dt need not start on a
+// 16-byte boundary in a packed layout); the slices share one workspace.  Device buffer:
+// [error words of the slices | A | D | per slice: x, dt, B, C, h0, y, h_final | workspace].
+constexpr int kHostParts = 16;    // the most slices (error words, events)
+constexpr int kHostTarget = 8;    // slices aimed at: each one costs about 20 API calls to enqueue
+
+struct HostLayout {
+    int64_t parts = 0;                       // slices
+    int64_t rows = 0, toks = 0;              // batch rows and tokens of a full slice
+    int64_t ranges = 1;                      // token ranges per row (1: slices of whole rows)
+    size_t a = 0, d = 0, slice0 = 0, slice = 0, ws = 0, ws_bytes = 0, bytes = 0;
+    size_t x = 0, dt = 0, bm = 0, cm = 0, h0 = 0, y = 0, hf = 0;   // offsets inside a slice
+    size_t x_t = 0, dt_t = 0, bc_t = 0, y_t = 0, st_b = 0;          // bytes per token (of one row), per state
+};
+
+// Slice k: batch rows [b0, b0 + nb), tokens [t0, t0 + nt).
+struct HostSlice {
+    int64_t b0, nb, t0, nt;
+};
+
+HostSlice host_slice(const HostLayout &h, const Problem &pr, int64_t k)
+{
+    if (h.ranges == 1) {
+        const int64_t b0 = k * h.rows;
+        return HostSlice{b0, std::min<int64_t>(h.rows, pr.B - b0), 0, pr.L};
+    }
+    const int64_t b0 = k / h.ranges, t0 = (k % h.ranges) * h.toks;
+    return HostSlice{b0, 1, t0, std::min<int64_t>(h.toks, pr.L - t0)};
+}
+
+HostLayout host_layout(const ssd_desc *desc, const Problem &pr)
+{
+    HostLayout h;
+    // whole rows once there are a few of them (a token range costs its row's state hand-off and
+    // another round of launches; with 4 rows of the 2.7B-shaped layer, 4 row slices measured
+    // 1.51 ms per call against 1.54 ms for 8 ranges)
+    if (pr.B >= kHostTarget / 2 || pr.L <= pr.T) {
+        h.parts = std::min<int64_t>(pr.B, kHostTarget);
+        h.rows = h.parts > 0 ? (pr.B + h.parts - 1) / h.parts : 0;
+        if (h.rows > 0) h.parts = (pr.B + h.rows - 1) / h.rows;
+        h.toks = pr.L;
+    } else {
+        // each row in ranges of whole chunks, about kHostTarget slices in all
+        const int64_t want = std::max<int64_t>(1, kHostTarget / pr.B);
+        h.toks = std::max<int64_t>(1, (pr.L + want - 1) / want);
+        h.toks = (h.toks + pr.T - 1) / pr.T * pr.T;
+        h.ranges = (pr.L + h.toks - 1) / h.toks;
+        h.rows = 1;
+        h.parts = pr.B * h.ranges;
+    }
+    const size_t es = esize(pr.in_dt), eo = esize(pr.out_dt), ed = pr.dt_f32 ? 4 : es;
+    h.x_t = (size_t)(pr.nh * pr.H) * es;
+    h.dt_t = (size_t)pr.nh * ed;
+    h.bc_t = (size_t)(pr.G * pr.S) * es;
+    h.y_t = (size_t)(pr.nh * pr.H) * eo;
+    h.st_b = (size_t)(pr.nh * pr.H * pr.S) * sizeof(float);
+    const size_t nt = (size_t)(h.rows * h.toks), nr = (size_t)h.rows;
+    size_t o = 0;
+    h.x = o;  o += align_up(nt * h.x_t, kWsAlign);
+    h.dt = o; o += align_up(nt * h.dt_t, kWsAlign);
+    h.bm = o; o += align_up(nt * h.bc_t, kWsAlign);
+    h.cm = o; o += align_up(nt * h.bc_t, kWsAlign);
+    h.h0 = o; o += align_up(nr * h.st_b, kWsAlign);
+    h.y = o;  o += align_up(nt * h.y_t, kWsAlign);
+    h.hf = o; o += align_up(nr * h.st_b, kWsAlign);
+    h.slice = o;
+    h.a = kWsAlign;                                        // after the slices' error words
+    h.d = h.a + align_up((size_t)pr.nh * sizeof(float), kWsAlign);
+    h.slice0 = h.d + align_up((size_t)pr.nh * sizeof(float), kWsAlign);
+    h.ws = h.slice0 + (size_t)h.parts * h.slice;
+    ssd_desc sub = *desc;
+    sub.batch = h.rows;
+    sub.seqlen = h.toks;
+    Problem ps;
+    if (h.rows > 0 && check_desc(&sub, &ps, true) == SSD_OK && nonempty(ps)) h.ws_bytes = carve(ps, nullptr).bytes;
+    h.bytes = h.ws + h.ws_bytes;
+    return h;
+}
+
+// The copy streams of ssd_fwd_host and their events, one set per device, created on first use.
+// Callers hold host_mutex() while they enqueue.
+struct HostStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, landed[kHostParts] = {}, done[kHostParts] = {};
+};
+
+std::mutex &host_mutex()
+{
+    static std::mutex mu;
+    return mu;
+}
+
+HostStreams *host_streams()
+{
+    static HostStreams cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    HostStreams &r = cache[dev];
+    if (r.join) return &r;
+    HostStreams n;
+    bool ok = cudaStreamCreateWithFlags(&n.in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&n.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) == cudaSuccess;
+    for (int k = 0; ok && k < kHostParts; ++k)
+        ok = cudaEventCreateWithFlags(&n.landed[k], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&n.done[k], cudaEventDisableTiming) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        for (cudaStream_t s : {n.in, n.out})
+            if (s) cudaStreamDestroy(s);
+        for (cudaEvent_t e : {n.fork, n.join})
+            if (e) cudaEventDestroy(e);
+        for (int k = 0; k < kHostParts; ++k)
+            for (cudaEvent_t e : {n.landed[k], n.done[k]})
+                if (e) cudaEventDestroy(e);
+        return nullptr;
+    }
+    r = n;
+    return &r;
+}
+
 }  // namespace
 
 extern "C" {
@@ -410,6 +538,123 @@ ssd_status ssd_fwd_timed(const ssd_desc *desc, const void *x, const void *dt, co
         if (!events[i]) return SSD_ERR_INVALID_ARG;
     return fwd_impl(desc, x, dt, A, Bm, Cm, D, h0, y, h_final, workspace, ws_bytes,
                     (cudaStream_t)stream, events);
+}
+
+ssd_status ssd_fwd_host_buffer_size(const ssd_desc *desc, size_t *bytes)
+{
+    Problem pr;
+    if (!bytes) return SSD_ERR_INVALID_ARG;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    *bytes = host_layout(desc, pr).bytes;
+    return SSD_OK;
+}
+
+ssd_status ssd_fwd_host(const ssd_desc *desc, const void *x, const void *dt, const float *A, const void *Bm,
+                        const void *Cm, const float *D, const float *h0, void *y, float *h_final, void *device_buffer,
+                        size_t buffer_bytes, ssd_stream_t stream)
+{
+    Problem pr;
+    ssd_status s = check_desc(desc, &pr, true);
+    if (s != SSD_OK) return s;
+    const HostLayout h = host_layout(desc, pr);
+    if (!device_buffer || !aligned(device_buffer, kWsAlign) || buffer_bytes < h.bytes) return SSD_ERR_WORKSPACE;
+    const bool empty = !nonempty(pr);
+    if (!empty && (!x || !dt || !A || !Bm || !Cm || !D || !y)) return SSD_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    char *base = (char *)device_buffer;
+    int *errs = (int *)base;
+    if (cudaMemsetAsync(errs, 0, kHostParts * sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
+    if (empty) {
+        // nothing to scan: h_final is h0 (zeros if absent), through the slices' state regions
+        if (!h_final || h.st_b == 0) return SSD_OK;
+        for (int64_t k = 0; k < h.parts; ++k) {
+            const HostSlice c = host_slice(h, pr, k);
+            const size_t n = (size_t)c.nb * h.st_b;
+            char *hf_d = base + h.slice0 + (size_t)k * h.slice + h.hf;
+            cudaError_t e = h0 ? cudaMemcpyAsync(hf_d, (const char *)h0 + (size_t)c.b0 * h.st_b, n,
+                                                 cudaMemcpyHostToDevice, st)
+                               : cudaMemsetAsync(hf_d, 0, n, st);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync((char *)h_final + (size_t)c.b0 * h.st_b, hf_d, n, cudaMemcpyDeviceToHost, st);
+            if (e != cudaSuccess) return SSD_ERR_CUDA;
+        }
+        return SSD_OK;
+    }
+    std::lock_guard<std::mutex> lock(host_mutex());
+    HostStreams *hs = host_streams();
+    if (!hs) return SSD_ERR_CUDA;
+    float *A_d = (float *)(base + h.a), *D_d = (float *)(base + h.d);
+    void *ws = base + h.ws;
+    auto H2D = [&](void *dst, const void *src, size_t n) {
+        return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, hs->in) == cudaSuccess;
+    };
+    auto D2H = [&](void *dst, const void *src, size_t n) {
+        return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, hs->out) == cudaSuccess;
+    };
+    // the copy streams start after everything enqueued on the caller's stream so far
+    if (cudaEventRecord(hs->fork, st) != cudaSuccess || cudaStreamWaitEvent(hs->in, hs->fork, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hs->out, hs->fork, 0) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (!H2D(A_d, A, (size_t)pr.nh * sizeof(float)) || !H2D(D_d, D, (size_t)pr.nh * sizeof(float)))
+        return SSD_ERR_CUDA;
+    // host offset of token t0 of batch row b0, for an array of `per_token` bytes per (row, token)
+    auto hoff = [&](const HostSlice &c, size_t per_token) { return ((size_t)c.b0 * pr.L + c.t0) * per_token; };
+    for (int64_t k = 0; k < h.parts; ++k) {
+        const HostSlice c = host_slice(h, pr, k);
+        char *r = base + h.slice0 + (size_t)k * h.slice;
+        const size_t nt = (size_t)(c.nb * c.nt);
+        if (!H2D(r + h.x, (const char *)x + hoff(c, h.x_t), nt * h.x_t) ||
+            !H2D(r + h.dt, (const char *)dt + hoff(c, h.dt_t), nt * h.dt_t) ||
+            !H2D(r + h.bm, (const char *)Bm + hoff(c, h.bc_t), nt * h.bc_t) ||
+            !H2D(r + h.cm, (const char *)Cm + hoff(c, h.bc_t), nt * h.bc_t) ||
+            (h0 && c.t0 == 0 && !H2D(r + h.h0, (const char *)h0 + (size_t)c.b0 * h.st_b, (size_t)c.nb * h.st_b)) ||
+            cudaEventRecord(hs->landed[k], hs->in) != cudaSuccess)
+            return SSD_ERR_CUDA;
+    }
+    for (int64_t k = 0; k < h.parts; ++k) {
+        const HostSlice c = host_slice(h, pr, k);
+        char *r = base + h.slice0 + (size_t)k * h.slice;
+        const size_t nt = (size_t)(c.nb * c.nt);
+        const bool row_end = c.t0 + c.nt == pr.L;
+        // a range after the first of its row enters from the state the range before it left
+        const float *h0_d = c.t0 > 0 ? (const float *)(base + h.slice0 + (size_t)(k - 1) * h.slice + h.hf)
+                                     : (h0 ? (const float *)(r + h.h0) : nullptr);
+        float *hf_d = (h_final || !row_end) ? (float *)(r + h.hf) : nullptr;
+        ssd_desc sub = *desc;
+        sub.batch = c.nb;
+        sub.seqlen = c.nt;
+        if (cudaStreamWaitEvent(st, hs->landed[k], 0) != cudaSuccess) return SSD_ERR_CUDA;
+        s = fwd_impl(&sub, r + h.x, r + h.dt, A_d, r + h.bm, r + h.cm, D_d, h0_d, r + h.y, hf_d, ws, h.ws_bytes, st,
+                     nullptr);
+        if (s != SSD_OK) return s;
+        // keep this slice's error word: the next slice clears the workspace's
+        if (cudaMemcpyAsync(errs + k, ws, sizeof(int), cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+            cudaEventRecord(hs->done[k], st) != cudaSuccess)
+            return SSD_ERR_CUDA;
+        if (cudaStreamWaitEvent(hs->out, hs->done[k], 0) != cudaSuccess ||
+            !D2H((char *)y + hoff(c, h.y_t), r + h.y, nt * h.y_t) ||
+            (h_final && row_end &&
+             !D2H((char *)h_final + (size_t)c.b0 * h.st_b, r + h.hf, (size_t)c.nb * h.st_b)))
+            return SSD_ERR_CUDA;
+    }
+    // the caller's stream continues once the outputs are back in host memory
+    if (cudaEventRecord(hs->join, hs->out) != cudaSuccess || cudaStreamWaitEvent(st, hs->join, 0) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    return SSD_OK;
+}
+
+ssd_status ssd_fwd_host_check(const void *device_buffer, ssd_stream_t stream)
+{
+    if (!device_buffer || !aligned(device_buffer, kWsAlign)) return SSD_ERR_INVALID_ARG;
+    int words[kHostParts] = {0};
+    if (cudaMemcpyAsync(words, device_buffer, sizeof(words), cudaMemcpyDeviceToHost, (cudaStream_t)stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    for (int w : words)
+        if (w) return SSD_ERR_TIMEOUT;
+    return SSD_OK;
 }
 
 ssd_status ssd_fwd_check(const void *workspace, ssd_stream_t stream)

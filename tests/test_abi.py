@@ -290,3 +290,23 @@ def test_float32_dt_beside_bfloat16_inputs(lib):
     g = desc(in_dtype=_native.SSD_F32, out_dtype=_native.SSD_F32, dt_dtype=_native.SSD_DT_FLOAT32)
     assert lib.ssd_fwd_workspace_size(ctypes.byref(f), ctypes.byref(nb)) == 0
     assert lib.ssd_fwd_workspace_size(ctypes.byref(g), ctypes.byref(nf)) == 0 and nb.value == nf.value
+
+
+def test_host_buffer_size(lib):
+    """ssd_fwd_host_buffer_size: host-side query; grows with the batch, covers the device path's
+    workspace for one slice, and rejects what ssd_fwd rejects."""
+    n1, n4, nw = ctypes.c_size_t(0), ctypes.c_size_t(0), ctypes.c_size_t(0)
+    d1, d4 = desc(batch=1), desc(batch=4)
+    assert lib.ssd_fwd_host_buffer_size(ctypes.byref(d1), ctypes.byref(n1)) == 0
+    assert lib.ssd_fwd_host_buffer_size(ctypes.byref(d4), ctypes.byref(n4)) == 0
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(d1), ctypes.byref(nw)) == 0
+    x_bytes = 512 * 8 * 64 * 2
+    assert n1.value >= nw.value + 2 * x_bytes          # the slice's workspace, x and y at least
+    assert n4.value >= 4 * 2 * x_bytes + nw.value       # four one-row slices and one slice's workspace
+    assert lib.ssd_fwd_host_buffer_size(ctypes.byref(desc(ngroups=3)), ctypes.byref(n1)) == 1
+    assert lib.ssd_fwd_host_buffer_size(ctypes.byref(d1), None) == 1
+    # a buffer that is too short is refused before anything is enqueued
+    fake = 1 << 20
+    assert lib.ssd_fwd_host(ctypes.byref(d1), fake, fake, fake, fake, fake, fake, None, fake, None, 1 << 21, 16,
+                            None) == 3
+
