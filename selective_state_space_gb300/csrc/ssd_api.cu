@@ -331,6 +331,10 @@ struct HostLayout {
     size_t a = 0, d = 0, slice0 = 0, slice = 0, ws = 0, ws_bytes = 0, bytes = 0;
     size_t x = 0, dt = 0, bm = 0, cm = 0, h0 = 0, y = 0, hf = 0;   // offsets inside a slice
     size_t x_t = 0, dt_t = 0, bc_t = 0, y_t = 0, st_b = 0;          // bytes per token (of one row), per state
+    // small inputs copied in whole, in one copy each before the slices (every slice's part of
+    // them then starts on a 16-byte boundary): dt, B and C, h0; their regions
+    bool m_dt = false, m_bc = false, m_h0 = false;
+    size_t dt_all = 0, b_all = 0, c_all = 0, h0_all = 0;
 };
 
 // Slice k: batch rows [b0, b0 + nb), tokens [t0, t0 + nt).
@@ -351,10 +355,9 @@ HostSlice host_slice(const HostLayout &h, const Problem &pr, int64_t k)
 HostLayout host_layout(const ssd_desc *desc, const Problem &pr)
 {
     HostLayout h;
-    // whole rows once there are a few of them (a token range costs its row's state hand-off and
-    // another round of launches; with 4 rows of the 2.7B-shaped layer, 4 row slices measured
-    // 1.51 ms per call against 1.54 ms for 8 ranges)
-    if (pr.B >= kHostTarget / 2 || pr.L <= pr.T) {
+    // whole rows when there are enough of them, else token ranges (the 2.7B-shaped layer, 4 rows:
+    // 8 ranges measured 1.38 ms per call against 1.48 ms for 4 row slices)
+    if (pr.B >= kHostTarget || pr.L <= pr.T) {
         h.parts = std::min<int64_t>(pr.B, kHostTarget);
         h.rows = h.parts > 0 ? (pr.B + h.parts - 1) / h.parts : 0;
         if (h.rows > 0) h.parts = (pr.B + h.rows - 1) / h.rows;
@@ -388,6 +391,27 @@ HostLayout host_layout(const ssd_desc *desc, const Problem &pr)
     h.d = h.a + align_up((size_t)pr.nh * sizeof(float), kWsAlign);
     h.slice0 = h.d + align_up((size_t)pr.nh * sizeof(float), kWsAlign);
     h.ws = h.slice0 + (size_t)h.parts * h.slice;
+    // An input small next to x (a 16th of it at most) goes in one copy when every slice's part of
+    // it starts on a 16-byte boundary: each copy costs a few microseconds however small it is.
+    const size_t rows_t = (size_t)(pr.B * pr.L), x_all = rows_t * h.x_t;
+    auto slices_aligned = [&](size_t per_token) {
+        for (int64_t k = 0; k < h.parts; ++k) {
+            const HostSlice c = host_slice(h, pr, k);
+            if ((((size_t)c.b0 * pr.L + c.t0) * per_token) % 16 != 0) return false;
+        }
+        return true;
+    };
+    h.m_dt = rows_t * h.dt_t * 16 <= x_all && slices_aligned(h.dt_t);
+    h.m_bc = rows_t * h.bc_t * 16 <= x_all && slices_aligned(h.bc_t);
+    h.m_h0 = (size_t)pr.B * h.st_b * 16 <= x_all;          // h0 parts start at whole rows
+    size_t w = h.ws;
+    if (h.m_dt) { h.dt_all = w; w += align_up(rows_t * h.dt_t, kWsAlign); }
+    if (h.m_bc) {
+        h.b_all = w; w += align_up(rows_t * h.bc_t, kWsAlign);
+        h.c_all = w; w += align_up(rows_t * h.bc_t, kWsAlign);
+    }
+    if (h.m_h0) { h.h0_all = w; w += align_up((size_t)pr.B * h.st_b, kWsAlign); }
+    h.ws = w;
     ssd_desc sub = *desc;
     sub.batch = h.rows;
     sub.seqlen = h.toks;
@@ -600,15 +624,28 @@ ssd_status ssd_fwd_host(const ssd_desc *desc, const void *x, const void *dt, con
         return SSD_ERR_CUDA;
     // host offset of token t0 of batch row b0, for an array of `per_token` bytes per (row, token)
     auto hoff = [&](const HostSlice &c, size_t per_token) { return ((size_t)c.b0 * pr.L + c.t0) * per_token; };
+    const size_t rows_t = (size_t)(pr.B * pr.L);
+    if ((h.m_dt && !H2D(base + h.dt_all, dt, rows_t * h.dt_t)) ||
+        (h.m_bc && (!H2D(base + h.b_all, Bm, rows_t * h.bc_t) || !H2D(base + h.c_all, Cm, rows_t * h.bc_t))) ||
+        (h.m_h0 && h0 && !H2D(base + h.h0_all, h0, (size_t)pr.B * h.st_b)))
+        return SSD_ERR_CUDA;
+    // device addresses of slice k's inputs: its own regions, or its part of a whole copy
+    auto dt_of = [&](const HostSlice &c, char *r) { return h.m_dt ? base + h.dt_all + hoff(c, h.dt_t) : r + h.dt; };
+    auto b_of = [&](const HostSlice &c, char *r) { return h.m_bc ? base + h.b_all + hoff(c, h.bc_t) : r + h.bm; };
+    auto c_of = [&](const HostSlice &c, char *r) { return h.m_bc ? base + h.c_all + hoff(c, h.bc_t) : r + h.cm; };
+    auto h0_of = [&](const HostSlice &c, char *r) {
+        return h.m_h0 ? base + h.h0_all + (size_t)c.b0 * h.st_b : r + h.h0;
+    };
     for (int64_t k = 0; k < h.parts; ++k) {
         const HostSlice c = host_slice(h, pr, k);
         char *r = base + h.slice0 + (size_t)k * h.slice;
         const size_t nt = (size_t)(c.nb * c.nt);
         if (!H2D(r + h.x, (const char *)x + hoff(c, h.x_t), nt * h.x_t) ||
-            !H2D(r + h.dt, (const char *)dt + hoff(c, h.dt_t), nt * h.dt_t) ||
-            !H2D(r + h.bm, (const char *)Bm + hoff(c, h.bc_t), nt * h.bc_t) ||
-            !H2D(r + h.cm, (const char *)Cm + hoff(c, h.bc_t), nt * h.bc_t) ||
-            (h0 && c.t0 == 0 && !H2D(r + h.h0, (const char *)h0 + (size_t)c.b0 * h.st_b, (size_t)c.nb * h.st_b)) ||
+            (!h.m_dt && !H2D(r + h.dt, (const char *)dt + hoff(c, h.dt_t), nt * h.dt_t)) ||
+            (!h.m_bc && (!H2D(r + h.bm, (const char *)Bm + hoff(c, h.bc_t), nt * h.bc_t) ||
+                         !H2D(r + h.cm, (const char *)Cm + hoff(c, h.bc_t), nt * h.bc_t))) ||
+            (h0 && !h.m_h0 && c.t0 == 0 &&
+             !H2D(r + h.h0, (const char *)h0 + (size_t)c.b0 * h.st_b, (size_t)c.nb * h.st_b)) ||
             cudaEventRecord(hs->landed[k], hs->in) != cudaSuccess)
             return SSD_ERR_CUDA;
     }
@@ -619,14 +656,14 @@ ssd_status ssd_fwd_host(const ssd_desc *desc, const void *x, const void *dt, con
         const bool row_end = c.t0 + c.nt == pr.L;
         // a range after the first of its row enters from the state the range before it left
         const float *h0_d = c.t0 > 0 ? (const float *)(base + h.slice0 + (size_t)(k - 1) * h.slice + h.hf)
-                                     : (h0 ? (const float *)(r + h.h0) : nullptr);
+                                     : (h0 ? (const float *)h0_of(c, r) : nullptr);
         float *hf_d = (h_final || !row_end) ? (float *)(r + h.hf) : nullptr;
         ssd_desc sub = *desc;
         sub.batch = c.nb;
         sub.seqlen = c.nt;
         if (cudaStreamWaitEvent(st, hs->landed[k], 0) != cudaSuccess) return SSD_ERR_CUDA;
-        s = fwd_impl(&sub, r + h.x, r + h.dt, A_d, r + h.bm, r + h.cm, D_d, h0_d, r + h.y, hf_d, ws, h.ws_bytes, st,
-                     nullptr);
+        s = fwd_impl(&sub, r + h.x, dt_of(c, r), A_d, b_of(c, r), c_of(c, r), D_d, h0_d, r + h.y, hf_d, ws, h.ws_bytes,
+                     st, nullptr);
         if (s != SSD_OK) return s;
         // keep this slice's error word: the next slice clears the workspace's
         if (cudaMemcpyAsync(errs + k, ws, sizeof(int), cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
