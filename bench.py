@@ -856,7 +856,9 @@ def main():
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if tc else ("f32" if shape.dtype == "f32" else "f32 (bf16 inputs)"),
+        "vs_baseline": None,
+        "dtype": ("tf32 (float32 inputs)" if shape.dtype == "f32" else "bf16") if tc
+        else ("f32" if shape.dtype == "f32" else "f32 (bf16 inputs)"),
         "data": "synthetic", "config": dict(config_of(shape), parallelism=f"replicas{world}",
                                             tensor_cores=tc),
         "tflops": flops / (ms_per_step * 1e-3) / 1e12,

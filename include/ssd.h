@@ -98,7 +98,8 @@ typedef struct {
  * phase is already complete (the normal kernels wait up to 250 ms).  The call then winds
  * down without hanging -- each CTA still waits for the copies and MMAs it has issued
  * before it releases its tensor memory -- and ssd_fwd_check reports SSD_ERR_TIMEOUT; its
- * outputs are invalid.  The CUDA-core kernels have no such waits and ignore the flag.
+ * outputs are invalid.  The CUDA-core kernels have no such waits, and the float32 tensor-core
+ * kernel waits only for its own MMAs; both ignore the flag.
  * Never set it in production code. */
 #define SSD_FLAG_EXPIRE_WAITS 2
 

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libssd.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["ssd_api.cu", "ssd_simt.cu", "ssd_tc.cu", "ssd_bwd.cu", "s6_scan.cu"]
+SOURCES = ["ssd_api.cu", "ssd_simt.cu", "ssd_tc.cu", "ssd_tf32.cu", "ssd_bwd.cu", "s6_scan.cu"]
 
 
 def _nvcc() -> str:

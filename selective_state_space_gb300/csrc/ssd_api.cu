@@ -109,6 +109,12 @@ bool use_tensor_cores(const ssd_desc *desc, const Problem &pr)
     return !(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tc_supported(pr);
 }
 
+// The float32 inputs that the kind::tf32 kernel takes (one launch for the whole pass).
+bool use_tf32(const ssd_desc *desc, const Problem &pr)
+{
+    return !(desc->flags & SSD_FLAG_FORCE_SIMT) && ssd::tf32_supported(pr);
+}
+
 int device_sms()
 {
     static std::mutex mu;
@@ -242,6 +248,16 @@ ssd_status fwd_impl(const ssd_desc *desc, const void *x, const void *dt, const f
     if (!workspace || !aligned(workspace, kWsAlign) || ws_bytes < w.bytes) return SSD_ERR_WORKSPACE;
 
     auto rec = [&](int i) -> bool { return !events || cudaEventRecord((cudaEvent_t)events[i], st) == cudaSuccess; };
+    if (use_tf32(desc, pr)) {
+        // one launch: the kernel takes its own cumsum; the events of the first three stages
+        // bracket nothing
+        if (cudaMemsetAsync(w.err, 0, 2 * sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
+        for (int i = 0; i < 7; ++i)
+            if (!rec(i)) return SSD_ERR_CUDA;
+        if (ssd::launch_ssd_tf32(pr, x, dt, A, Bm, Cm, D, h0, y, h_final, w.err, st) != cudaSuccess || !rec(7))
+            return SSD_ERR_CUDA;
+        return SSD_OK;
+    }
     const bool tc = use_tensor_cores(desc, pr);
     // the error word and, next to it, the count of finished cumsum CTAs
     if (cudaMemsetAsync(w.err, 0, 2 * sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
@@ -497,7 +513,7 @@ ssd_status ssd_fwd_path(const ssd_desc *desc, int32_t *uses_tensor_cores)
     if (!uses_tensor_cores) return SSD_ERR_INVALID_ARG;
     ssd_status s = check_desc(desc, &pr, true);
     if (s != SSD_OK) return s;
-    *uses_tensor_cores = use_tensor_cores(desc, pr) ? 1 : 0;
+    *uses_tensor_cores = (use_tensor_cores(desc, pr) || use_tf32(desc, pr)) ? 1 : 0;
     return SSD_OK;
 }
 
@@ -508,7 +524,7 @@ ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan)
     ssd_status s = check_desc(desc, &pr, true);
     if (s != SSD_OK) return s;
     ssd_plan p = {};
-    p.tensor_cores = use_tensor_cores(desc, pr) ? 1 : 0;
+    p.tensor_cores = (use_tensor_cores(desc, pr) || use_tf32(desc, pr)) ? 1 : 0;
     if (pr.B == 0 || pr.nh == 0 || pr.L == 0) {
         // nothing to scan: at most one copy or memset of h_final, issued only if h_final is given
         p.super_tokens = (int32_t)std::min<int64_t>(pr.T, 0x7fffffff);
@@ -516,6 +532,16 @@ ssd_status ssd_fwd_plan(const ssd_desc *desc, ssd_plan *plan)
         return SSD_OK;
     }
     const int32_t nseq = (int32_t)(pr.B * pr.nh);
+    if (use_tf32(desc, pr)) {
+        // one launch, one CTA per sequence walking it whole
+        p.super_tokens = p.tail_super_tokens = (int32_t)pr.L;
+        p.n_super = p.tail_n_super = 1;
+        p.split_sequences = nseq;
+        p.kernel_launches = 1;
+        p.memsets = 1;
+        *plan = p;
+        return SSD_OK;
+    }
     if (p.tensor_cores) {        const ssd::ScanSplit sp = choose_tc_plan(pr);
         PlanPart parts[2];
         plan_parts(pr, sp, parts);

@@ -9,6 +9,14 @@ namespace ssd {
 // True when the tensor-core kernels handle this problem shape.
 bool tc_supported(const Problem &pr);
 
+// The float32 path on the tensor cores (kind::tf32; ssd_tf32.cu): float32 inputs, H = 64,
+// S = 64 or 128, L <= 1024.  One launch: one CTA per (batch, head) walks the sequence with
+// the state in TMEM, its own in-chunk cumsum included; `err` (nullable) receives error bits.
+bool tf32_supported(const Problem &pr);
+cudaError_t launch_ssd_tf32(const Problem &pr, const void *x, const void *dt, const float *A, const void *Bm,
+                            const void *Cm, const float *D, const float *h0, void *y, float *h_final, int *err,
+                            cudaStream_t st);
+
 // Heads per chunk_state CTA (the heads of one group that share its B tiles); a
 // sequence run given to launch_chunk_state_tc must start and end on a multiple of it.
 int state_heads_per_cta(const Problem &pr);

@@ -156,6 +156,12 @@ def test_fwd_plan_is_consistent(lib):
     assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0
     assert (p.tensor_cores, p.super_tokens, p.n_super, p.kernel_launches, p.memsets) == (0, T, nc, 4, 1)
     assert (p.split_sequences, p.tail_super_tokens, p.tail_n_super) == (nseq, T, nc)
+    # float32 inputs of H = 64, S <= 128: one kind::tf32 launch walking every sequence whole
+    d = desc(in_dtype=_native.SSD_F32, out_dtype=_native.SSD_F32, dstate=64, chunk=64)
+    assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0
+    assert (p.tensor_cores, p.n_super, p.super_tokens, p.kernel_launches, p.memsets) == (1, 1, 512, 1, 1)
+    d.flags = 1
+    assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0 and p.tensor_cores == 0
     # empty sequence: nothing launched
     d = desc(seqlen=0)
     assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0 and p.kernel_launches == 0

@@ -19,6 +19,7 @@ CASES = [
      _native.SSD_FLAG_FORCE_SIMT, None),
     (workloads.custom(2, 1024, 8, 64, 128, 2, 256, "bf16", seed=55, name="host-dt-f32"), 0, "f32"),
     (workloads.custom(2, 96, 4, 16, 32, 2, 32, "f32", h0_recipe="normal", seed=56, name="host-f32"), 0, None),
+    (workloads.custom(2, 300, 4, 64, 64, 1, 64, "f32", seed=60, name="host-tf32"), 0, None),
 ]
 
 

@@ -59,6 +59,12 @@ SMALL = [
     workloads.custom(1, 3001, 4, 64, 128, 1, 128, "bf16", h0_recipe="normal", seed=28, name="tc-ragged-odd"),
     workloads.custom(2, 77, 6, 8, 16, 3, 16, "f32", h0_recipe="normal", seed=15, name="odd-f32"),
     workloads.custom(1, 33, 2, 1, 1, 1, 1, "f32", seed=16, name="scalar-T1"),
+    # float32 inputs that take the kind::tf32 tensor-core kernel (H = 64, S = 64 or 128): ragged,
+    # several sub-chunks, chunks shorter and longer than its 128-token sub-chunk, G > 1, dt = 0
+    workloads.custom(2, 300, 4, 64, 64, 2, 64, "f32", h0_recipe="normal", seed=17, name="tf32-ragged"),
+    workloads.custom(1, 520, 2, 64, 128, 1, 32, "f32", seed=18, name="tf32-s128"),
+    workloads.custom(2, 384, 4, 64, 64, 1, 256, "f32", dt_zero_frac=0.1, h0_recipe="normal", seed=19,
+                     name="tf32-hold"),
 ]
 
 
@@ -66,7 +72,9 @@ def test_tensor_core_path_selected_for_bf16_layer_shapes():
     for shape in workloads.WORKLOADS[1:] + [workloads.BLOG_SHAPE]:
         assert tc_path(shape), shape.name
         assert not tc_path(shape, SSD_FLAG_FORCE_SIMT)
-    assert not tc_path(workloads.WORKLOADS[0])   # float32 inputs run on the CUDA cores
+    assert tc_path(workloads.WORKLOADS[0])       # float32 inputs of H = 64, S <= 128: kind::tf32
+    assert not tc_path(workloads.WORKLOADS[0], SSD_FLAG_FORCE_SIMT)
+    assert not tc_path(workloads.custom(1, 64, 2, 8, 16, 1, 16, "f32", name="f32-narrow"))
     # lengths that are not a multiple of the chunk stay on the tensor cores
     for shape in SMALL:
         if shape.name in ("c3-ragged", "c4-ragged", "tc-ragged-76", "tc-ragged-super", "tc-ragged-odd"):
