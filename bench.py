@@ -65,8 +65,8 @@ def stage_bytes(s: workloads.Shape, plan: dict):
     the intermediates it moves counted: G, the float32 dt copy, the super-chunk states and the
     super-chunk-start states, all float32; 0 for a stage that does not launch.  A plan cuts the
     sequences ((batch, head) pairs) in two parts; chunk_state and state_passing run per part and
-    their bytes are summed.  Also the whole-step compulsory I/O ("step": each input read once, each
-    output written once, intermediates excluded)."""
+    their bytes are summed.  Also the whole-step compulsory I/O ("step": each input read once,
+    each output written once, intermediates excluded)."""
     e = esize(s.dtype)
     Bsz, L, nh, H, S, G, T, nc = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups, s.chunk, s.nchunks
     x = Bsz * L * nh * H * e
@@ -844,7 +844,7 @@ def main():
     sb = stage_bytes(shape, plan)
     top = max(STAGES, key=lambda s_: stage_ms[s_] if sb[s_] else -1.0)
     kname = top
-    # SURVEY 8(d): the dominant kernel's algorithmic bytes are the compulsory I/O of the step --
+    # the dominant kernel's algorithmic bytes are the compulsory I/O of the step --
     # every input read once and every output written once, intermediates excluded (the scan reads
     # every input and writes every output of the step)
     alg_top = sb["step"]
