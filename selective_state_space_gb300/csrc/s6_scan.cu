@@ -10,11 +10,14 @@
 // Tiles of kTT tokens are staged through shared memory: rows of x and delta are
 // contiguous in time, so consecutive threads load consecutive tokens; B and C rows
 // of the group are shared by all channels of the block.  The next tile is loaded
-// into registers while the current one is scanned.  Each lane records its partial
-// sum of C h per token in shared memory; the output pass adds the kSplit partials
-// and D x and writes y coalesced, so the token loop carries no shuffle.  The scan
-// is bound by the special-function unit (one exp2 per channel, state and token)
-// once N >= 8.
+// into registers while the current one is scanned.  Tokens go kU at a time: every
+// shared-memory read of the group is issued first, then the recurrences run (two
+// states per paired float32 instruction when a lane holds an even number of them),
+// then each lane records its partial sums of C h in shared memory.  (Interleaving
+// those stores with the next token's reads would keep the reads behind them.)  The
+// output pass adds the kSplit partials and D x and writes y coalesced, so the token
+// loop carries no shuffle.  The scan is bound by the special-function unit (one exp2
+// per channel, state and token) once N >= 8.
 #include "ssd_common.cuh"
 
 namespace ssd {
@@ -35,8 +38,10 @@ __device__ __forceinline__ float fast_exp2(float v)
 }
 
 // Shared memory of one block (dynamic): the channel tile as (x, delta) pairs, the group's
-// (B, C) pairs per state, each lane's partial sum of C h per channel and token (the four
-// lanes of a channel write four different banks), and D of the block's channels.
+// B and C per state, each lane's partial sum of C h per channel and token (the four lanes of a
+// channel write four different banks), and D of the block's channels.  With an even number of
+// states per lane, B and C are stored per pair of states as (B_n, B_n+1, C_n, C_n+1), one
+// 16-byte read for two states; with one state per lane, as (B_n, C_n).
 template <int NS>
 struct S6Smem {
     static constexpr int NP = NS * kSplit;     // padded state count
@@ -55,10 +60,13 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
 {
     using Sm = S6Smem<NS>;
     constexpr int NP = Sm::NP;
+    constexpr bool kPair = NS % 2 == 0;                         // states taken two at a time
+    constexpr int NQ = kPair ? NS / 2 : NS;                     // (pairs of) states per lane
+    constexpr int kU = NS >= 8 ? 4 : 8;                         // tokens whose reads are issued together
     constexpr int kLb = (NP * kTT + kThreads - 1) / kThreads;   // B (and C) elements per thread per tile
     extern __shared__ float4 s6_smem[];
     float2 *xd = reinterpret_cast<float2 *>(s6_smem);          // [kCh][kXP]  (x, delta)
-    float2 *bc = xd + Sm::xd;                                   // [NP][kXP]   (B, C)
+    float2 *bc = xd + Sm::xd;                                   // [NP][kXP] (B, C), or [NP/2][kXP] float4 pairs
     float *yp = reinterpret_cast<float *>(bc + Sm::bc);         // [kCh][kSplit][kXP]
     float *dsk = yp + Sm::yp;                                   // [kCh]  D of the block's channels
     const int tid = threadIdx.x;
@@ -71,7 +79,7 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
     const Tin *Bg = Bm + ((int64_t)b * G + g) * N * L;
     const Tin *Cg = Cm + ((int64_t)b * G + g) * N * L;
 
-    // this thread's channel and states
+    // this thread's channel and states; with kPair, element q holds states 2q and 2q + 1
     const int ch = tid / kSplit, slice = tid % kSplit;
     const bool active = ch < nch;
     const int d = g * cpg + c0 + (active ? ch : 0);
@@ -83,7 +91,14 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
         a2[s] = on ? A[(int64_t)d * N + n] * kLog2e : 0.f;
         h[s] = (on && h0) ? h0[((int64_t)b * dim + d) * N + n] : 0.f;
     }
-
+    float2 hp[kPair ? NQ : 1], ap[kPair ? NQ : 1];
+    if constexpr (kPair) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            hp[q] = make_float2(h[2 * q], h[2 * q + 1]);
+            ap[q] = make_float2(a2[2 * q], a2[2 * q + 1]);
+        }
+    }
     // global -> registers for the tile starting at t0, kept in the input dtype: nothing consumes the
     // loads until stage() converts them, after the current tile's scan
     const Tin zero = from_f32<Tin>(0.f);
@@ -123,27 +138,76 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
 #pragma unroll
         for (int i = 0; i < kLb; ++i) {
             const int e = i * kThreads + tid, n = e / kTT, t = e % kTT;
-            if (e < NP * kTT) bc[n * kXP + t] = make_float2(to_f32(rb[i]), to_f32(rc[i]));
+            if (e < NP * kTT) {
+                if constexpr (kPair) {
+                    float *cell = reinterpret_cast<float *>(bc) + ((n >> 1) * kXP + t) * 4 + (n & 1);
+                    cell[0] = to_f32(rb[i]);
+                    cell[2] = to_f32(rc[i]);
+                } else {
+                    bc[n * kXP + t] = make_float2(to_f32(rb[i]), to_f32(rc[i]));
+                }
+            }
         }
     };
-    // one token: update this lane's states, record its partial sum of C h
     const float2 *xr = xd + ch * kXP;
-    const float2 *bcr = bc + (slice * NS) * kXP;
+    const float2 *bcr = bc + (slice * NS) * kXP;                                         // (B, C) rows
+    const float4 *bc4r = reinterpret_cast<const float4 *>(bc) + (slice * NQ) * kXP;      // pair rows
     float *ypr = yp + (ch * kSplit + slice) * kXP;
-    auto token = [&](int t) {
-        const float2 v = xr[t];
+    // one token: update this lane's states and return its partial sum of C h
+    auto step = [&](float2 v, const float4 *q4, const float2 *q2) {
         const float dx = v.y * v.x;
-        float acc = 0.f;
+        if constexpr (kPair) {
+            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int s = 0; s < NS; ++s) {
-            const float2 q = bcr[s * kXP + t];
-            const float abar = fast_exp2(v.y * a2[s]);
-            h[s] = fmaf(abar, h[s], dx * q.x);
-            acc = fmaf(q.y, h[s], acc);
+            for (int q = 0; q < NQ; ++q) {
+                const float2 e = __fmul2_rn(make_float2(v.y, v.y), ap[q]);
+                const float2 abar = make_float2(fast_exp2(e.x), fast_exp2(e.y));
+                hp[q] = __ffma2_rn(abar, hp[q], __fmul2_rn(make_float2(dx, dx), make_float2(q4[q].x, q4[q].y)));
+                acc = __ffma2_rn(make_float2(q4[q].z, q4[q].w), hp[q], acc);
+            }
+            return acc.x + acc.y;
+        } else {
+            float acc = 0.f;
+#pragma unroll
+            for (int s = 0; s < NS; ++s) {
+                const float abar = fast_exp2(v.y * a2[s]);
+                h[s] = fmaf(abar, h[s], dx * q2[s].x);
+                acc = fmaf(q2[s].y, h[s], acc);
+            }
+            return acc;
         }
-        ypr[t] = acc;
     };
-
+    // kU tokens from t: every shared-memory read first, then the recurrences, then the partial
+    // sums
+    auto tokens = [&](int t) {
+        float2 v[kU];
+        float4 q4[kPair ? kU : 1][kPair ? NQ : 1];
+        float2 q2[kPair ? 1 : kU][kPair ? 1 : NS];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            v[u] = xr[t + u];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                if constexpr (kPair) q4[u][q] = bc4r[q * kXP + t + u];
+                else q2[u][q] = bcr[q * kXP + t + u];
+            }
+        }
+        float acc[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) acc[u] = step(v[u], q4[kPair ? u : 0], q2[kPair ? 0 : u]);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) ypr[t + u] = acc[u];
+    };
+    auto token = [&](int t) {
+        float4 q4[kPair ? NQ : 1];
+        float2 q2[kPair ? 1 : NS];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            if constexpr (kPair) q4[q] = bc4r[q * kXP + t];
+            else q2[q] = bcr[q * kXP + t];
+        }
+        ypr[t] = step(xr[t], q4, q2);
+    };
     const int64_t ntiles = (L + kTT - 1) / kTT;
     if (tid < kCh) dsk[tid] = (D && tid < nch) ? D[g * cpg + c0 + tid] : 0.f;
     fetch(0);
@@ -154,8 +218,8 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
         if (k + 1 < ntiles) fetch(t0 + kTT);
         const int tn = (int)min((int64_t)kTT, L - t0);
         if (tn == kTT) {
-#pragma unroll 8
-            for (int t = 0; t < kTT; ++t) token(t);
+#pragma unroll 1
+            for (int t = 0; t < kTT; t += kU) tokens(t);
         } else {
             for (int t = 0; t < tn; ++t) token(t);
         }
@@ -181,7 +245,8 @@ k_s6_scan(const Tin *__restrict__ x, const Tin *__restrict__ delta, const float 
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
             const int n = slice * NS + s;
-            if (n < N) h_final[((int64_t)b * dim + d) * N + n] = h[s];
+            const float hv = kPair ? ((s & 1) ? hp[s >> 1].y : hp[s >> 1].x) : h[s];
+            if (n < N) h_final[((int64_t)b * dim + d) * N + n] = hv;
         }
     }
 }
