@@ -188,10 +188,14 @@ ssd::ScanSplit choose_tc_plan(const Problem &pr)
     int64_t tail = (last + per_row - 1) / per_row * spc;      // sequences of the last wave
     tail = (tail + align - 1) / align * align;
     if (tail >= nseq) return sp;
-    // the tail's chunks over all SMs, at least one chunk per super-chunk
+    // the tail's chunks over all SMs, at least two chunks per super-chunk where the first
+    // part's are longer: a scan CTA's start-up costs about two 128-token periods, so one-chunk
+    // super-chunks would nearly double the tail's time (B = 4, L = 4096, 80 heads of 64 x 128:
+    // 124.9 us per pass with two, 126.6 us with one, 126.3 us with four)
     const int64_t tail_chunks = tail / spc * (int64_t)pr.nc * npb;
     int R1 = (int)((tail_chunks + sms - 1) / sms);
     if (R1 < 1) R1 = 1;
+    if (R1 < 2 && R > 2) R1 = 2;
     if (R1 >= R) return sp;
     sp.split = nseq - tail;
     sp.R1 = R1;
