@@ -298,6 +298,24 @@ def test_float32_dt_beside_bfloat16_inputs(lib):
     assert lib.ssd_fwd_workspace_size(ctypes.byref(g), ctypes.byref(nf)) == 0 and nb.value == nf.value
 
 
+def test_tail_super_chunks_hold_two_chunks(lib):
+    """A plan that cuts the sequences of a nearly empty last wave into short super-chunks gives
+    them at least two chunks when the whole sequences' super-chunks are longer: a scan CTA's
+    start-up costs about two 128-token periods.  Host-side query (the SM count of the device, or
+    148 without one): with 80 heads of 64 x 128 and 256-token chunks, 160 head pairs leave a
+    short last wave on a GB300-sized part."""
+    P = _native.Plan
+    for seqlen in (1024, 2048, 4096):
+        d = desc(batch=4, seqlen=seqlen, nheads=80, headdim=64, dstate=128, ngroups=1, chunk=256,
+                 in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16)
+        p = P()
+        assert lib.ssd_fwd_plan(ctypes.byref(d), ctypes.byref(p)) == 0
+        if p.split_sequences == 4 * 80 or p.super_tokens <= 2 * 256:
+            continue                                   # no tail cut on this device, or nothing longer
+        assert p.tail_super_tokens >= 2 * 256, (seqlen, p.tail_super_tokens)
+        assert p.tail_super_tokens % 256 == 0 and p.tail_n_super * p.tail_super_tokens >= seqlen
+
+
 def test_host_buffer_size(lib):
     """ssd_fwd_host_buffer_size: host-side query; grows with the batch, covers the device path's
     workspace for one slice, and rejects what ssd_fwd rejects."""
