@@ -64,7 +64,8 @@ typedef enum { SSD_DT_AS_INPUTS = 0, SSD_DT_FLOAT32 = 1 } ssd_dt_dtype;
 typedef enum {
     SSD_OK = 0,
     SSD_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, negative size, bad dtype, G does not divide nh */
-    SSD_ERR_UNSUPPORTED = 2,  /* well-formed problem outside what this library handles (see limits below) */
+    SSD_ERR_UNSUPPORTED = 2,  /* well-formed problem outside what this library handles (see limits below;
+                                 every entry point: arrays of 2^62 bytes or more, whose sizes could wrap) */
     SSD_ERR_WORKSPACE = 3,    /* workspace NULL, smaller than ssd_fwd_workspace_size, or not 256-B aligned */
     SSD_ERR_CUDA = 4,         /* a CUDA runtime call or a kernel launch failed; call cudaGetLastError */
     SSD_ERR_TOO_LARGE = 5,    /* ssd_fwd_noalloc: the problem needs more scratch than SSD_NOALLOC_SCRATCH_BYTES */
@@ -283,7 +284,7 @@ ssd_status ssd_bwd(const ssd_desc *desc, const void *x, const void *dt, const fl
  *   Bm, Cm       [B][G][N][L]  in dtype                 D   [dim] float32, nullable (no skip)
  *   h0, h_final  [B][dim][N]   float32, nullable (zeros / not written)
  * delta is the positive step (no softplus or bias applied inside).
- * Limits: 1 <= N <= 32, G divides dim, B <= 65535.  Pointers aligned to their
+ * Limits: 1 <= N <= 32, G divides dim, B <= 65535, B * dim * L * N * 16 < 2^62.  Pointers aligned to their
  * element size; y must not overlap an input.  Deterministic. */
 typedef struct {
     int64_t batch;      /* B >= 0 */

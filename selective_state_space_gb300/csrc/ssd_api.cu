@@ -55,6 +55,15 @@ ssd_status check_desc(const ssd_desc *d, Problem *pr, bool need_seq)
     pr->dt_f32 = d->dt_dtype == SSD_DT_FLOAT32 && d->in_dtype == SSD_BF16;
     pr->wait_ns = (d->flags & SSD_FLAG_EXPIRE_WAITS) ? 0ull : 250000000ull;
     if (need_seq && pr->nc > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
+    // every array size (workspace, buffers, the offsets the kernels compute) is formed in 64-bit
+    // arithmetic: a problem whose largest arrays need 2^62 bytes or more is refused before any
+    // size is formed, so that no size can wrap around
+    const double lim = 4611686018427387904.0;   // 2^62
+    const double rows = (double)pr->B * (double)pr->L;
+    const double states = (double)pr->B * (double)pr->nh * (double)pr->nc * (double)pr->H * (double)pr->S;
+    if (16.0 * states >= lim || 16.0 * rows * (double)pr->nh * (double)pr->H >= lim ||
+        16.0 * rows * (double)pr->G * (double)pr->S >= lim)
+        return SSD_ERR_UNSUPPORTED;
     return SSD_OK;
 }
 
@@ -902,6 +911,10 @@ ssd_status ssd_s6_fwd(const ssd_s6_desc *desc, const void *x, const void *delta,
         (desc->out_dtype != SSD_F32 && desc->out_dtype != SSD_BF16))
         return SSD_ERR_INVALID_ARG;
     if (desc->dstate > 32 || desc->batch > 65535 || desc->dim > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
+    // the offsets the kernel forms are 64-bit: arrays of 2^62 bytes or more are refused
+    if (16.0 * (double)desc->batch * (double)desc->dim * (double)desc->seqlen * (double)desc->dstate >=
+        4611686018427387904.0)
+        return SSD_ERR_UNSUPPORTED;
     const ssd::S6Problem p{desc->batch, desc->seqlen, desc->dim, desc->dstate, desc->ngroups, desc->in_dtype,
                            desc->out_dtype};
     cudaStream_t st = (cudaStream_t)stream;

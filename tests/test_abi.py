@@ -316,6 +316,28 @@ def test_tail_super_chunks_hold_two_chunks(lib):
         assert p.tail_super_tokens % 256 == 0 and p.tail_n_super * p.tail_super_tokens >= seqlen
 
 
+def test_sizes_that_would_wrap_are_refused(lib):
+    """A problem whose arrays would need 2^62 bytes or more is refused (SSD_ERR_UNSUPPORTED)
+    before any size is formed: a wrapped workspace size would let the kernels write past a
+    buffer sized from it."""
+    n = ctypes.c_size_t(0)
+    huge = desc(batch=65535, seqlen=1 << 38, nheads=8, headdim=64, dstate=128, ngroups=1, chunk=256,
+                in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16)
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(huge), ctypes.byref(n)) == 2
+    assert lib.ssd_fwd_host_buffer_size(ctypes.byref(huge), ctypes.byref(n)) == 2
+    assert lib.ssd_bwd_workspace_size(ctypes.byref(huge), ctypes.byref(n)) == 2
+    p = _native.Plan()
+    assert lib.ssd_fwd_plan(ctypes.byref(huge), ctypes.byref(p)) == 2
+    s6 = _native.S6Desc(batch=65535, seqlen=1 << 40, dim=1 << 20, dstate=16, ngroups=1,
+                        in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16, flags=0, reserved=0)
+    fake = 1 << 20    # refused during validation, never dereferenced
+    assert lib.ssd_s6_fwd(ctypes.byref(s6), fake, fake, fake, fake, fake, None, None, fake, None, None) == 2
+    # a large but representable problem still gets a size
+    big = desc(batch=64, seqlen=1 << 20, nheads=8, headdim=64, dstate=128, ngroups=1, chunk=256,
+               in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16)
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(big), ctypes.byref(n)) == 0 and n.value > 0
+
+
 def test_host_buffer_size(lib):
     """ssd_fwd_host_buffer_size: host-side query; grows with the batch, covers the device path's
     workspace for one slice, and rejects what ssd_fwd rejects."""
