@@ -65,7 +65,8 @@ typedef enum {
     SSD_OK = 0,
     SSD_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, negative size, bad dtype, G does not divide nh */
     SSD_ERR_UNSUPPORTED = 2,  /* well-formed problem outside what this library handles (see limits below;
-                                 every entry point: arrays of 2^62 bytes or more, whose sizes could wrap) */
+                                 every entry point: arrays of 2^62 bytes or more, whose sizes could wrap;
+                                 B * nh of 2^31 or more) */
     SSD_ERR_WORKSPACE = 3,    /* workspace NULL, smaller than ssd_fwd_workspace_size, or not 256-B aligned */
     SSD_ERR_CUDA = 4,         /* a CUDA runtime call or a kernel launch failed; call cudaGetLastError */
     SSD_ERR_TOO_LARGE = 5,    /* ssd_fwd_noalloc: the problem needs more scratch than SSD_NOALLOC_SCRATCH_BYTES */

@@ -41,6 +41,8 @@ ssd_status check_desc(const ssd_desc *d, Problem *pr, bool need_seq)
     // grid-dimension limits of the launches (y and z are at most 65535)
     if (d->batch > 65535) return SSD_ERR_UNSUPPORTED;
     if (d->nheads * ((d->headdim + 31) / 32) * ((d->dstate + 63) / 64) > 65535) return SSD_ERR_UNSUPPORTED;
+    // sequence ((batch, head) pair) indices are 32-bit inside the kernels
+    if (d->batch * d->nheads > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
     pr->B = d->batch;
     pr->L = need_seq ? d->seqlen : 1;
     pr->nh = d->nheads;

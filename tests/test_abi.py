@@ -332,6 +332,9 @@ def test_sizes_that_would_wrap_are_refused(lib):
                         in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16, flags=0, reserved=0)
     fake = 1 << 20    # refused during validation, never dereferenced
     assert lib.ssd_s6_fwd(ctypes.byref(s6), fake, fake, fake, fake, fake, None, None, fake, None, None) == 2
+    # sequence indices are 32-bit in the kernels: B * nh of 2^31 or more is refused
+    many = desc(batch=65535, seqlen=1, nheads=65535, headdim=1, dstate=1, ngroups=1, chunk=1)
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(many), ctypes.byref(n)) == 2
     # a large but representable problem still gets a size
     big = desc(batch=64, seqlen=1 << 20, nheads=8, headdim=64, dstate=128, ngroups=1, chunk=256,
                in_dtype=_native.SSD_BF16, out_dtype=_native.SSD_BF16)
