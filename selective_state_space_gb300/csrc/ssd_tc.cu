@@ -1767,9 +1767,7 @@ bool tc_supported(const Problem &pr)
     if (pr.S != 128 && pr.S != 256) return false;
     if (pr.H != 64 && pr.H != 128) return false;
     if (pr.T % kQ != 0 || pr.T > 256) return false;
-    // TMA coordinates are 32-bit: token positions, and the prefetch two 128-token tiles ahead of
-    // them, stay below 2^31
-    if (pr.L > 0x7fffffffLL - 1024 || pr.B > 65535) return false;
+    if (pr.L > 0x7fffffffLL || pr.B > 65535) return false;
     return true;
 }
 
